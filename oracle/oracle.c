@@ -1,0 +1,341 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU reference for the online-softmax attention
+ * forward.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg load this library.  It shares no code, header, table or
+ * helper with the GPU path and includes nothing from it.
+ *
+ * Every routine below is the plain definition (or the pages' algorithm, step
+ * by step) written in fp64 with no blocking, fusion or reordering:
+ *
+ *   oracle_attention      three-pass safe softmax attention, S materialised
+ *                         per query row.  "Online Softmax 算法详解" section 2.1
+ *                         (the three passes), section 8.1 (LSE definition);
+ *                         masked-row convention from section 7.2/7.3.
+ *   oracle_online_blocks  the blockwise (m, l, O) recurrence with a caller
+ *                         chosen block partition and block order.
+ *                         "在线Softmax算法解析" section 3.2; "01 -- La
+ *                         recurrencia del online softmax", section "La
+ *                         recurrencia"; -inf reference point from
+ *                         "Online Softmax 算法详解" section 7.1.
+ *   oracle_merge          the two-block merge rule folded over P parts
+ *                         (airsota.com online-softmax card, section 三,
+ *                         "Running Combined Updates"; associativity per
+ *                         "La recurrencia del online softmax", practice 4).
+ *   oracle_softmax_two_pass
+ *                         Milakov & Gimelshein two-pass normaliser
+ *                         ("Online Softmax 算法详解" section 2.2).
+ *
+ * Causal convention (not fixed by the pages; the reading used throughout):
+ * key j is visible to query i iff j <= i + (nk - nq)  (bottom-right aligned).
+ *
+ * All routines are re-entrant.  oracle_attention splits its rows over
+ * `nthreads` POSIX threads (nthreads <= 0 means one thread).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Three-pass safe-softmax attention                                          */
+/* ------------------------------------------------------------------------ */
+
+/* One query row.  s is caller scratch of nk doubles. */
+static void attention_row(const double *qi, const double *k, const double *v,
+                          int64_t nk, int64_t d, double scale,
+                          int64_t last_visible, double *s, double *oi,
+                          double *lse_i)
+{
+    /* Materialise the score row S_j = scale * <q_i, k_j>; -inf where masked. */
+    for (int64_t j = 0; j < nk; ++j) {
+        if (j > last_visible) {
+            s[j] = -INFINITY;
+            continue;
+        }
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            acc += qi[c] * k[j * d + c];
+        s[j] = scale * acc;
+    }
+
+    /* Pass 1: m = max_j S_j. */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nk; ++j)
+        if (s[j] > m)
+            m = s[j];
+
+    /* A row with no visible key: O = 0 and LSE = -inf. */
+    if (m == -INFINITY) {
+        for (int64_t c = 0; c < d; ++c)
+            oi[c] = 0.0;
+        *lse_i = -INFINITY;
+        return;
+    }
+
+    /* Pass 2: l = sum_j exp(S_j - m). */
+    double l = 0.0;
+    for (int64_t j = 0; j < nk; ++j)
+        l += exp(s[j] - m);
+
+    /* Pass 3: P_j = exp(S_j - m) / l and O = sum_j P_j v_j. */
+    for (int64_t c = 0; c < d; ++c)
+        oi[c] = 0.0;
+    for (int64_t j = 0; j < nk; ++j) {
+        double p = exp(s[j] - m) / l;
+        for (int64_t c = 0; c < d; ++c)
+            oi[c] += p * v[j * d + c];
+    }
+
+    /* LSE = ln sum_j exp(S_j) = m + ln l. */
+    *lse_i = m + log(l);
+}
+
+typedef struct {
+    const double *q, *k, *v;
+    int64_t nq, nk, d;
+    double scale;
+    int causal;
+    const int64_t *rows;
+    int64_t row_begin, row_end;
+    double *o, *lse;
+    int status;
+} attention_job;
+
+static void *attention_worker(void *arg)
+{
+    attention_job *job = (attention_job *)arg;
+    double *s = (double *)malloc((size_t)(job->nk > 0 ? job->nk : 1) * sizeof(double));
+    if (!s) {
+        job->status = -1;
+        return NULL;
+    }
+    for (int64_t r = job->row_begin; r < job->row_end; ++r) {
+        int64_t i = job->rows ? job->rows[r] : r;
+        int64_t last_visible = job->causal ? i + (job->nk - job->nq) : job->nk - 1;
+        attention_row(job->q + i * job->d, job->k, job->v, job->nk, job->d,
+                      job->scale, last_visible, s, job->o + r * job->d,
+                      job->lse + r);
+    }
+    free(s);
+    job->status = 0;
+    return NULL;
+}
+
+/*
+ * q [nq][d], k [nk][d], v [nk][d] : one head, row-major fp64.
+ * rows[nrows] : query rows to compute (NULL: all nq rows, nrows must be nq).
+ * o [nrows][d], lse [nrows] : outputs, in the order of `rows`.
+ * Returns 0, or -1 on a bad argument / allocation failure.
+ */
+int oracle_attention(const double *q, int64_t nq, const double *k,
+                     const double *v, int64_t nk, int64_t d, double scale,
+                     int causal, const int64_t *rows, int64_t nrows,
+                     double *o, double *lse, int nthreads)
+{
+    if (!q || !k || !v || !o || !lse || nq < 0 || nk < 0 || d <= 0 || nrows < 0)
+        return -1;
+    if (!rows && nrows != nq)
+        return -1;
+    for (int64_t r = 0; rows && r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= nq)
+            return -1;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > nrows)
+        nthreads = nrows > 0 ? (int)nrows : 1;
+
+    attention_job *jobs = (attention_job *)calloc((size_t)nthreads, sizeof(attention_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) {
+        free(jobs);
+        free(tids);
+        return -1;
+    }
+    int64_t per = (nrows + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        attention_job *job = &jobs[t];
+        job->q = q; job->k = k; job->v = v;
+        job->nq = nq; job->nk = nk; job->d = d;
+        job->scale = scale; job->causal = causal;
+        job->rows = rows;
+        job->row_begin = (int64_t)t * per < nrows ? (int64_t)t * per : nrows;
+        job->row_end = job->row_begin + per < nrows ? job->row_begin + per : nrows;
+        job->o = o; job->lse = lse;
+        job->status = -1;
+    }
+    int rc = 0;
+    int *created = (int *)calloc((size_t)nthreads, sizeof(int));
+    if (!created) {
+        free(jobs);
+        free(tids);
+        return -1;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        if (nthreads > 1 && pthread_create(&tids[t], NULL, attention_worker, &jobs[t]) == 0)
+            created[t] = 1;
+        else
+            attention_worker(&jobs[t]); /* single thread, or no thread available */
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (created[t])
+            pthread_join(tids[t], NULL);
+    free(created);
+    for (int t = 0; t < nthreads; ++t)
+        if (jobs[t].status != 0)
+            rc = -1;
+    free(jobs);
+    free(tids);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The blockwise online recurrence, one row                                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * s[n] : the row's (already scaled) scores, -inf allowed.
+ * v[n][dv] : value rows.
+ * block_start[nb], block_len[nb] : the blocks, in processing order (any
+ *   order; together they should cover each index once).
+ * Outputs: *m_out, *l_out (running max and sum at the end), o_out[dv] = O/l
+ * (0 when l = 0), *lse_out = m + ln l (-inf when l = 0).
+ *
+ * State starts at m = -inf, l = 0, O = 0.  Per block:
+ *   m_blk = max of the block; m_new = max(m, m_blk)
+ *   ref   = m_new, or 0 when m_new is -inf (no NaN from -inf - -inf)
+ *   alpha = exp(m - ref); l <- alpha * l; O <- alpha * O
+ *   p_j   = exp(s_j - ref); l <- l + sum p_j; O <- O + sum p_j v_j
+ *   m     <- m_new
+ * Finally O <- O / l.
+ */
+int oracle_online_blocks(const double *s, const double *v, int64_t n,
+                         int64_t dv, const int64_t *block_start,
+                         const int64_t *block_len, int64_t nb,
+                         double *m_out, double *l_out, double *o_out,
+                         double *lse_out)
+{
+    if (!s || !v || !block_start || !block_len || !m_out || !l_out || !o_out ||
+        !lse_out || n < 0 || dv <= 0 || nb < 0)
+        return -1;
+    double m = -INFINITY, l = 0.0;
+    double *o = (double *)calloc((size_t)dv, sizeof(double));
+    if (!o)
+        return -1;
+
+    for (int64_t b = 0; b < nb; ++b) {
+        int64_t j0 = block_start[b], len = block_len[b];
+        if (j0 < 0 || len < 0 || j0 + len > n) {
+            free(o);
+            return -1;
+        }
+        double m_blk = -INFINITY;
+        for (int64_t j = j0; j < j0 + len; ++j)
+            if (s[j] > m_blk)
+                m_blk = s[j];
+        double m_new = m > m_blk ? m : m_blk;
+        double ref = (m_new == -INFINITY) ? 0.0 : m_new;
+        double alpha = exp(m - ref);
+        l = l * alpha;
+        for (int64_t c = 0; c < dv; ++c)
+            o[c] = o[c] * alpha;
+        for (int64_t j = j0; j < j0 + len; ++j) {
+            double p = exp(s[j] - ref);
+            l = l + p;
+            for (int64_t c = 0; c < dv; ++c)
+                o[c] = o[c] + p * v[j * dv + c];
+        }
+        m = m_new;
+    }
+
+    *m_out = m;
+    *l_out = l;
+    for (int64_t c = 0; c < dv; ++c)
+        o_out[c] = (l == 0.0) ? 0.0 : o[c] / l;
+    *lse_out = (l == 0.0) ? -INFINITY : m + log(l);
+    free(o);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The two-block merge rule, folded left over P parts                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Part p carries (m[p], l[p], o[p][dv]) with o normalised (O_p / l_p, or 0
+ * when l_p = 0).  Two parts combine as
+ *   m   = max(m1, m2)
+ *   l   = l1 exp(m1 - m) + l2 exp(m2 - m)
+ *   O   = O1 (l1 exp(m1 - m) / l) + O2 (l2 exp(m2 - m) / l)
+ * with an empty part (m = -inf, l = 0) contributing nothing.  The fold runs
+ * left to right; outputs are the merged (m, l, O) and LSE = m + ln l
+ * (-inf and O = 0 when every part is empty).
+ */
+int oracle_merge(const double *m, const double *l, const double *o,
+                 int64_t nparts, int64_t dv, double *m_out, double *l_out,
+                 double *o_out, double *lse_out)
+{
+    if (!m || !l || !o || !m_out || !l_out || !o_out || !lse_out || nparts < 1 || dv <= 0)
+        return -1;
+    double m1 = m[0], l1 = l[0];
+    for (int64_t c = 0; c < dv; ++c)
+        o_out[c] = o[c];
+    for (int64_t p = 1; p < nparts; ++p) {
+        double m2 = m[p], l2 = l[p];
+        const double *o2 = o + p * dv;
+        double mm = m1 > m2 ? m1 : m2;
+        if (mm == -INFINITY) { /* both sides empty so far */
+            m1 = -INFINITY;
+            l1 = 0.0;
+            for (int64_t c = 0; c < dv; ++c)
+                o_out[c] = 0.0;
+            continue;
+        }
+        double w1 = (m1 == -INFINITY) ? 0.0 : l1 * exp(m1 - mm);
+        double w2 = (m2 == -INFINITY) ? 0.0 : l2 * exp(m2 - mm);
+        double ll = w1 + w2;
+        for (int64_t c = 0; c < dv; ++c)
+            o_out[c] = (ll == 0.0) ? 0.0 : o_out[c] * (w1 / ll) + o2[c] * (w2 / ll);
+        m1 = mm;
+        l1 = ll;
+    }
+    if (l1 == 0.0) {
+        for (int64_t c = 0; c < dv; ++c)
+            o_out[c] = 0.0;
+    }
+    *m_out = m1;
+    *l_out = l1;
+    *lse_out = (l1 == 0.0) ? -INFINITY : m1 + log(l1);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Two-pass online normaliser                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Pass 1 fuses the max and the sum element by element:
+ *   m_new = max(m, x_i); l = exp(m - m_new) l + exp(x_i - m_new); m = m_new
+ * Pass 2: p_i = exp(x_i - m) / l.
+ * A row of all -inf yields p = 0 (the -inf reference point is replaced by 0,
+ * as in the blockwise recurrence).  Returns LSE = m + ln l in *lse_out.
+ */
+int oracle_softmax_two_pass(const double *x, int64_t n, double *p, double *lse_out)
+{
+    if (!x || !p || !lse_out || n < 0)
+        return -1;
+    double m = -INFINITY, l = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double m_new = m > x[i] ? m : x[i];
+        double ref = (m_new == -INFINITY) ? 0.0 : m_new;
+        l = exp(m - ref) * l + exp(x[i] - ref);
+        m = m_new;
+    }
+    double ref = (m == -INFINITY) ? 0.0 : m;
+    for (int64_t i = 0; i < n; ++i)
+        p[i] = (l == 0.0) ? 0.0 : exp(x[i] - ref) / l;
+    *lse_out = (l == 0.0) ? -INFINITY : m + log(l);
+    return 0;
+}

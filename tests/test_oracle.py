@@ -1,0 +1,330 @@
+"""Pins for the fp64 oracle, independent of the oracle itself.
+
+Each test checks the oracle against something the pages or mathematics fix:
+values printed for worked examples (tests/golden/worked_examples.json, each
+with its citation), closed forms, invariants the pages state, special cases
+that reduce to library routines (scipy.special.softmax / logsumexp), and the
+masked-row convention.  tests/test_oracle_mutants.py checks that plausible
+mistakes in oracle.c fail at least one of these pins.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special as sps
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")
+
+
+@pytest.fixture(scope="module")
+def golden():
+    with open(GOLDEN, encoding="utf-8") as f:
+        return json.load(f)
+
+
+def close(a, b, unit):
+    return abs(float(a) - float(b)) <= unit * (1 + 1e-9)
+
+
+def one_row_attention(scores, values, scale=1.0, causal=False):
+    """Feed a score row through the attention routine: q = e0, k_j = s_j e0."""
+    s = np.asarray(scores, dtype=np.float64)
+    v = np.asarray(values, dtype=np.float64)
+    if v.ndim == 1:
+        v = v[:, None]
+    n, dv = v.shape
+    d = max(dv, 1)
+    q = np.zeros((1, d))
+    q[0, 0] = 1.0
+    k = np.zeros((n, d))
+    k[:, 0] = s
+    vv = np.zeros((n, d))
+    vv[:, :dv] = v
+    o, lse = oracle.attention(q, k, vv, scale, causal)
+    return o[0, :dv], lse[0]
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_p1_no_rescale_example(golden):
+    g = golden["p1_no_rescale"]
+    s, blocks = g["scores"], [tuple(b) for b in g["blocks"]]
+    m1, l1, _, _ = oracle.online_blocks(s[:2], np.ones(2), [(0, 2)])
+    assert m1 == g["after_block_1"]["m"] and close(l1, g["after_block_1"]["l"], g["after_block_1"]["unit"])
+    for x, p in zip(s[2:], g["block_2_exps"]["values"]):
+        assert close(math.exp(x - m1), p, g["block_2_exps"]["unit"])
+    m, l, o, lse = oracle.online_blocks(s, np.ones(4), blocks)
+    assert m == g["final"]["m"] and close(l, g["final"]["l"], g["final"]["unit"])
+    assert abs(o[0] - 1.0) < 1e-15
+    # the same through the three-pass attention routine
+    o_att, lse_att = one_row_attention(s, np.ones(4))
+    assert abs(lse_att - lse) < 1e-13 and abs(lse - (m + math.log(l))) < 1e-15
+
+
+def test_p1_rescale_example(golden):
+    g = golden["p1_rescale"]
+    s, blocks = g["scores"], [tuple(b) for b in g["blocks"]]
+    m1, l1, _, _ = oracle.online_blocks(s[:2], np.ones(2), [(0, 2)])
+    assert m1 == g["after_block_1"]["m"] and close(l1, g["after_block_1"]["l"], g["after_block_1"]["unit"])
+    alpha = math.exp(m1 - 5.0)
+    assert close(alpha, g["second_block_scale"]["value"], g["second_block_scale"]["unit"])
+    assert close(l1 * alpha, g["scaled_l"]["value"], g["scaled_l"]["unit"])
+    m, l, _, _ = oracle.online_blocks(s, np.ones(4), blocks)
+    assert m == g["final"]["m"]
+    assert close(l, g["final"]["l"], g["final"]["unit"])
+    assert close(l, g["check_sum"]["total"], g["check_sum"]["unit"])
+    # the page's per-term check: exp(s_j - 5) for each score
+    for x, t in zip(s, [g["check_sum"]["terms"][i] for i in (0, 1, 2, 3)]):
+        assert close(math.exp(x - 5.0), t, g["check_sum"]["unit"])
+    # block order reversed gives the same state
+    m_r, l_r, _, _ = oracle.online_blocks(s, np.ones(4), blocks[::-1])
+    assert m_r == m and abs(l_r - l) < 1e-14
+
+
+def test_p4_large_jump_example(golden):
+    g = golden["p4_large_jump"]
+    s, v, blocks = g["scores"], g["values"], [tuple(b) for b in g["blocks"]]
+    m1, l1, o1, _ = oracle.online_blocks(s[:2], v[:2], [(0, 2)])
+    a1 = g["after_block_1"]
+    assert m1 == a1["m"] and close(l1, a1["l"], a1["unit"])
+    assert close(o1[0] * l1, a1["o_unnormalised"], a1["unit"])  # unnormalised O
+    for x, p in zip(s[:2], a1["p"]):
+        assert close(math.exp(x - m1), p, a1["unit"])
+    alpha = math.exp(m1 - 10.0)
+    assert close(alpha, g["alpha"]["value"], g["alpha"]["unit"])
+    assert close(alpha * l1, g["rescaled_l"]["value"], g["rescaled_l"]["unit"])
+    for x, p in zip(s[2:], g["p_2"]["values"]):
+        assert close(math.exp(x - 10.0), p, g["p_2"]["unit"])
+    m, l, o, _ = oracle.online_blocks(s, v, blocks)
+    assert m == g["final"]["m"] and close(l, g["final"]["l"], g["final"]["unit"])
+    assert abs(o[0] - g["final"]["o"]) < 1e-15
+    sa = g["softmax_all_at_once"]
+    p_att, _ = one_row_attention(s, np.eye(4))
+    for pv, ref, unit, garbled in zip(p_att, sa["values"], sa["units"], sa["garbled"]):
+        if garbled:
+            assert abs(pv - ref) <= sa["garbled_rel_tol"] * ref
+        else:
+            assert close(pv, ref, unit)
+
+
+def test_p1_overflow_row(golden):
+    g = golden["p1_overflow_row"]
+    s = np.array(g["scores"], dtype=np.float64)
+    p, lse = one_row_attention(s, np.eye(3))
+    assert np.all(np.isfinite(p)) and abs(p.sum() - 1.0) < 1e-15
+    # LSE from the page's printed exponentials, within their printed precision
+    lse_printed = math.log(sum(g["printed_exp"]))
+    assert abs(lse - lse_printed) <= g["printed_exp_rel_unit"]
+    # each P_j against the printed exp_j / sum(printed)
+    for pj, e in zip(p, g["printed_exp"]):
+        assert abs(pj - e / sum(g["printed_exp"])) <= 2 * g["printed_exp_rel_unit"] * pj
+    # fp64 exp overflows above ~709.78; the stable form must not
+    p2, lse2 = one_row_attention([1000.0, 1001.0], np.eye(2))
+    assert abs(p2[0] - 1 / (1 + math.e)) < 1e-15 and abs(p2[1] - math.e / (1 + math.e)) < 1e-15
+    assert abs(lse2 - (1001.0 + math.log1p(math.exp(-1.0)))) < 1e-12
+
+
+def test_p4_practice_1_closed_form():
+    # s = [0] then [5], V = [[2],[3]].  Closed form: O = (2 e^-5 + 3) / (1 + e^-5),
+    # l = 1 + e^-5 relative to m = 5.
+    m, l, o, lse = oracle.online_blocks([0.0, 5.0], [[2.0], [3.0]], [(0, 1), (1, 1)])
+    e5 = math.exp(-5.0)
+    assert m == 5.0 and abs(l - (1 + e5)) < 1e-15
+    assert abs(o[0] - (2 * e5 + 3) / (1 + e5)) < 1e-15
+    assert abs(lse - (5 + math.log1p(e5))) < 1e-15
+
+
+def test_first_block_from_minus_inf():
+    # Starting state m = -inf, l = 0: the first block's scale exp(-inf - m') is 0
+    # and no NaN appears, also when a whole block is -inf.
+    ninf = -math.inf
+    s = [ninf, ninf, 1.0, 2.0]
+    m, l, o, lse = oracle.online_blocks(s, np.eye(4), [(0, 2), (2, 2)])
+    assert m == 2.0 and abs(l - (1 + math.exp(-1))) < 1e-15
+    assert np.all(np.isfinite(o)) and o[0] == 0.0 and o[1] == 0.0
+    m, l, o, lse = oracle.online_blocks([ninf, ninf], np.eye(2), [(0, 1), (1, 1)])
+    assert m == ninf and l == 0.0 and np.all(o == 0.0) and lse == ninf
+
+
+# ------------------------------------------------------- library special cases
+
+@pytest.mark.parametrize("nq,nk,d,causal,seed", [
+    (5, 7, 3, False, 0), (7, 7, 4, True, 1), (4, 9, 2, True, 2),
+    (9, 4, 3, True, 3), (1, 1, 5, False, 4), (3, 16, 8, False, 5),
+])
+def test_attention_matches_scipy_softmax(nq, nk, d, causal, seed):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((nq, d)) * 2
+    k = rng.standard_normal((nk, d))
+    v = rng.standard_normal((nk, d))
+    scale = 1 / math.sqrt(d)
+    o, lse = oracle.attention(q, k, v, scale, causal)
+    S = scale * (q @ k.T)
+    if causal:
+        ii = np.arange(nq)[:, None]
+        jj = np.arange(nk)[None, :]
+        S = np.where(jj <= ii + (nk - nq), S, -np.inf)
+    for i in range(nq):
+        if np.all(np.isneginf(S[i])):
+            assert np.all(o[i] == 0.0) and lse[i] == -np.inf
+            continue
+        p = sps.softmax(S[i])
+        np.testing.assert_allclose(o[i], p @ v, rtol=1e-12, atol=1e-13)
+        assert abs(lse[i] - sps.logsumexp(S[i])) < 1e-12
+
+
+def test_rows_subset_and_threads_agree():
+    rng = np.random.default_rng(7)
+    q, k, v = (rng.standard_normal((33, 16)) for _ in range(3))
+    o_all, l_all = oracle.attention(q, k, v, 0.25, True, threads=1)
+    rows = [32, 0, 5, 5, 17]
+    o_sub, l_sub = oracle.attention(q, k, v, 0.25, True, rows=rows, threads=3)
+    np.testing.assert_array_equal(o_sub, o_all[rows])
+    np.testing.assert_array_equal(l_sub, l_all[rows])
+
+
+def test_two_pass_softmax_matches_scipy():
+    rng = np.random.default_rng(3)
+    for n in (1, 2, 17, 300):
+        x = rng.standard_normal(n) * 30
+        p, lse = oracle.softmax_two_pass(x)
+        np.testing.assert_allclose(p, sps.softmax(x), rtol=1e-12, atol=1e-300)
+        assert abs(lse - sps.logsumexp(x)) < 1e-12
+    p, lse = oracle.softmax_two_pass([-math.inf] * 3)
+    assert np.all(p == 0) and lse == -math.inf
+
+
+# ------------------------------------------------------------- closed forms
+
+def test_single_key():
+    # Nk = 1: O = v_0 and LSE = scale * <q, k_0>.
+    rng = np.random.default_rng(11)
+    q, k, v = rng.standard_normal((4, 6)), rng.standard_normal((1, 6)), rng.standard_normal((1, 6))
+    o, lse = oracle.attention(q, k, v, 0.5, False)
+    np.testing.assert_array_equal(o, np.repeat(v, 4, axis=0))
+    np.testing.assert_allclose(lse, 0.5 * (q @ k[0]), rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_queries_average_visible_values(causal):
+    # Q = 0: P is uniform over the visible keys, O = their mean, LSE = ln(count).
+    rng = np.random.default_rng(12)
+    nq, nk, d = 6, 10, 4
+    q = np.zeros((nq, d))
+    k, v = rng.standard_normal((nk, d)), rng.standard_normal((nk, d))
+    o, lse = oracle.attention(q, k, v, 0.3, causal)
+    for i in range(nq):
+        cnt = (i + nk - nq + 1) if causal else nk
+        np.testing.assert_allclose(o[i], v[:cnt].mean(axis=0), rtol=1e-13, atol=1e-14)
+        assert abs(lse[i] - math.log(cnt)) < 1e-14
+
+
+def test_rows_of_p_sum_to_one_and_constant_values():
+    # V = identity gives O = P (rows sum to 1); V = 1 gives O = 1.
+    rng = np.random.default_rng(13)
+    nk = 12
+    q, k = rng.standard_normal((5, nk)) * 3, rng.standard_normal((nk, nk))
+    o, _ = oracle.attention(q, k, np.eye(nk), 1.0, False)
+    np.testing.assert_allclose(o.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    assert np.all(o > 0)
+    o1, _ = oracle.attention(q, k, np.ones((nk, nk)), 1.0, True)
+    np.testing.assert_allclose(o1, 1.0, rtol=0, atol=1e-14)
+
+
+def test_shift_invariance():
+    # Adding c to a row's logits (extra feature: q' = [q, c/scale], k' = [k, 1])
+    # leaves O unchanged and shifts LSE by c.
+    rng = np.random.default_rng(14)
+    nq, nk, d, scale, c = 4, 9, 5, 0.7, 3.25
+    q, k, v = rng.standard_normal((nq, d)), rng.standard_normal((nk, d)), rng.standard_normal((nk, d))
+    o, lse = oracle.attention(q, k, v, scale, False)
+    q2 = np.concatenate([q, np.full((nq, 1), c / scale)], axis=1)
+    k2 = np.concatenate([k, np.ones((nk, 1))], axis=1)
+    v2 = np.concatenate([v, np.zeros((nk, 1))], axis=1)
+    o2, lse2 = oracle.attention(q2, k2, v2, scale, False)
+    np.testing.assert_allclose(o2[:, :d], o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse + c, rtol=0, atol=1e-12)
+
+
+def test_fully_masked_rows():
+    # Causal with nq > nk: rows i < nq - nk see no key: O = 0 exactly, LSE = -inf.
+    rng = np.random.default_rng(15)
+    nq, nk, d = 8, 3, 4
+    q, k, v = rng.standard_normal((nq, d)), rng.standard_normal((nk, d)), rng.standard_normal((nk, d))
+    o, lse = oracle.attention(q, k, v, 1.0, True)
+    for i in range(nq - nk):
+        assert np.all(o[i] == 0.0) and lse[i] == -np.inf
+    for i in range(nq - nk, nq):
+        assert np.all(np.isfinite(o[i])) and np.isfinite(lse[i])
+    # first visible row sees exactly key 0
+    np.testing.assert_array_equal(o[nq - nk], v[0])
+
+
+# ------------------------------------- block size / order independence, merge
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_online_blocks_match_three_pass(seed):
+    rng = np.random.default_rng(100 + seed)
+    nk, d = 130, 5
+    q = rng.standard_normal((1, d)) * 4
+    k, v = rng.standard_normal((nk, d)), rng.standard_normal((nk, d))
+    scale = 0.9
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, False)
+    s = scale * (k @ q[0])
+    for bc in (1, 2, 3, 64, 128, nk):
+        blocks = [(j, min(bc, nk - j)) for j in range(0, nk, bc)]
+        for order in range(3):
+            bl = list(blocks)
+            if order == 1:
+                bl = bl[::-1]
+            elif order == 2:
+                rng.shuffle(bl)
+            m, l, o, lse = oracle.online_blocks(s, v, bl)
+            assert m == s.max()
+            np.testing.assert_allclose(o, o_ref[0], rtol=1e-12, atol=1e-12)
+            assert abs(lse - lse_ref[0]) < 1e-12
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_merge_of_random_partition_matches_full(seed):
+    rng = np.random.default_rng(200 + seed)
+    n, dv = 97, 6
+    s = rng.standard_normal(n) * 5
+    v = rng.standard_normal((n, dv))
+    _, _, o_ref, lse_ref = oracle.online_blocks(s, v, [(0, n)])
+    cuts = np.sort(rng.choice(np.arange(1, n), size=6, replace=False))
+    edges = [0, *cuts.tolist(), n]
+    parts = [(edges[i], edges[i + 1] - edges[i]) for i in range(len(edges) - 1)]
+    parts.append((n, 0))  # an empty part must contribute nothing
+    ms, ls, os_ = [], [], []
+    for (j0, ln) in parts:
+        m, l, o, _ = oracle.online_blocks(s, v, [(j0, ln)])
+        ms.append(m); ls.append(l); os_.append(o)
+    for perm in (list(range(len(parts))), list(range(len(parts)))[::-1], rng.permutation(len(parts)).tolist()):
+        m, l, o, lse = oracle.merge([ms[p] for p in perm], [ls[p] for p in perm], [os_[p] for p in perm])
+        np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-13)
+        assert abs(lse - lse_ref) < 1e-12 and m == s.max()
+    # all parts empty -> O = 0, LSE = -inf
+    m, l, o, lse = oracle.merge([-math.inf] * 3, [0.0] * 3, np.zeros((3, dv)))
+    assert m == -math.inf and l == 0.0 and np.all(o == 0.0) and lse == -math.inf
+
+
+def test_merge_two_blocks_closed_form():
+    # The two-block rule on s = [0 | 5], V = [2 | 3] reproduces practice problem 1.
+    e5 = math.exp(-5.0)
+    m, l, o, lse = oracle.merge([0.0, 5.0], [1.0, 1.0], [[2.0], [3.0]])
+    assert m == 5.0 and abs(l - (1 + e5)) < 1e-15
+    assert abs(o[0] - (2 * e5 + 3) / (1 + e5)) < 1e-15
+
+
+def test_alpha_at_most_one_and_exp_args_nonpositive():
+    # The running max never decreases, so every rescale factor is <= 1 and every
+    # exponent argument s_j - m is <= 0: the unnormalised l stays <= block count.
+    rng = np.random.default_rng(16)
+    s = rng.standard_normal(200) * 20
+    m, l, _, _ = oracle.online_blocks(s, np.ones(200), [(j, 10) for j in range(0, 200, 10)])
+    assert 1.0 <= l <= 200.0 and m == s.max()
