@@ -1,0 +1,477 @@
+"""Benchmark of the single-pass online-softmax attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline] [--no-e2e]
+
+One step = one fa_fwd call (the whole hot path: QK^T, online softmax, PV,
+finalize; for split-KV workloads also the merge) over the workload's inputs.
+Default workload: non-causal B=2 H=32 Nq=Nk=4096 d=128, Q x4 (the
+configuration the tensor-peak target is quoted on).  Inputs (Q+K+V = 201 MB)
+exceed the 129 MB L2 and the L2 is also flushed (a 512 MB write) before every
+timed step; the flush is outside the step's CUDA-event pair.
+
+Prints ONE JSON line (rank 0).  Multi-GPU (torchrun): replicas only, each
+rank runs the same workload on its own GPU; value = sum over ranks of the
+work / max over ranks of the time.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+row sample of the same workload (there is no other implementation to run).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from online_softmax_sm_gb300 import workloads  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and % of dense BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD_ALIASES = {"c1": workloads.C1, "c2": workloads.C2, "c3": workloads.C3, "c4": workloads.C4,
+                    "c4_masked": workloads.C4_MASKED, "c5": workloads.C5}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def workload_of(name: str) -> workloads.Workload:
+    if name in WORKLOAD_ALIASES:
+        return WORKLOAD_ALIASES[name]
+    if name in workloads.WORKLOADS:
+        return workloads.WORKLOADS[name]
+    raise SystemExit(f"unknown workload {name}")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "online_softmax_sm_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None if absent or taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload_name)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.device_index = device_index
+        self.thread = None
+
+    def start(self):
+        ident = None
+        try:
+            props = torch.cuda.get_device_properties(self.device_index)
+            ident = "GPU-" + str(props.uuid)
+        except Exception:
+            ident = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if ident:
+            cmd += ["-i", ident]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)  # let the first samples arrive before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = None
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = [p for (t, p) in sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]]
+            note = "timed region shorter than the 50 ms sampling period; nearest samples"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        smax = [num(p[2]) for p in inside if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in inside:
+            for nm, val in zip(names, p[5:9]):
+                if val.strip().lower() in ("active", "1"):
+                    reasons.add(nm)
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None,
+               "reasons": sorted(reasons), "samples": len(inside),
+               "power_w_max": max([num(p[3]) for p in inside if num(p[3]) is not None], default=None)}
+        if note:
+            out["note"] = note
+        return out
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_oracle_sample(w: workloads.Workload, q, k, v, target_s: float, seed: int = 0):
+    """Time the oracle on a bounded row sample of the workload; returns a dict."""
+    import numpy as np
+
+    import oracle
+
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(seed)
+    B, H = w.B, w.H
+    # per-row cost: 4*Nk_visible*d; calibrate on a small sample first
+    head = (0, 0)
+    qh, kh, vh = (x[head[0], head[1]].cpu().double().numpy() for x in (q, k, v))
+
+    def row_flops(rows):
+        if not w.causal:
+            return 4.0 * w.Nk * w.d * len(rows)
+        off = w.Nk - w.Nq
+        return float(sum(4.0 * max(0, min(w.Nk, r + off + 1)) * w.d for r in rows))
+
+    calib_rows = sorted(rng.choice(w.Nq, size=min(w.Nq, 256), replace=False).tolist())
+    t0 = time.perf_counter()
+    oracle.attention(qh, kh, vh, w.scale, w.causal, rows=calib_rows, threads=threads)
+    dt = time.perf_counter() - t0
+    rate = row_flops(calib_rows) / max(dt, 1e-9)
+    want_flops = rate * target_s
+    total_rows = B * H * w.Nq
+    avg_row = w.flops / total_rows
+    n_rows = int(min(total_rows, max(256, want_flops / avg_row)))
+    # whole heads first, then a partial head
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    rng.shuffle(heads)
+    plan = []
+    left = n_rows
+    for (b, h) in heads:
+        if left <= 0:
+            break
+        take = min(left, w.Nq)
+        rows = None if take == w.Nq else sorted(rng.choice(w.Nq, size=take, replace=False).tolist())
+        plan.append(((b, h), rows))
+        left -= take
+    flops = 0.0
+    elapsed = 0.0  # oracle time only (bf16 -> fp64 conversion excluded)
+    for (b, h), rows in plan:
+        qh, kh, vh = (x[b, h].cpu().double().numpy() for x in (q, k, v))
+        rr = rows if rows is not None else list(range(w.Nq))
+        ts = time.perf_counter()
+        oracle.attention(qh, kh, vh, w.scale, w.causal, rows=rows, threads=threads)
+        elapsed += time.perf_counter() - ts
+        flops += row_flops(rr)
+    return {"tflops": flops / elapsed / 1e12, "seconds": elapsed, "rows": n_rows,
+            "heads": len(plan), "threads": threads, "flops": flops}
+
+
+def run_reference(args, w):
+    world, rank, local = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+
+    threads = oracle.default_threads()
+    q, k, v = workloads.generate(w, device="cpu")
+    rng = np.random.default_rng(1)
+    per_step_s = 3.0
+    # calibrate rows per step
+    qh, kh, vh = (x[0, 0].double().numpy() for x in (q, k, v))
+    rows = sorted(rng.choice(w.Nq, size=min(w.Nq, 128), replace=False).tolist())
+    t0 = time.perf_counter()
+    oracle.attention(qh, kh, vh, w.scale, w.causal, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    avg_row = w.flops / (w.B * w.H * w.Nq)
+    rows_per_step = int(max(32, min(w.Nq, len(rows) * per_step_s / max(dt, 1e-9))))
+    heads_np = {}
+
+    def step(i):
+        b = (i // w.H) % w.B
+        h = i % w.H
+        if (b, h) not in heads_np:
+            heads_np[(b, h)] = tuple(x[b, h].double().numpy() for x in (q, k, v))
+        qh, kh, vh = heads_np[(b, h)]
+        rr = sorted(rng.choice(w.Nq, size=rows_per_step, replace=False).tolist())
+        oracle.attention(qh, kh, vh, w.scale, w.causal, rows=rr, threads=threads)
+        return rr
+
+    for i in range(args.warmup):
+        step(i)
+    times, flops = [], 0.0
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        rr = step(args.warmup + i)
+        times.append(time.perf_counter() - t0)
+        if w.causal:
+            off = w.Nk - w.Nq
+            flops += sum(4.0 * max(0, min(w.Nk, r + off + 1)) * w.d for r in rr)
+        else:
+            flops += 4.0 * w.Nk * w.d * len(rr)
+    total = sum(times)
+    value = flops / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **{kk: vv for kk, vv in w.describe().items() if kk != "name"}},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_per_step} seeded query rows per step, one head per step "
+                                   f"(avg {avg_row:.3g} FLOP per row), fp64 three-pass oracle"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import online_softmax_sm_gb300 as fa
+
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    fa.lib()
+
+    q, k, v = workloads.generate(w, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    launches_per_step = 1 if w.n_splits <= 1 else 2
+
+    def step():
+        fa.fwd(q, k, v, w.scale, w.causal, w.n_splits, out=o, lse=lse, bc=w.bc)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.device_status(dev) != fa.FA_OK:
+        raise SystemExit("device status reports a timed-out wait")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_region0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_region1 = time.time()
+    barrier(world)
+    sampler.stop()
+    if fa.device_status(dev) != fa.FA_OK:
+        raise SystemExit("device status reports a timed-out wait")
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_local = statistics.mean(step_ms)
+    ms = max_over_ranks(ms_local, world, dev)
+    value = world * w.flops / (ms * 1e-3) / 1e12
+
+    # ---- dominant kernel: the forward kernel (split: time it alone via fa_fwd_partial)
+    peaks, peak_src = load_peaks()
+    if w.n_splits > 1:
+        m_p = torch.empty((w.n_splits, w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+        l_p = torch.empty_like(m_p)
+        o_p = torch.empty((w.n_splits, w.B, w.H, w.Nq, w.d), dtype=torch.float32, device=dev)
+        kt = []
+        for i in range(max(10, min(args.steps, 50))):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fa.fwd_partial(q, k, v, w.n_splits, w.scale, w.causal, m_p, l_p, o_p)
+            b.record(stream)
+            kt.append((a, b))
+        torch.cuda.synchronize(dev)
+        k_ms = statistics.mean(a.elapsed_time(b) for a, b in kt)
+        kern_bytes = (w.B * w.H * w.Nq * w.d + 2 * w.B * w.H * w.Nk * w.d) * 2
+        achieved = kern_bytes / (k_ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                    "kernel": "fa_fwd_kernel<128,128,1> (split partials)", "kernel_ms": k_ms,
+                    "algorithmic_bytes_per_launch": kern_bytes, "peak_source": peak_src + " hbm_gbs"}
+        del m_p, l_p, o_p
+    else:
+        achieved = w.flops / (ms_local * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                    "kernel": "fa_fwd_kernel", "kernel_ms": ms_local,
+                    "algorithmic_flops_per_launch": w.flops,
+                    "peak_source": peak_src + " bf16_tflops (burst: one launch timed alone)"}
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        n_e2e = max(5, min(args.steps, 30))
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            fa.fwd(dq, dk, dv, w.scale, w.causal, w.n_splits, out=o, lse=lse, bc=w.bc)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        tt = []
+        for _ in range(n_e2e):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            tt.append((a, b))
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in tt), world, dev)
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        e2e = {"value": world * w.flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+        del dq, dk, dv
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s = cpu_oracle_sample(w, q, k, v, args.cpu_seconds)
+        cpu = {"value": s["tflops"], "unit": "TFLOPS", "cores": s["threads"], "kind": "oracle",
+               "sample": f"{s['rows']} seeded query rows over {s['heads']} heads of this workload "
+                         f"({s['flops']:.3g} FLOP, {s['seconds']:.1f} s), fp64 three-pass oracle"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                       "causal": w.causal, "n_splits": w.n_splits, "scale": w.scale,
+                       "q_mult": w.q_mult, "k_ramp": w.k_ramp, "seed": w.seed,
+                       "l2": "flushed before every timed step (512 MB write); inputs > L2",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "tensor_peak_frac": value / world / float(peaks["bf16_tflops"])},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": sampler.summary(t_region0, t_region1),
+            "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = workload_of(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

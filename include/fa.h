@@ -1,0 +1,148 @@
+/*
+ * fa.h -- C ABI of the single-pass online-softmax attention forward for
+ * NVIDIA GB300 (sm_103a).  Library: libfa.so.
+ *
+ * Operation (all entry points): for each batch b, head h and query row i,
+ *
+ *   S_ij  = scale * <q[b,h,i,:], k[b,h,j,:]>      (-inf where masked)
+ *   O_i   = sum_j softmax_j(S_i) v[b,h,j,:]
+ *   LSE_i = ln sum_j exp(S_ij)                     (natural log)
+ *
+ * computed in one pass over K/V tiles with the online-softmax recurrence
+ * (running max m, running sum l, rescaled accumulator O, one division by l at
+ * the end): "Online Softmax 算法详解" (inference.lei6393.com) sections 2.3, 3.2,
+ * 4.7 and 8.1; "在线Softmax算法解析：FlashAttention核心技术" (intelliparadigm.com)
+ * section 3.2; "01 -- La recurrencia del online softmax" (lynx-cortex.pages.dev),
+ * section "La recurrencia".
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, row-major, in device memory (cudaMalloc / caching
+ *     allocator memory of the current device).  The caller owns every buffer;
+ *     the library keeps no pointer after the call returns.
+ *   - q, k, v, o: bf16 [B][H][N][d] with N = Nq for q/o and Nk for k/v;
+ *     base addresses 16-byte aligned.  lse: fp32 [B][H][Nq].
+ *   - d in {64, 128}; 1 <= Nq, Nk <= 2^30; B*H <= 65535; scale finite and > 0
+ *     (the usual value is 1/sqrt(d)).
+ *   - causal != 0: key j is visible to query i iff j <= i + (Nk - Nq)
+ *     (bottom-right alignment; equal to j <= i when Nq == Nk).  A query row
+ *     that sees no key gets O = 0 and LSE = -inf ("Online Softmax 算法详解"
+ *     sections 7.2-7.3).
+ *   - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls are asynchronous on it; buffers must stay valid until the work
+ *     on `stream` completes.  The calling thread's current device must be the
+ *     device that owns the buffers and the stream.
+ *   - Return value: FA_OK (0), or a negative FA_ERR_* code.  Argument errors
+ *     are detected before anything is launched; on error nothing is written.
+ *     The library never aborts the process and never traps on the device.
+ *   - Device-side timeouts: every wait inside the kernels is bounded.  A wait
+ *     that runs out stops its CTA cleanly (outputs of that CTA are left
+ *     unwritten) and records FA_ERR_DEVICE_TIMEOUT, which
+ *     fa_get_device_status() reports.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_OK 0
+#define FA_ERR_INVALID_ARG (-1)    /* null/misaligned pointer, bad size, bad scale */
+#define FA_ERR_UNSUPPORTED (-2)    /* d not in {64,128}, or device is not sm_103 */
+#define FA_ERR_CUDA (-3)           /* a CUDA call failed; fa_strerror() has details */
+#define FA_ERR_DEVICE_TIMEOUT (-4) /* a kernel wait ran out (fa_get_device_status) */
+#define FA_ERR_NO_MEMORY (-5)      /* the split-KV workspace could not be allocated */
+
+/*
+ * Attention forward, O and LSE.
+ *
+ * n_splits == 1: one kernel, each CTA walks the whole key axis and writes O
+ *   (bf16) and LSE (fp32) directly.
+ * n_splits  > 1: split-KV.  The key axis is cut into n_splits contiguous
+ *   ranges of K/V tiles (clamped to the number of 128-key tiles); each range
+ *   yields a partial (m, l, O) triple per row, combined by the two-block merge
+ *   rule (see fa_merge_splits).  The fp32 workspace for the partials is taken
+ *   with cudaMallocAsync on `stream` and released with cudaFreeAsync on the
+ *   same stream (FA_ERR_NO_MEMORY if that fails).
+ *
+ * q, k, v : in,  bf16 [B][H][Nq|Nk][d]
+ * o       : out, bf16 [B][H][Nq][d]
+ * lse     : out, fp32 [B][H][Nq], natural-log units of the scaled logits:
+ *           LSE_i = scale*m_i + ln l_i ("Online Softmax 算法详解" section 8.2).
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+           int Nk, int d, float scale, int causal, int n_splits, void* stream);
+
+/* Options for fa_fwd_ex.  Zero-initialise, then set what you need. */
+typedef struct fa_opts {
+  int bc;                     /* K/V tile rows: 0 = default (128), or 64 or 128 */
+  int q_tiles_per_cta;        /* 0 = automatic (2 when Nq > 128), or 1 or 2 */
+  unsigned long long timeout_ns; /* bound of each device-side wait; 0 = 4 s */
+  int test_skip_kv_load;      /* test hook: 0 = off; n > 0 makes the producer
+                                 of every CTA skip its n-th K/V tile load, so
+                                 the consumer's wait runs out and the call
+                                 reports FA_ERR_DEVICE_TIMEOUT */
+} fa_opts;
+
+/* fa_fwd with options; opts may be NULL (same as fa_fwd). */
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Nq, int Nk, int d, float scale, int causal, int n_splits, void* stream,
+              const fa_opts* opts);
+
+/*
+ * Split-KV forward without the merge: writes the n_splits partial triples
+ * ("the partial (m^(i), l^(i), O^(i))" of the two-block merge rule, airsota.com
+ * online-softmax card, section 三).  Split s covers K/V tiles
+ * [s*T', min(T, (s+1)*T')) with T = ceil(Nk/128) and T' = ceil(T/n_splits);
+ * a split with no visible key yields m = -inf, l = 0, O = 0.
+ *
+ * m_part : out, fp32 [n_splits][B][H][Nq]   m_s = scale * (raw max), natural-log units
+ * l_part : out, fp32 [n_splits][B][H][Nq]   l_s = sum_j exp(scale*S_ij - m_s)
+ * o_part : out, fp32 [n_splits][B][H][Nq][d] O_s / l_s; 16-byte aligned
+ * 1 <= n_splits <= 65535.
+ */
+int fa_fwd_partial(const void* q, const void* k, const void* v, float* m_part, float* l_part,
+                   float* o_part, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                   int n_splits, void* stream);
+
+/*
+ * Merge n_splits partial triples per row with the two-block merge rule
+ * (airsota.com online-softmax card, section 三, "Running Combined Updates"),
+ * in its n-way form (associative: "La recurrencia del online softmax",
+ * practice problem 4):
+ *   M = max_s m_s;  w_s = l_s exp(m_s - M);  l = sum_s w_s;
+ *   O = sum_s w_s O_s / l;  LSE = M + ln l;  l = 0 -> O = 0, LSE = -inf.
+ *
+ * m_part, l_part : in, fp32 [n_splits][B][H][Nq] (layout of fa_fwd_partial)
+ * o_part         : in, fp32 [n_splits][B][H][Nq][d], 16-byte aligned
+ * o              : out, bf16 [B][H][Nq][d], 16-byte aligned
+ * lse            : out, fp32 [B][H][Nq]
+ */
+int fa_merge_splits(const float* m_part, const float* l_part, const float* o_part, void* o,
+                    float* lse, int B, int H, int Nq, int d, int n_splits, void* stream);
+
+/* Bytes of fp32 workspace fa_fwd takes for split-KV with these sizes
+ * (0 for n_splits <= 1 or invalid sizes). */
+size_t fa_split_workspace_bytes(int B, int H, int Nq, int d, int n_splits);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT if any kernel of this library
+ * recorded a timed-out wait since the last call, or FA_ERR_CUDA.
+ */
+int fa_get_device_status(void* stream);
+
+/* Static description of an FA_* code; for FA_ERR_CUDA, the text of the last
+ * CUDA error seen by this thread.  Never NULL. */
+const char* fa_strerror(int code);
+
+/* Library ABI version (major * 100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

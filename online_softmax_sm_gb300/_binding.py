@@ -1,0 +1,193 @@
+"""ctypes binding of libfa.so (include/fa.h).
+
+Argument marshalling only: every step of the attention forward runs in the
+library's CUDA kernels.  torch supplies device memory and the current stream.
+If libfa.so is missing, every call raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "fa.h")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_CUDA = -3
+FA_ERR_DEVICE_TIMEOUT = -4
+FA_ERR_NO_MEMORY = -5
+
+
+class FaOpts(ctypes.Structure):
+    _fields_ = [("bc", ctypes.c_int), ("q_tiles_per_cta", ctypes.c_int),
+                ("timeout_ns", ctypes.c_ulonglong), ("test_skip_kv_load", ctypes.c_int)]
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} (code {code})")
+        self.code = code
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_fp = ctypes.POINTER(ctypes.c_float)
+_i = ctypes.c_int
+
+
+def _declare(L):
+    L.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp]
+    L.fa_fwd.restype = _i
+    L.fa_fwd_ex.argtypes = L.fa_fwd.argtypes + [ctypes.POINTER(FaOpts)]
+    L.fa_fwd_ex.restype = _i
+    L.fa_fwd_partial.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float,
+                                 _i, _i, _vp]
+    L.fa_fwd_partial.restype = _i
+    L.fa_merge_splits.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]
+    L.fa_merge_splits.restype = _i
+    L.fa_split_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+    L.fa_split_workspace_bytes.restype = ctypes.c_size_t
+    L.fa_get_device_status.argtypes = [_vp]
+    L.fa_get_device_status.restype = _i
+    L.fa_strerror.argtypes = [_i]
+    L.fa_strerror.restype = ctypes.c_char_p
+    L.fa_version.argtypes = []
+    L.fa_version.restype = _i
+
+
+def lib():
+    """The loaded libfa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; run `python -m online_softmax_sm_gb300.build` "
+                "(or __graft_entry__.build()).  There is no fallback implementation.")
+        L = ctypes.CDLL(LIB_PATH)
+        _declare(L)
+        _lib = L
+    return _lib
+
+
+def declared_symbols(header: str = HEADER) -> list[str]:
+    """Function names declared in include/fa.h."""
+    with open(header, encoding="utf-8") as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", text, re.M)))
+
+
+def strerror(code: int) -> str:
+    return lib().fa_strerror(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != FA_OK:
+        raise FAError(rc, what)
+
+
+def _stream_handle(dev: torch.device, stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    return s.cuda_stream
+
+
+def _check_qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    B, H, Nq, d = q.shape
+    if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError("k and v must be [B, H, Nk, d] matching q")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
+    return B, H, Nq, k.shape[2], d
+
+
+def fwd(q, k, v, scale: float | None = None, causal: bool = False, n_splits: int = 1,
+        out=None, lse=None, bc: int = 0, q_tiles_per_cta: int = 0, timeout_ns: int = 0,
+        test_skip_kv_load: int = 0, stream=None):
+    """fa_fwd / fa_fwd_ex.  Returns (o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq])."""
+    B, H, Nq, Nk, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    assert out.shape == q.shape and out.dtype == torch.bfloat16 and out.is_contiguous()
+    assert lse.shape == (B, H, Nq) and lse.dtype == torch.float32 and lse.is_contiguous()
+    L = lib()
+    with torch.cuda.device(q.device):
+        sh = _stream_handle(q.device, stream)
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                B, H, Nq, Nk, d, float(scale), int(bool(causal)), int(n_splits), sh)
+        if bc or q_tiles_per_cta or timeout_ns or test_skip_kv_load:
+            opts = FaOpts(int(bc), int(q_tiles_per_cta), int(timeout_ns), int(test_skip_kv_load))
+            rc = L.fa_fwd_ex(*args, ctypes.byref(opts))
+        else:
+            rc = L.fa_fwd(*args)
+    _check(rc, "fa_fwd")
+    return out, lse
+
+
+def fwd_partial(q, k, v, n_splits: int, scale: float | None = None, causal: bool = False,
+                m_part=None, l_part=None, o_part=None, stream=None):
+    """fa_fwd_partial.  Returns (m_part [S,B,H,Nq], l_part [S,B,H,Nq], o_part [S,B,H,Nq,d])."""
+    B, H, Nq, Nk, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = d ** -0.5
+    dev = q.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    m_part = torch.empty((n_splits, B, H, Nq), **f32) if m_part is None else m_part
+    l_part = torch.empty((n_splits, B, H, Nq), **f32) if l_part is None else l_part
+    o_part = torch.empty((n_splits, B, H, Nq, d), **f32) if o_part is None else o_part
+    L = lib()
+    with torch.cuda.device(dev):
+        rc = L.fa_fwd_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), m_part.data_ptr(),
+                              l_part.data_ptr(), o_part.data_ptr(), B, H, Nq, Nk, d, float(scale),
+                              int(bool(causal)), int(n_splits), _stream_handle(dev, stream))
+    _check(rc, "fa_fwd_partial")
+    return m_part, l_part, o_part
+
+
+def merge_splits(m_part, l_part, o_part, out=None, lse=None, stream=None):
+    """fa_merge_splits.  Returns (o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq])."""
+    S, B, H, Nq, d = o_part.shape
+    for t in (m_part, l_part, o_part):
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.device.type != "cuda":
+            raise ValueError("partials must be contiguous fp32 CUDA tensors")
+    assert m_part.shape == (S, B, H, Nq) and l_part.shape == (S, B, H, Nq)
+    dev = o_part.device
+    out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=dev) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev) if lse is None else lse
+    L = lib()
+    with torch.cuda.device(dev):
+        rc = L.fa_merge_splits(m_part.data_ptr(), l_part.data_ptr(), o_part.data_ptr(),
+                               out.data_ptr(), lse.data_ptr(), B, H, Nq, d, S,
+                               _stream_handle(dev, stream))
+    _check(rc, "fa_merge_splits")
+    return out, lse
+
+
+def split_workspace_bytes(B: int, H: int, Nq: int, d: int, n_splits: int) -> int:
+    return int(lib().fa_split_workspace_bytes(B, H, Nq, d, n_splits))
+
+
+def device_status(device=None, stream=None) -> int:
+    """fa_get_device_status on `device` (default: current).  Returns the FA_* code."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib().fa_get_device_status(_stream_handle(dev, stream)))
+
+
+def version() -> int:
+    return int(lib().fa_version())

@@ -1,0 +1,331 @@
+// fa_api.cu -- the C ABI (include/fa.h): argument validation, TMA tensor
+// maps, launch configuration, the split-KV workspace and error reporting.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+constexpr int kVersion = 100;
+constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSeq = 1 << 30;
+
+thread_local cudaError_t t_last_cuda = cudaSuccess;
+thread_local char t_msg[256];
+
+// Device status word, one per device (kernels record timed-out waits here).
+__device__ int g_fa_status;
+
+struct DevState {
+  bool checked = false;
+  bool supported = false;
+  int* status = nullptr;
+};
+DevState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda = e;
+  return FA_ERR_CUDA;
+}
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Current device: sm_103 check and the status-word address, once per device.
+int device_state(DevState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState& st = g_dev[dev];
+  if (!st.checked) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    st.supported = (major == 10 && minor == 3);
+    if (st.supported) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_fa_status)) != cudaSuccess) return cuda_fail(e);
+      st.status = static_cast<int*>(p);
+    }
+    st.checked = true;
+  }
+  if (!st.supported) return FA_ERR_UNSUPPORTED;
+  *out = &st;
+  return FA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 3-D bf16 map over [batch][rows][inner] with a (64 x box_rows x 1) box and
+// the 128-byte swizzle; out-of-range rows read as zero / are clipped on store.
+int make_map(CUtensorMap* m, const void* base, int inner, int rows, int batch, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cuda_fail(cudaErrorNotSupported);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2,
+                                 static_cast<cuuint64_t>(inner) * 2 * static_cast<cuuint64_t>(rows)};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return FA_OK;
+}
+
+int check_sizes(int B, int H, int Nq, int Nk, int d, float scale) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
+  if (Nq > kMaxSeq || Nk > kMaxSeq) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 65535) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+cudaError_t launch_fwd(int d, int bc, int qt, const CUtensorMap* maps, const fa::FwdParams& p,
+                       dim3 grid, cudaStream_t s) {
+  if (d == 64) return bc == 64 ? fa::launch_fwd_d64_bc64(qt, maps, p, grid, s)
+                               : fa::launch_fwd_d64_bc128(qt, maps, p, grid, s);
+  return bc == 64 ? fa::launch_fwd_d128_bc64(qt, maps, p, grid, s)
+                  : fa::launch_fwd_d128_bc128(qt, maps, p, grid, s);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct SplitLayout {
+  size_t m_off, l_off, o_off, total;
+};
+
+SplitLayout split_layout(long long rows, int d, int n_splits) {
+  SplitLayout L;
+  const size_t ml = align256(static_cast<size_t>(n_splits) * rows * sizeof(float));
+  L.m_off = 0;
+  L.l_off = ml;
+  L.o_off = 2 * ml;
+  L.total = 2 * ml + align256(static_cast<size_t>(n_splits) * rows * d * sizeof(float));
+  return L;
+}
+
+// Shared body of fa_fwd / fa_fwd_ex / fa_fwd_partial.
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+             int Nk, int d, float scale, int causal, int n_splits, void* stream,
+             const fa_opts* opts, float* m_part, float* l_part, float* o_part) {
+  const bool partial = (m_part != nullptr);
+  int rc = check_sizes(B, H, Nq, Nk, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!q || !k || !v) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return FA_ERR_INVALID_ARG;
+  if (partial) {
+    if (!l_part || !o_part || !aligned(m_part, 4) || !aligned(l_part, 4) || !aligned(o_part, 16))
+      return FA_ERR_INVALID_ARG;
+  } else {
+    if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4)) return FA_ERR_INVALID_ARG;
+  }
+  if (n_splits < 1 || n_splits > 65535) return FA_ERR_INVALID_ARG;
+  int bc = 128, qt_opt = 0, skip = -1;
+  unsigned long long timeout = kDefaultTimeoutNs;
+  if (opts) {
+    if (opts->bc != 0 && opts->bc != 64 && opts->bc != 128) return FA_ERR_INVALID_ARG;
+    if (opts->q_tiles_per_cta < 0 || opts->q_tiles_per_cta > 2) return FA_ERR_INVALID_ARG;
+    if (opts->test_skip_kv_load < 0) return FA_ERR_INVALID_ARG;
+    if (opts->bc) bc = opts->bc;
+    qt_opt = opts->q_tiles_per_cta;
+    if (opts->timeout_ns) timeout = opts->timeout_ns;
+    skip = opts->test_skip_kv_load - 1;
+  }
+  DevState* dev = nullptr;
+  if ((rc = device_state(&dev)) != FA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  const int BH = B * H;
+  const int kv_tiles = (Nk + bc - 1) / bc;
+  const int qt = qt_opt ? qt_opt : (Nq > 128 ? 2 : 1);
+  int splits = n_splits;
+  if (!partial && splits > kv_tiles) splits = kv_tiles;
+
+  fa::FwdParams p{};
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.BH = BH;
+  p.n_splits = partial ? splits : (splits > 1 ? splits : 1);
+  p.partial = (partial || splits > 1) ? 1 : 0;
+  p.kv_tiles = kv_tiles;
+  p.tiles_per_split = (kv_tiles + splits - 1) / splits;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.timeout_ns = timeout;
+  p.test_skip_load = skip;
+  p.status = dev->status;
+  p.lse = lse;
+
+  CUtensorMap maps[4];
+  if ((rc = make_map(&maps[0], q, d, Nq, BH, 128)) != FA_OK) return rc;
+  if ((rc = make_map(&maps[1], k, d, Nk, BH, bc)) != FA_OK) return rc;
+  if ((rc = make_map(&maps[2], v, d, Nk, BH, bc)) != FA_OK) return rc;
+  if (!partial && splits == 1) {
+    if ((rc = make_map(&maps[3], o, d, Nq, BH, 128)) != FA_OK) return rc;
+  } else {
+    maps[3] = maps[0];  // unused by the partial epilogue
+  }
+  const dim3 grid((Nq + 128 * qt - 1) / (128 * qt), static_cast<unsigned>(p.n_splits),
+                  static_cast<unsigned>(BH));
+  const long long rows = static_cast<long long>(BH) * Nq;
+
+  if (partial) {
+    p.m_part = m_part;
+    p.l_part = l_part;
+    p.o_part = o_part;
+    cudaError_t e = launch_fwd(d, bc, qt, maps, p, grid, s);
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+  }
+  if (splits == 1) {
+    cudaError_t e = launch_fwd(d, bc, qt, maps, p, grid, s);
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+  }
+
+  // split-KV: stream-ordered workspace, partial kernel, merge, release
+  const SplitLayout L = split_layout(rows, d, splits);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, L.total, s);
+  if (e != cudaSuccess) {
+    t_last_cuda = e;
+    return FA_ERR_NO_MEMORY;
+  }
+  char* base = static_cast<char*>(ws);
+  p.m_part = reinterpret_cast<float*>(base + L.m_off);
+  p.l_part = reinterpret_cast<float*>(base + L.l_off);
+  p.o_part = reinterpret_cast<float*>(base + L.o_off);
+  e = launch_fwd(d, bc, qt, maps, p, grid, s);
+  if (e == cudaSuccess) {
+    fa::MergeParams mp{};
+    mp.m_part = p.m_part;
+    mp.l_part = p.l_part;
+    mp.o_part = p.o_part;
+    mp.o = o;
+    mp.lse = lse;
+    mp.rows = rows;
+    mp.n_splits = splits;
+    e = fa::launch_merge(d, mp, s);
+  }
+  cudaError_t ef = cudaFreeAsync(ws, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (ef != cudaSuccess) return cuda_fail(ef);
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+           int Nk, int d, float scale, int causal, int n_splits, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, stream, nullptr,
+                  nullptr, nullptr, nullptr);
+}
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Nq, int Nk, int d, float scale, int causal, int n_splits, void* stream,
+              const fa_opts* opts) {
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, stream, opts, nullptr,
+                  nullptr, nullptr);
+}
+
+int fa_fwd_partial(const void* q, const void* k, const void* v, float* m_part, float* l_part,
+                   float* o_part, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                   int n_splits, void* stream) {
+  if (!m_part) return FA_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, nullptr, nullptr, B, H, Nq, Nk, d, scale, causal, n_splits, stream,
+                  nullptr, m_part, l_part, o_part);
+}
+
+int fa_merge_splits(const float* m_part, const float* l_part, const float* o_part, void* o,
+                    float* lse, int B, int H, int Nq, int d, int n_splits, void* stream) {
+  if (B < 1 || H < 1 || Nq < 1 || Nq > kMaxSeq) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 65535) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (n_splits < 1 || n_splits > 65535) return FA_ERR_INVALID_ARG;
+  if (!m_part || !l_part || !o_part || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(o_part, 16) || !aligned(o, 16) || !aligned(m_part, 4) || !aligned(l_part, 4) ||
+      !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  DevState* dev = nullptr;
+  int rc = device_state(&dev);
+  if (rc != FA_OK) return rc;
+  fa::MergeParams mp{};
+  mp.m_part = m_part;
+  mp.l_part = l_part;
+  mp.o_part = o_part;
+  mp.o = o;
+  mp.lse = lse;
+  mp.rows = static_cast<long long>(B) * H * Nq;
+  mp.n_splits = n_splits;
+  cudaError_t e = fa::launch_merge(d, mp, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+size_t fa_split_workspace_bytes(int B, int H, int Nq, int d, int n_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || n_splits <= 1 || (d != 64 && d != 128)) return 0;
+  return split_layout(static_cast<long long>(B) * H * Nq, d, n_splits).total;
+}
+
+int fa_get_device_status(void* stream) {
+  DevState* dev = nullptr;
+  int rc = device_state(&dev);
+  if (rc != FA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  const int zero = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&host, dev->status, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return host == fa::kDevTimeout ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+const char* fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported (head dim must be 64 or 128; device must be sm_103)";
+    case FA_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out; the affected CTAs stopped without writing";
+    case FA_ERR_NO_MEMORY: return "could not allocate the split-KV workspace";
+    case FA_ERR_CUDA:
+      std::snprintf(t_msg, sizeof(t_msg), "CUDA error %d: %s", static_cast<int>(t_last_cuda),
+                    cudaGetErrorString(t_last_cuda));
+      return t_msg;
+    default: return "unknown error code";
+  }
+}
+
+int fa_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// fa_internal.h -- declarations shared by the library's translation units
+// (kernel parameters, launcher prototypes, device status codes).  Not part of
+// the public C ABI (that is include/fa.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Device status word values (written by kernels, read by fa_get_device_status).
+enum : int {
+  kDevOk = 0,
+  kDevTimeout = 1,  // a bounded mbarrier wait ran out; the CTA stopped cleanly
+};
+
+struct FwdParams {
+  // n_splits == 1: final outputs.  o is written by TMA through the O map.
+  float* lse;  // [B*H][Nq]
+  // partial != 0: write partial triples instead, index ((split * BH + bh) * Nq + row).
+  int partial;
+  float* m_part;  // natural-log units (scale * raw max), -inf if empty
+  float* l_part;  // sum of exp(scale*s - m_part)
+  float* o_part;  // [.., d] fp32, O_split / l_split (0 if empty)
+  int Nq, Nk, BH;
+  int n_splits;
+  int tiles_per_split;  // K/V tiles per split
+  int kv_tiles;         // ceil(Nk / BC)
+  int causal;
+  float scale;       // natural-units logit scale
+  float scale_log2;  // scale * log2(e)
+  unsigned long long timeout_ns;
+  int test_skip_load;  // >= 0: the producer skips this K/V load (test hook)
+  int* status;         // device status word
+};
+
+struct MergeParams {
+  const float* m_part;
+  const float* l_part;
+  const float* o_part;
+  void* o;     // bf16 [rows][d]
+  float* lse;  // [rows]
+  long long rows;  // B*H*Nq
+  int n_splits;
+};
+
+// Launchers (one per translation unit); return cudaSuccess or the launch error.
+// qt: Q tiles (128 rows each) per CTA.
+cudaError_t launch_fwd_d64_bc64(int qt, const CUtensorMap* maps, const FwdParams& p, dim3 grid,
+                                cudaStream_t s);
+cudaError_t launch_fwd_d64_bc128(int qt, const CUtensorMap* maps, const FwdParams& p, dim3 grid,
+                                 cudaStream_t s);
+cudaError_t launch_fwd_d128_bc64(int qt, const CUtensorMap* maps, const FwdParams& p, dim3 grid,
+                                 cudaStream_t s);
+cudaError_t launch_fwd_d128_bc128(int qt, const CUtensorMap* maps, const FwdParams& p, dim3 grid,
+                                  cudaStream_t s);
+cudaError_t launch_merge(int d, const MergeParams& p, cudaStream_t s);
+
+}  // namespace fa

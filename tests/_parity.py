@@ -1,0 +1,95 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path, run the fp64
+oracle on the same bf16 inputs, compare element by element.
+
+Tolerance (bf16 inputs, fp32 accumulation, bf16 O): max |dO| <= 1e-2,
+mean |dO| <= 1e-3, max |dLSE| <= 1e-3.  Rows the oracle marks fully masked
+(LSE = -inf) must come back with O exactly 0 and LSE exactly -inf.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import online_softmax_sm_gb300 as fa
+from online_softmax_sm_gb300 import workloads
+
+MAX_ABS_O = 1e-2
+MEAN_ABS_O = 1e-3
+MAX_ABS_LSE = 1e-3
+
+
+class Diff:
+    def __init__(self):
+        self.max_o = 0.0
+        self.sum_o = 0.0
+        self.n_o = 0
+        self.max_lse = 0.0
+        self.rows = 0
+        self.masked_rows = 0
+
+    def add(self, o_gpu: np.ndarray, lse_gpu: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray):
+        masked = np.isneginf(lse_ref)
+        if masked.any():
+            assert np.all(o_gpu[masked] == 0.0), "masked rows must give O = 0 exactly"
+            assert np.all(np.isneginf(lse_gpu[masked])), "masked rows must give LSE = -inf"
+        keep = ~masked
+        assert np.all(np.isfinite(o_gpu)), "non-finite O"
+        assert np.all(np.isfinite(lse_gpu[keep])), "non-finite LSE on a visible row"
+        d = np.abs(o_gpu - o_ref)
+        self.max_o = max(self.max_o, float(d.max(initial=0.0)))
+        self.sum_o += float(d.sum())
+        self.n_o += d.size
+        if keep.any():
+            self.max_lse = max(self.max_lse, float(np.abs(lse_gpu[keep] - lse_ref[keep]).max()))
+        self.rows += o_gpu.shape[0]
+        self.masked_rows += int(masked.sum())
+
+    @property
+    def mean_o(self):
+        return self.sum_o / max(self.n_o, 1)
+
+    def check(self, what=""):
+        msg = (f"{what}: rows={self.rows} masked={self.masked_rows} max|dO|={self.max_o:.3e} "
+               f"mean|dO|={self.mean_o:.3e} max|dLSE|={self.max_lse:.3e}")
+        assert self.max_o <= MAX_ABS_O, msg
+        assert self.mean_o <= MEAN_ABS_O, msg
+        assert self.max_lse <= MAX_ABS_LSE, msg
+        return msg
+
+
+def compare(q, k, v, o, lse, scale, causal, heads=None, rows=None, diff: Diff | None = None,
+            threads=None) -> Diff:
+    """q/k/v/o: [B,H,N,d] (any device), lse [B,H,Nq].  heads: list of (b,h)."""
+    diff = diff or Diff()
+    B, H = q.shape[0], q.shape[1]
+    heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    for (b, h) in heads:
+        o_ref, lse_ref = oracle.attention(q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu(), scale, causal,
+                                          rows=rows, threads=threads)
+        og = o[b, h].cpu().double().numpy()
+        lg = lse[b, h].cpu().double().numpy()
+        if rows is not None:
+            og, lg = og[rows], lg[rows]
+        diff.add(og, lg, o_ref, lse_ref)
+    return diff
+
+
+def run_workload(w: workloads.Workload, heads=None, rows=None, n_splits=None, bc=None, qt=0):
+    q, k, v = workloads.generate(w, device="cuda")
+    o, lse = fa.fwd(q, k, v, w.scale, w.causal, w.n_splits if n_splits is None else n_splits,
+                    bc=w.bc if bc is None else bc, q_tiles_per_cta=qt)
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FA_OK
+    return compare(q, k, v, o, lse, w.scale, w.causal, heads=heads, rows=rows)
+
+
+def sample_rows(nq: int, tile: int = 128, extra: int = 64, seed: int = 0) -> list[int]:
+    """Every tile's first and last row, the last row overall, plus seeded extras."""
+    rng = np.random.default_rng(seed)
+    rows = set()
+    for t0 in range(0, nq, tile):
+        rows.add(t0)
+        rows.add(min(t0 + tile, nq) - 1)
+    rows.update(rng.integers(0, nq, size=extra).tolist())
+    return sorted(rows)
