@@ -16,18 +16,28 @@
 // a row with l = 0 gets O = 0 and LSE = -inf (sections 7.2-7.3).
 //
 // CTA = QT query tiles of 128 rows of one (b, h), over one range of K/V tiles
-// (the whole key axis, or one split of it).  Warp roles:
-//   warps 0 .. 4*QT-1   softmax warpgroup i = warp/4 owns Q tile i; thread t
-//                       owns row t of that tile (TMEM lane t), so row max and
-//                       row sum are register-local (no shuffles).  Also does
-//                       the O rescale and the epilogue of its tile.
-//   warp 4*QT           MMA issuer (one elected thread).
-//   warp 4*QT+1         TMA producer (one elected thread): Q once, then K_j,
-//                       V_j, K_{j+1}, ... through a ring of shared-memory stages.
+// (the whole key axis, or one split of it).  Warpgroup roles:
+//   WG i < QT     tile i.  Thread t owns row t of the tile (TMEM lane t), so
+//                 row max and row sum are register-local (no shuffles).  Each
+//                 step: read S_i, publish alpha per row, write P_i into TMEM.
+//                 The warpgroup's first warp also drives tile i's MMAs (lane 0
+//                 issues): O_i += P_i V_j as soon as P_i and the O rescale are
+//                 in place, then S_i = Q_i K_{j+1}^T once that MMA completed.
+//                 The two tiles' chains interleave on the tensor pipe, one
+//                 tile's MMAs covering the other tile's softmax.  Also runs
+//                 the epilogue of its tile.
+//   WG QT         correction: O_i <- alpha O_i in TMEM once P_i(j-1).V_{j-1}
+//                 has landed, skipped for a warp whose 32 rows all kept their
+//                 max.  Runs beside the softmax, off its critical path.
+//   last WG       warp 0: TMA producer (one thread): Q once, then K_j, V_j,
+//                 K_{j+1}, ... through a ring of shared-memory stages.
+//                 Warp 1 allocates TMEM.  Other warps idle.
+// setmaxnreg moves registers from the producer and correction warpgroups to
+// the softmax warpgroups.
 // TMEM (fp32 columns): S_i at [i*BC, (i+1)*BC), O_i at [QT*BC + i*D, ..+D).
 // P_i (bf16 pairs) overwrites the first BC/2 columns of S_i and is the A
-// operand of the P.V MMA straight from TMEM.  Because P_i aliases S_i, the
-// MMA thread issues S_i(j+1) only after P_i(j).V_j has completed.
+// operand of the P.V MMA straight from TMEM.  Because P_i aliases S_i, S_i(j+1)
+// is issued only after P_i(j).V_j has completed.
 //
 // Every mbarrier wait is bounded by a global-timer limit.  A wait that runs
 // out sets the CTA's abort flag and the device status word; every role then
@@ -46,11 +56,21 @@ struct FwdCfg {
   static_assert(BC == 64 || BC == 128, "K/V tile");
   static_assert(QT == 1 || QT == 2, "Q tiles per CTA");
   static constexpr int kBr = 128;  // query rows per tile (= TMEM lanes)
-  static constexpr int kSoftmaxWarps = 4 * QT;
-  static constexpr int kMmaWarp = kSoftmaxWarps;
-  static constexpr int kLoadWarp = kSoftmaxWarps + 1;
-  static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
-  static constexpr int kChunks = D / 64;         // 64-column (128-byte) swizzle chunks
+  static constexpr int kCorrWG = QT;             // correction warpgroup
+  static constexpr int kLoadWarp = 4 * (QT + 1);  // first warp of the last WG
+  static constexpr int kAllocWarp = kLoadWarp + 1;
+  static constexpr int kThreads = 4 * (QT + 2) * 32;
+  // Registers per thread at launch (65536 / threads, multiple of 8) and the
+  // setmaxnreg split that moves them to the softmax warpgroups.  The split must
+  // add up to what the block launches with, or setmaxnreg.inc would wait forever.
+  static constexpr int kRegLaunch = QT == 2 ? 128 : 168;
+  static constexpr int kRegSoftmax = QT == 2 ? 192 : 216;
+  static constexpr int kRegCorr = QT == 2 ? 64 : 160;
+  static constexpr int kRegOther = QT == 2 ? 64 : 128;
+  static_assert(QT * kRegSoftmax + kRegCorr + kRegOther == (QT + 2) * kRegLaunch,
+                "setmaxnreg split must add up to the registers the block launches with");
+  static_assert(kRegLaunch * kThreads <= 65536, "launch register budget");
+  static constexpr int kChunks = D / 64;          // 64-column (128-byte) swizzle chunks
   static constexpr int kQChunkBytes = kBr * 128;  // 128 rows x 128 B
   static constexpr int kQTileBytes = kChunks * kQChunkBytes;
   static constexpr int kKVChunkBytes = BC * 128;
@@ -62,7 +82,7 @@ struct FwdCfg {
                                    : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256
                                                       : 512;
-  static constexpr int kCtlBytes = 1024;
+  static constexpr int kCtlBytes = 2048;
   static constexpr int kSmemLimit = 227 * 1024;
   static constexpr int kStagesFit =
       (kSmemLimit - 1024 - kCtlBytes - QT * kQTileBytes) / kKVTileBytes;
@@ -74,14 +94,17 @@ struct FwdCfg {
 struct __align__(8) Ctl {
   uint64_t q_full;
   uint64_t kv_full[8];
-  uint64_t kv_empty[8];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_done[2];
-  uint64_t drain;
+  uint64_t kv_empty[8][2];  // [stage][tile]: that tile's MMAs reading the stage completed
+  uint64_t s_full[2];       // S_i(j) in TMEM (MMA commit)
+  uint64_t alpha_full[2];   // alpha_i(j) published (128 softmax arrivals)
+  uint64_t pv_ready[2];     // P_i(j) written and O_i rescaled (128 + 128 arrivals)
+  uint64_t o_done[2];       // O_i += P_i(j) V_j completed (MMA commit)
+  uint64_t drain[2];        // every MMA tile i issued has completed
   uint32_t tmem_base;
   int abort;
+  float alpha[2][128];      // per-row rescale factor, softmax -> correction
 };
+static_assert(sizeof(Ctl) <= 2048, "control block");
 
 struct WaitCtx {
   volatile int* abort;
@@ -102,6 +125,11 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
       return false;
     }
   }
+}
+
+// Warp-uniform bounded wait: true only if every lane saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+  return __all_sync(0xffffffffu, wait_bounded(bar, parity, w));
 }
 
 // Bounded wait for this thread's own copies / MMAs in flight (ignores abort).
@@ -137,7 +165,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
   const int row0 = qg * (C::kBr * QT);
   const int kv_begin = split * p.tiles_per_split;
   const int kv_end = min(p.kv_tiles, kv_begin + p.tiles_per_split);
-  int end_i[QT];
+  int n_i[QT];  // K/V steps of tile i: [kv_begin, kv_begin + n_i)
   int kv_end_cta = kv_begin;
 #pragma unroll
   for (int i = 0; i < QT; ++i) {
@@ -154,31 +182,33 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
       }
       e = max(e, kv_begin);
     }
-    end_i[i] = e;
+    n_i[i] = e - kv_begin;
     kv_end_cta = max(kv_end_cta, e);
   }
 
   const uint32_t bar_q = smem_u32(&ctl->q_full);
   const uint32_t bar_kv_full = smem_u32(&ctl->kv_full[0]);
-  const uint32_t bar_kv_empty = smem_u32(&ctl->kv_empty[0]);
+  const uint32_t bar_kv_empty = smem_u32(&ctl->kv_empty[0][0]);  // + 16*stage + 8*tile
   const uint32_t bar_s = smem_u32(&ctl->s_full[0]);
-  const uint32_t bar_p = smem_u32(&ctl->p_full[0]);
+  const uint32_t bar_alpha = smem_u32(&ctl->alpha_full[0]);
+  const uint32_t bar_pv = smem_u32(&ctl->pv_ready[0]);
   const uint32_t bar_o = smem_u32(&ctl->o_done[0]);
-  const uint32_t bar_drain = smem_u32(&ctl->drain);
+  const uint32_t bar_drain = smem_u32(&ctl->drain[0]);
 
   // ---- setup
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar_kv_full + 8 * s, 1);
-      mbar_init(bar_kv_empty + 8 * s, 1);
+      for (int i = 0; i < QT; ++i) mbar_init(bar_kv_empty + 16 * s + 8 * i, 1);
     }
     for (int i = 0; i < QT; ++i) {
       mbar_init(bar_s + 8 * i, 1);
-      mbar_init(bar_p + 8 * i, 128);
+      mbar_init(bar_alpha + 8 * i, 128);
+      mbar_init(bar_pv + 8 * i, 256);
       mbar_init(bar_o + 8 * i, 1);
+      mbar_init(bar_drain + 8 * i, 1);
     }
-    mbar_init(bar_drain, 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -187,7 +217,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  if (warp == C::kMmaWarp) {
+  if (warp == C::kAllocWarp) {
     tmem_alloc(smem_u32(&ctl->tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
@@ -196,19 +226,22 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   const WaitCtx wc{&ctl->abort, p.status, p.timeout_ns};
+  const int wg = warp >> 2;
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
 
-  if (warp == C::kLoadWarp) {
-    // ================================================================ producer
-    if (lane == 0) {
+  if (wg == QT + 1) {
+    setmaxnreg_dec<C::kRegOther>();
+    if (warp == C::kLoadWarp && lane == 0) {
+      // ============================================================== producer
       uint32_t qbytes = 0;
 #pragma unroll
       for (int i = 0; i < QT; ++i)
-        if (end_i[i] > kv_begin) qbytes += C::kQTileBytes;
+        if (n_i[i] > 0) qbytes += C::kQTileBytes;
       if (qbytes) {
         mbar_arrive_expect_tx(bar_q, qbytes);
 #pragma unroll
         for (int i = 0; i < QT; ++i) {
-          if (end_i[i] <= kv_begin) continue;
+          if (n_i[i] <= 0) continue;
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem_u32(sQ + i * C::kQTileBytes + c * C::kQChunkBytes), &tm_q, bar_q,
@@ -221,10 +254,16 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
       for (int j = kv_begin; ok && j < kv_end_cta; ++j) {
         for (int kv = 0; kv < 2; ++kv, ++it) {
           const int stage = it % C::kStages;
-          const uint32_t ph = (it / C::kStages) & 1;
-          if (!wait_bounded(bar_kv_empty + 8 * stage, ph ^ 1, wc)) {
-            ok = false;
-            break;
+          const int use = it / C::kStages;
+          if (use > 0) {
+            // the stage's previous content (ring position it - kStages) must be
+            // released by every tile that read it
+            const int prev_step = (it - C::kStages) >> 1;
+#pragma unroll
+            for (int i = 0; i < QT; ++i)
+              if (ok && prev_step < n_i[i])
+                ok = wait_bounded(bar_kv_empty + 16 * stage + 8 * i, (use - 1) & 1, wc);
+            if (!ok) break;
           }
           if (it == p.test_skip_load) continue;  // test hook: this stage never fills
           const uint32_t full = bar_kv_full + 8 * stage;
@@ -235,7 +274,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
             tma_load_3d(smem_u32(sKV + stage * C::kKVTileBytes + c * C::kKVChunkBytes), map, full,
                         c * 64, j * BC, bh);
           issued_mask |= 1u << stage;
-          issued_par = (issued_par & ~(1u << stage)) | (ph << stage);
+          issued_par = (issued_par & ~(1u << stage)) | (static_cast<uint32_t>(use & 1) << stage);
         }
       }
       // Every copy started here must land before the CTA may exit.
@@ -244,107 +283,128 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
       if (qbytes) wait_own(bar_q, 0, p.timeout_ns);
     }
     __syncwarp();
-  } else if (warp == C::kMmaWarp) {
-    // ============================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BC, false);  // K-major A (Q), B (K)
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);    // B = V is MN-major
-      bool ok = kv_end_cta > kv_begin;
-      if (ok) ok = wait_bounded(bar_q, 0, wc);
-      if (ok) tc_fence_after();
-      int it = 0;
-      for (int jj = 0; ok && kv_begin + jj < kv_end_cta; ++jj) {
-        const int j = kv_begin + jj;
-        {  // S_i = Q_i K_j^T
-          const int stage = it % C::kStages;
-          const uint32_t ph = (it / C::kStages) & 1;
-          ++it;
-          if (!wait_bounded(bar_kv_full + 8 * stage, ph, wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sK = smem_u32(sKV + stage * C::kKVTileBytes);
-#pragma unroll
-          for (int i = 0; i < QT; ++i) {
-            if (j >= end_i[i]) continue;
-            if (jj > 0) {  // P_i(j-1) (aliasing S_i) must have been consumed
-              if (!wait_bounded(bar_o + 8 * i, (jj - 1) & 1, wc)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-            }
-            const uint32_t sQi = smem_u32(sQ + i * C::kQTileBytes);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off_q = (kk / 4) * C::kQChunkBytes + (kk % 4) * 32;
-              const uint32_t off_k = (kk / 4) * C::kKVChunkBytes + (kk % 4) * 32;
-              mma_bf16_ss(tmem + C::kSCol + i * BC, smem_desc_sw128(sQi + off_q, 16, 1024),
-                          smem_desc_sw128(sK + off_k, 16, 1024), kIdescQK, kk > 0);
-            }
-            mma_commit(bar_s + 8 * i);
-          }
-          if (!ok) break;
-          mma_commit(bar_kv_empty + 8 * stage);
-        }
-        {  // O_i += P_i V_j
-          const int stage = it % C::kStages;
-          const uint32_t ph = (it / C::kStages) & 1;
-          ++it;
-          if (!wait_bounded(bar_kv_full + 8 * stage, ph, wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sV = smem_u32(sKV + stage * C::kKVTileBytes);
-#pragma unroll
-          for (int i = 0; i < QT; ++i) {
-            if (j >= end_i[i]) continue;
-            if (!wait_bounded(bar_p + 8 * i, jj & 1, wc)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < BC / 16; ++kk) {
-              // 16 keys = two 8-row groups (SBO 1024 B); D columns in 64-wide
-              // chunks BC*128 B apart (LBO).
-              mma_bf16_ts(tmem + C::kOCol + i * D, tmem + C::kSCol + i * BC + kk * 8,
-                          smem_desc_sw128(sV + kk * 2048, C::kKVChunkBytes, 1024), kIdescPV,
-                          (jj > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(bar_o + 8 * i);
-          }
-          if (!ok) break;
-          mma_commit(bar_kv_empty + 8 * stage);
-        }
-      }
-      // Everything issued above completes before TMEM may be freed.
-      mma_commit(bar_drain);
-      wait_own(bar_drain, 0, p.timeout_ns);
-    }
-    __syncwarp();
-  } else {
-    // ===================================================== softmax warpgroup
-    const int i = warp >> 2;
+  } else if (wg == C::kCorrWG) {
+    // ========================================================= correction
+    if constexpr (C::kRegCorr < C::kRegLaunch) setmaxnreg_dec<C::kRegCorr>();
     const int t = threadIdx.x & 127;
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int n_max = 0;
+#pragma unroll
+    for (int i = 0; i < QT; ++i) n_max = max(n_max, n_i[i]);
+    bool ok = true;
+    for (int jj = 0; ok && jj < n_max; ++jj) {
+#pragma unroll
+      for (int i = 0; i < QT; ++i) {
+        if (jj >= n_i[i]) continue;
+        bool got = wait_bounded(bar_alpha + 8 * i, jj & 1, wc);
+        if (got && jj > 0) got = wait_bounded(bar_o + 8 * i, (jj - 1) & 1, wc);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        if (jj > 0) {
+          const float alpha = ctl->alpha[i][t];
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            tc_fence_after();
+            const uint32_t tO = tmem + lane_off + C::kOCol + i * D;
+            const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 32) {
+              uint32_t o[32];
+              tmem_ld32_sync(tO + cc, o);
+#pragma unroll
+              for (int k = 0; k < 32; k += 2) {
+                float y0, y1;
+                f2_unpack(fmul2(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), a2), y0, y1);
+                o[k] = __float_as_uint(y0);
+                o[k + 1] = __float_as_uint(y1);
+              }
+              tmem_st32(tO + cc, o);
+            }
+            tmem_wait_st();
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar_pv + 8 * i);
+      }
+    }
+  } else {
+    // ========================================================== tile i
+    setmaxnreg_inc<C::kRegSoftmax>();
+    const int i = wg;
+    const int t = threadIdx.x & 127;
+    const bool driver = (warp & 3) == 0;  // this warp issues tile i's MMAs (lane 0)
     const uint32_t tS = tmem + lane_off + C::kSCol + i * BC;
     const uint32_t tO = tmem + lane_off + C::kOCol + i * D;
     const int row = row0 + C::kBr * i + t;
-    const int n = end_i[i] - kv_begin;
+    const int n = n_i[i];
     const float c = p.scale_log2;
     // last key visible to this row
     const int lim = p.causal ? min(p.Nk - 1, row + (p.Nk - p.Nq)) : p.Nk - 1;
+
+    // MMA issue (warp-uniform arguments; lane 0 issues).
+    constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BC, false);  // K-major A (Q), B (K)
+    constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);    // B = V is MN-major
+    // Descriptor templates; the start-address field (bits 0-13, address >> 4)
+    // of a shared address below 256 KB never carries, so per-MMA offsets are
+    // plain 32-bit adds to the low word.
+    const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ + i * C::kQTileBytes), 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(smem_u32(sKV), 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(smem_u32(sKV), C::kKVChunkBytes, 1024);
+    const uint64_t hi_q = dq0 & 0xFFFFFFFF00000000ull, hi_k = dk0 & 0xFFFFFFFF00000000ull,
+                   hi_v = dv0 & 0xFFFFFFFF00000000ull;
+    const uint32_t lo_q = static_cast<uint32_t>(dq0), lo_k = static_cast<uint32_t>(dk0),
+                   lo_v = static_cast<uint32_t>(dv0);
+    auto issue_qk = [&](int jj) {  // S_i = Q_i K_jj^T, then release K's stage for tile i
+      const int stage = (2 * jj) % C::kStages;
+      const uint32_t k_lo = lo_k + ((stage * C::kKVTileBytes) >> 4);
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_q = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
+          const uint32_t off_k = ((kk / 4) * C::kKVChunkBytes + (kk % 4) * 32) >> 4;
+          mma_bf16_ss(tmem + C::kSCol + i * BC, hi_q | (lo_q + off_q), hi_k | (k_lo + off_k),
+                      kIdescQK, kk > 0);
+        }
+        mma_commit(bar_s + 8 * i);
+        mma_commit(bar_kv_empty + 16 * stage + 8 * i);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int jj) {  // O_i += P_i V_jj, then release V's stage for tile i
+      const int stage = (2 * jj + 1) % C::kStages;
+      const uint32_t v_lo = lo_v + ((stage * C::kKVTileBytes) >> 4);
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < BC / 16; ++kk) {
+          // 16 keys = two 8-row groups (SBO 1024 B); D columns in 64-wide chunks
+          // BC*128 B apart (LBO).
+          mma_bf16_ts(tmem + C::kOCol + i * D, tmem + C::kSCol + i * BC + kk * 8,
+                      hi_v | (v_lo + ((kk * 2048) >> 4)), kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar_o + 8 * i);
+        mma_commit(bar_kv_empty + 16 * stage + 8 * i);
+      }
+      __syncwarp();
+    };
+    auto kv_ready = [&](int pos) {
+      return warp_wait(bar_kv_full + 8 * (pos % C::kStages), (pos / C::kStages) & 1, wc);
+    };
+
+    bool ok = true;
+    bool issued_any = false;
+    if (driver && n > 0) {
+      ok = warp_wait(bar_q, 0, wc) && kv_ready(0);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0);
+        issued_any = true;
+      }
+    }
     float m = -INFINITY;
     float l = 0.f;
-    bool ok = true;
-    for (int jj = 0; jj < n; ++jj) {
+    for (int jj = 0; ok && jj < n; ++jj) {
       const int j = kv_begin + jj;
-      bool got = wait_bounded(bar_s + 8 * i, jj & 1, wc);
-      if (got && jj > 0) got = wait_bounded(bar_o + 8 * i, (jj - 1) & 1, wc);
-      if (!__all_sync(0xffffffffu, got)) {
+      if (!warp_wait(bar_s + 8 * i, jj & 1, wc)) {
         ok = false;
         break;
       }
@@ -363,57 +423,69 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
           if (key0 + cc > lim) s[cc] = -INFINITY;
       }
 
-      // m' = max(m, rowmax S): eight independent partial maxima
-      float mx[8];
+      // m' = max(m, rowmax S): four independent chains of three-input max
+      float mx[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = s[u];
+      for (int u = 0; u < 4; ++u) mx[u] = fmaxf(s[2 * u], s[2 * u + 1]);
 #pragma unroll
-      for (int cc = 8; cc < BC; ++cc) mx[cc & 7] = fmaxf(mx[cc & 7], s[cc]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_new = fmaxf(m, mt);
+      for (int cc = 8; cc < BC; cc += 2) mx[(cc >> 1) & 3] = max3f(mx[(cc >> 1) & 3], s[cc], s[cc + 1]);
+      const float m_new = max3f(m, fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = (m_new == m) ? 1.f : ex2_approx((m - m_ref) * c);
+      ctl->alpha[i][t] = alpha;  // the correction warpgroup rescales O_i by it
+      mbar_arrive(bar_alpha + 8 * i);
 
-      // P = 2^(s*c - m_ref*c); rowsum of the fp32 P (before the bf16 cast)
-      const float neg = m_ref * c;
-      float ls[8];
+      // P = 2^(s*c - m_ref*c) (packed FFMA, then EX2); rowsum of the fp32 P
+      // (before the bf16 cast) in four packed partial sums.
+      const uint64_t c2 = f2_pack(c, c);
+      const uint64_t neg2 = f2_pack(-m_ref * c, -m_ref * c);
+      uint64_t ls[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+      for (int u = 0; u < 4; ++u) ls[u] = 0ull;
       uint32_t pk[BC / 2];
 #pragma unroll
       for (int cc = 0; cc < BC; cc += 2) {
-        const float p0 = ex2_approx(fmaf(s[cc], c, -neg));
-        const float p1 = ex2_approx(fmaf(s[cc + 1], c, -neg));
-        ls[(cc >> 1) & 7] += p0 + p1;
+        float x0, x1;
+        f2_unpack(ffma2(f2_pack(s[cc], s[cc + 1]), c2, neg2), x0, x1);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        ls[(cc >> 1) & 3] = fadd2(ls[(cc >> 1) & 3], f2_pack(p0, p1));
         pk[cc >> 1] = pack_bf16x2(p0, p1);
       }
-      const float rowsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      float lsum[4];
+      f2_unpack(fadd2(ls[0], ls[1]), lsum[0], lsum[1]);
+      f2_unpack(fadd2(ls[2], ls[3]), lsum[2], lsum[3]);
+      const float rowsum = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
 #pragma unroll
       for (int h = 0; h < BC / 64; ++h) tmem_st32(tS + h * 32, pk + h * 32);
-
-      // O <- alpha O (PV_i(j-1) is complete), skipped when no row of this
-      // warp changed its max.
-      if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t o[32];
-          tmem_ld32_sync(tO + cc, o);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-          tmem_st32(tO + cc, o);
-        }
-      }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_p + 8 * i);
+      mbar_arrive(bar_pv + 8 * i);
       l = alpha * l + rowsum;
       m = m_new;
+
+      if (driver) {
+        // O_i += P_i V_j once all 128 rows wrote P and O_i is rescaled; then,
+        // when that MMA has completed (P_i aliases S_i), S_i = Q_i K_{j+1}^T.
+        ok = warp_wait(bar_pv + 8 * i, jj & 1, wc) && kv_ready(2 * jj + 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(jj);
+        if (jj + 1 < n) {
+          ok = warp_wait(bar_o + 8 * i, jj & 1, wc) && kv_ready(2 * jj + 2);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk(jj + 1);
+        }
+      }
     }
-    if (ok && n > 0) {
-      const bool got = wait_bounded(bar_o + 8 * i, (n - 1) & 1, wc);
-      ok = __all_sync(0xffffffffu, got);
+    if (driver && issued_any) {
+      // Everything this warp issued completes before TMEM may be freed.
+      if (lane == 0) mma_commit(bar_drain + 8 * i);
+      __syncwarp();
+      wait_own(bar_drain + 8 * i, 0, p.timeout_ns);
     }
+    if (ok && n > 0) ok = warp_wait(bar_o + 8 * i, (n - 1) & 1, wc);
     const bool bad = named_bar_or(1 + i, 128, !ok || *wc.abort);
     // A tile that starts past the last query row has nothing to write.
     if (!bad && row0 + C::kBr * i < p.Nq) {
@@ -489,7 +561,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
   // ---- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == C::kMmaWarp) {
+  if (warp == C::kAllocWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -499,6 +571,13 @@ template <int D, int BC, int QT>
 cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, dim3 grid, cudaStream_t s) {
   using C = FwdCfg<D, BC, QT>;
   auto kern = fa_fwd_kernel<D, BC, QT>;
+  // The setmaxnreg split assumes the block launches with exactly kRegLaunch
+  // registers per thread; with fewer, setmaxnreg.inc could never be granted.
+  static const bool regs_ok = [&] {
+    cudaFuncAttributes attr{};
+    return cudaFuncGetAttributes(&attr, kern) == cudaSuccess && attr.numRegs == C::kRegLaunch;
+  }();
+  if (!regs_ok) return cudaErrorInvalidKernelImage;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(maps[0], maps[1], maps[2], maps[3], p);
