@@ -19,25 +19,26 @@
 // (the whole key axis, or one split of it).  Warpgroup roles:
 //   WG i < QT     tile i.  Thread t owns row t of the tile (TMEM lane t), so
 //                 row max and row sum are register-local (no shuffles).  Each
-//                 step: read S_i, publish alpha per row, write P_i into TMEM.
-//                 The warpgroup's first warp also drives tile i's MMAs (lane 0
-//                 issues): O_i += P_i V_j as soon as P_i and the O rescale are
-//                 in place, then S_i = Q_i K_{j+1}^T once that MMA completed.
-//                 The two tiles' chains interleave on the tensor pipe, one
-//                 tile's MMAs covering the other tile's softmax.  Also runs
-//                 the epilogue of its tile.
+//                 step: read S_i, publish alpha per row, write P_i (bf16) to
+//                 shared memory.  Also runs the epilogue of its tile.
 //   WG QT         correction: O_i <- alpha O_i in TMEM once P_i(j-1).V_{j-1}
 //                 has landed, skipped for a warp whose 32 rows all kept their
 //                 max.  Runs beside the softmax, off its critical path.
-//   last WG       warp 0: TMA producer (one thread): Q once, then K_j, V_j,
-//                 K_{j+1}, ... through a ring of shared-memory stages.
-//                 Warp 1 allocates TMEM.  Other warps idle.
+//   last WG       warp 0: TMA producer (one thread): Q once, then K and V
+//                 tiles through a ring of shared-memory stages, K one step
+//                 ahead of V (see ring_pos_k / ring_pos_v).
+//                 Warp 1: MMA issuer.  Warp-uniform code, one elected lane
+//                 issues; a small scheduler issues whichever MMA has its
+//                 inputs: S_i = Q_i K_{j+1}^T as soon as every row of tile i
+//                 has read S_i(j) (so it overlaps that step's exponentials),
+//                 O_i += P_i V_j once P_i and the O rescale are in place.
+//                 Warp 2 allocates TMEM.  Warp 3 idles.
 // setmaxnreg moves registers from the producer and correction warpgroups to
 // the softmax warpgroups.
 // TMEM (fp32 columns): S_i at [i*BC, (i+1)*BC), O_i at [QT*BC + i*D, ..+D).
-// P_i (bf16 pairs) overwrites the first BC/2 columns of S_i and is the A
-// operand of the P.V MMA straight from TMEM.  Because P_i aliases S_i, S_i(j+1)
-// is issued only after P_i(j).V_j has completed.
+// Shared memory: Q_i, P_i (both [128 rows][BC or D] bf16, 128-byte swizzle, the
+// layout the MMA reads K-major), then the K/V ring.  P_i(j+1) is written only
+// after O_i += P_i(j) V_j has completed.
 //
 // Every mbarrier wait is bounded by a global-timer limit.  A wait that runs
 // out sets the CTA's abort flag and the device status word; every role then
@@ -58,7 +59,8 @@ struct FwdCfg {
   static constexpr int kBr = 128;  // query rows per tile (= TMEM lanes)
   static constexpr int kCorrWG = QT;             // correction warpgroup
   static constexpr int kLoadWarp = 4 * (QT + 1);  // first warp of the last WG
-  static constexpr int kAllocWarp = kLoadWarp + 1;
+  static constexpr int kMmaWarp = kLoadWarp + 1;
+  static constexpr int kAllocWarp = kLoadWarp + 2;
   static constexpr int kThreads = 4 * (QT + 2) * 32;
   // Registers per thread at launch (65536 / threads, multiple of 8) and the
   // setmaxnreg split that moves them to the softmax warpgroups.  The split must
@@ -73,6 +75,7 @@ struct FwdCfg {
   static constexpr int kChunks = D / 64;          // 64-column (128-byte) swizzle chunks
   static constexpr int kQChunkBytes = kBr * 128;  // 128 rows x 128 B
   static constexpr int kQTileBytes = kChunks * kQChunkBytes;
+  static constexpr int kPTileBytes = (BC / 64) * kQChunkBytes;  // 128 rows x BC keys, bf16
   static constexpr int kKVChunkBytes = BC * 128;
   static constexpr int kKVTileBytes = kChunks * kKVChunkBytes;
   static constexpr int kSCol = 0;
@@ -85,10 +88,11 @@ struct FwdCfg {
   static constexpr int kCtlBytes = 2048;
   static constexpr int kSmemLimit = 227 * 1024;
   static constexpr int kStagesFit =
-      (kSmemLimit - 1024 - kCtlBytes - QT * kQTileBytes) / kKVTileBytes;
+      (kSmemLimit - 1024 - kCtlBytes - QT * (kQTileBytes + kPTileBytes)) / kKVTileBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static_assert(kStages >= 2, "shared memory");
-  static constexpr int kSmemBytes = 1024 + QT * kQTileBytes + kStages * kKVTileBytes + kCtlBytes;
+  static constexpr int kSmemBytes =
+      1024 + QT * (kQTileBytes + kPTileBytes) + kStages * kKVTileBytes + kCtlBytes;
 };
 
 struct __align__(8) Ctl {
@@ -96,10 +100,12 @@ struct __align__(8) Ctl {
   uint64_t kv_full[8];
   uint64_t kv_empty[8][2];  // [stage][tile]: that tile's MMAs reading the stage completed
   uint64_t s_full[2];       // S_i(j) in TMEM (MMA commit)
+  uint64_t s_free[2];       // all 128 rows of S_i(j) read into registers
   uint64_t alpha_full[2];   // alpha_i(j) published (128 softmax arrivals)
-  uint64_t pv_ready[2];     // P_i(j) written and O_i rescaled (128 + 128 arrivals)
+  uint64_t alpha_free[2];   // alpha_i(j) read by the correction (128 arrivals)
+  uint64_t pv_ready[2];     // P_i(j) in shared memory and O_i rescaled (128 + 128 arrivals)
   uint64_t o_done[2];       // O_i += P_i(j) V_j completed (MMA commit)
-  uint64_t drain[2];        // every MMA tile i issued has completed
+  uint64_t drain;           // every MMA issued has completed
   uint32_t tmem_base;
   int abort;
   float alpha[2][128];      // per-row rescale factor, softmax -> correction
@@ -141,6 +147,26 @@ __device__ __forceinline__ void wait_own(uint32_t bar, uint32_t parity,
   }
 }
 
+// Order of the K/V tiles through the shared-memory ring for a CTA with n steps:
+// K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}.  K runs one step
+// ahead of V, so K_{j+1} reuses the slot of V_{j-2} and V_j the slot of K_j:
+// both are free long before they are needed, and S_i(j+1) can start while
+// step j's softmax is still running.
+__device__ __forceinline__ int ring_pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int ring_pos_v(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
+// Inverse: position p -> (is_v, step).
+__device__ __forceinline__ void ring_decode(int p, int n, bool& is_v, int& step) {
+  if (p == 0) {
+    is_v = false, step = 0;
+  } else if (p == 2 * n - 1) {
+    is_v = true, step = n - 1;
+  } else if (p & 1) {
+    is_v = false, step = (p + 1) >> 1;
+  } else {
+    is_v = true, step = (p - 2) >> 1;
+  }
+}
+
 template <int D, int BC, int QT>
 __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -152,7 +178,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint8_t* sQ = smem;
-  uint8_t* sKV = sQ + QT * C::kQTileBytes;
+  uint8_t* sP = sQ + QT * C::kQTileBytes;
+  uint8_t* sKV = sP + QT * C::kPTileBytes;
   Ctl* ctl = reinterpret_cast<Ctl*>(sKV + C::kStages * C::kKVTileBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -190,10 +217,12 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
   const uint32_t bar_kv_full = smem_u32(&ctl->kv_full[0]);
   const uint32_t bar_kv_empty = smem_u32(&ctl->kv_empty[0][0]);  // + 16*stage + 8*tile
   const uint32_t bar_s = smem_u32(&ctl->s_full[0]);
+  const uint32_t bar_sfree = smem_u32(&ctl->s_free[0]);
   const uint32_t bar_alpha = smem_u32(&ctl->alpha_full[0]);
+  const uint32_t bar_afree = smem_u32(&ctl->alpha_free[0]);
   const uint32_t bar_pv = smem_u32(&ctl->pv_ready[0]);
   const uint32_t bar_o = smem_u32(&ctl->o_done[0]);
-  const uint32_t bar_drain = smem_u32(&ctl->drain[0]);
+  const uint32_t bar_drain = smem_u32(&ctl->drain);
 
   // ---- setup
   if (threadIdx.x == 0) {
@@ -204,11 +233,13 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
     }
     for (int i = 0; i < QT; ++i) {
       mbar_init(bar_s + 8 * i, 1);
+      mbar_init(bar_sfree + 8 * i, 128);
       mbar_init(bar_alpha + 8 * i, 128);
+      mbar_init(bar_afree + 8 * i, 128);
       mbar_init(bar_pv + 8 * i, 256);
       mbar_init(bar_o + 8 * i, 1);
-      mbar_init(bar_drain + 8 * i, 1);
     }
+    mbar_init(bar_drain, 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -231,7 +262,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
 
   if (wg == QT + 1) {
     setmaxnreg_dec<C::kRegOther>();
-    if (warp == C::kLoadWarp && lane == 0) {
+    if (warp == C::kLoadWarp) {
+      if (lane == 0) {
       // ============================================================== producer
       uint32_t qbytes = 0;
 #pragma unroll
@@ -249,40 +281,162 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
         }
       }
       uint32_t issued_mask = 0, issued_par = 0;
-      int it = 0;
+      const int n_cta = kv_end_cta - kv_begin;
       bool ok = true;
-      for (int j = kv_begin; ok && j < kv_end_cta; ++j) {
-        for (int kv = 0; kv < 2; ++kv, ++it) {
-          const int stage = it % C::kStages;
-          const int use = it / C::kStages;
-          if (use > 0) {
-            // the stage's previous content (ring position it - kStages) must be
-            // released by every tile that read it
-            const int prev_step = (it - C::kStages) >> 1;
+      for (int it = 0; ok && it < 2 * n_cta; ++it) {
+        const int stage = it % C::kStages;
+        const int use = it / C::kStages;
+        if (use > 0) {
+          // the slot's previous content (ring position it - kStages) must be
+          // released by every tile that read it
+          bool pv_;
+          int prev_step;
+          ring_decode(it - C::kStages, n_cta, pv_, prev_step);
 #pragma unroll
-            for (int i = 0; i < QT; ++i)
-              if (ok && prev_step < n_i[i])
-                ok = wait_bounded(bar_kv_empty + 16 * stage + 8 * i, (use - 1) & 1, wc);
-            if (!ok) break;
-          }
-          if (it == p.test_skip_load) continue;  // test hook: this stage never fills
-          const uint32_t full = bar_kv_full + 8 * stage;
-          mbar_arrive_expect_tx(full, C::kKVTileBytes);
-          const CUtensorMap* map = kv ? &tm_v : &tm_k;
-#pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(smem_u32(sKV + stage * C::kKVTileBytes + c * C::kKVChunkBytes), map, full,
-                        c * 64, j * BC, bh);
-          issued_mask |= 1u << stage;
-          issued_par = (issued_par & ~(1u << stage)) | (static_cast<uint32_t>(use & 1) << stage);
+          for (int i = 0; i < QT; ++i)
+            if (ok && prev_step < n_i[i])
+              ok = wait_bounded(bar_kv_empty + 16 * stage + 8 * i, (use - 1) & 1, wc);
+          if (!ok) break;
         }
+        if (it == p.test_skip_load) continue;  // test hook: this slot never fills
+        bool is_v;
+        int step;
+        ring_decode(it, n_cta, is_v, step);
+        const uint32_t full = bar_kv_full + 8 * stage;
+        mbar_arrive_expect_tx(full, C::kKVTileBytes);
+        const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem_u32(sKV + stage * C::kKVTileBytes + c * C::kKVChunkBytes), map, full,
+                      c * 64, (kv_begin + step) * BC, bh);
+        issued_mask |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (static_cast<uint32_t>(use & 1) << stage);
       }
       // Every copy started here must land before the CTA may exit.
       for (int s = 0; s < C::kStages; ++s)
         if ((issued_mask >> s) & 1u) wait_own(bar_kv_full + 8 * s, (issued_par >> s) & 1u, p.timeout_ns);
       if (qbytes) wait_own(bar_q, 0, p.timeout_ns);
+      }
+      __syncwarp();
+    } else if (warp == C::kMmaWarp) {
+      // ============================================================ MMA issuer
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BC, false);  // K-major A (Q), B (K)
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);    // A = P K-major, B = V MN-major
+      // Descriptor templates; the start-address field (bits 0-13, address >> 4)
+      // of a shared address below 256 KB never carries, so per-MMA offsets are
+      // plain 32-bit adds to the low word.
+      const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dp0 = smem_desc_sw128(smem_u32(sP), 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(sKV), 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(sKV), C::kKVChunkBytes, 1024);
+      const uint64_t hi_q = dq0 & 0xFFFFFFFF00000000ull, hi_p = dp0 & 0xFFFFFFFF00000000ull,
+                     hi_k = dk0 & 0xFFFFFFFF00000000ull, hi_v = dv0 & 0xFFFFFFFF00000000ull;
+      const uint32_t lo_q = static_cast<uint32_t>(dq0), lo_p = static_cast<uint32_t>(dp0),
+                     lo_k = static_cast<uint32_t>(dk0), lo_v = static_cast<uint32_t>(dv0);
+      int qk[QT], pv[QT];  // next step whose S_i / O_i MMA is not issued yet
+#pragma unroll
+      for (int i = 0; i < QT; ++i) qk[i] = pv[i] = 0;
+      auto probe = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_test(bar, parity));
+      };
+      const int n_cta = kv_end_cta - kv_begin;
+      bool ok = n_cta > 0;
+      if (ok) ok = warp_wait(bar_q, 0, wc);
+      if (ok) tc_fence_after();
+      uint32_t idle = 0;
+      uint64_t t_idle = 0;
+      int last = QT - 1;
+      while (ok) {
+        bool all_done = true, issued = false;
+        int sleep_i = -1;
+#pragma unroll
+        for (int r = 0; r < QT; ++r) {
+          const int i = (last + 1 + r) % QT;
+          if (pv[i] >= n_i[i]) continue;
+          all_done = false;
+          if (sleep_i < 0) sleep_i = i;
+          const int q = qk[i];
+          if (q < n_i[i] && q <= pv[i] + 1) {
+            // S_i(q) = Q_i K_q^T: needs K_q and every row done reading S_i(q-1).
+            const int pos = ring_pos_k(q);
+            const int stage = pos % C::kStages;
+            if (probe(bar_kv_full + 8 * stage, (pos / C::kStages) & 1) &&
+                (q == 0 || probe(bar_sfree + 8 * i, (q - 1) & 1))) {
+              tc_fence_after();
+              const uint32_t q_lo = lo_q + ((i * C::kQTileBytes) >> 4);
+              const uint32_t k_lo = lo_k + ((stage * C::kKVTileBytes) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off_q = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
+                const uint32_t off_k = ((kk / 4) * C::kKVChunkBytes + (kk % 4) * 32) >> 4;
+                mma_bf16_ss_elect(tmem + C::kSCol + i * BC, hi_q | (q_lo + off_q),
+                                  hi_k | (k_lo + off_k), kIdescQK, kk > 0);
+              }
+              mma_commit_elect(bar_s + 8 * i);
+              mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
+              qk[i] = q + 1;
+              last = i;
+              issued = true;
+              break;
+            }
+          }
+          const int v = pv[i];
+          if (v < qk[i]) {
+            // O_i += P_i(v) V_v: needs V_v, P_i(v) in smem and O_i rescaled.
+            const int pos = ring_pos_v(v, n_cta);
+            const int stage = pos % C::kStages;
+            if (probe(bar_kv_full + 8 * stage, (pos / C::kStages) & 1) &&
+                probe(bar_pv + 8 * i, v & 1)) {
+              tc_fence_after();
+              const uint32_t p_lo = lo_p + ((i * C::kPTileBytes) >> 4);
+              const uint32_t v_lo = lo_v + ((stage * C::kKVTileBytes) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < BC / 16; ++kk) {
+                // P: 16 keys of the K-major tile.  V: 16 keys = two 8-row groups
+                // (SBO 1024 B); D columns in 64-wide chunks BC*128 B apart (LBO).
+                const uint32_t off_p = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
+                mma_bf16_ss_elect(tmem + C::kOCol + i * D, hi_p | (p_lo + off_p),
+                                  hi_v | (v_lo + ((kk * 2048) >> 4)), kIdescPV,
+                                  (v > 0 || kk > 0) ? 1u : 0u);
+              }
+              mma_commit_elect(bar_o + 8 * i);
+              mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
+              pv[i] = v + 1;
+              last = i;
+              issued = true;
+              break;
+            }
+          }
+        }
+        if (all_done) break;
+        if (issued) {
+          idle = 0;
+          continue;
+        }
+        // Nothing ready: sleep briefly on the next input tile sleep_i waits for
+        // rather than spin on issue slots the softmax warps need.
+        if (pv[sleep_i] < qk[sleep_i])
+          mbar_try_wait_hint(bar_pv + 8 * sleep_i, pv[sleep_i] & 1, 100);
+        else if (qk[sleep_i] > 0)
+          mbar_try_wait_hint(bar_sfree + 8 * sleep_i, (qk[sleep_i] - 1) & 1, 100);
+        if ((idle++ & 63) == 0) {
+          const uint64_t now = global_timer_ns();
+          if (idle == 1) t_idle = now;
+          if (__any_sync(0xffffffffu, *wc.abort != 0)) break;
+          if (now - t_idle > p.timeout_ns) {
+            if (lane == 0) {
+              *wc.abort = 1;
+              atomicExch(p.status, kDevTimeout);
+            }
+            break;
+          }
+        }
+      }
+      // Everything issued above completes before TMEM may be freed.
+      mma_commit_elect(bar_drain);
+      wait_own(bar_drain, 0, p.timeout_ns);
+      __syncwarp();
     }
-    __syncwarp();
   } else if (wg == C::kCorrWG) {
     // ========================================================= correction
     if constexpr (C::kRegCorr < C::kRegLaunch) setmaxnreg_dec<C::kRegCorr>();
@@ -295,14 +449,17 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
 #pragma unroll
       for (int i = 0; i < QT; ++i) {
         if (jj >= n_i[i]) continue;
-        bool got = wait_bounded(bar_alpha + 8 * i, jj & 1, wc);
-        if (got && jj > 0) got = wait_bounded(bar_o + 8 * i, (jj - 1) & 1, wc);
-        if (!__all_sync(0xffffffffu, got)) {
+        if (!__all_sync(0xffffffffu, wait_bounded(bar_alpha + 8 * i, jj & 1, wc))) {
+          ok = false;
+          break;
+        }
+        const float alpha = ctl->alpha[i][t];
+        mbar_arrive(bar_afree + 8 * i);  // the softmax may publish alpha_i(j+1)
+        if (jj > 0 && !__all_sync(0xffffffffu, wait_bounded(bar_o + 8 * i, (jj - 1) & 1, wc))) {
           ok = false;
           break;
         }
         if (jj > 0) {
-          const float alpha = ctl->alpha[i][t];
           if (__any_sync(0xffffffffu, alpha != 1.f)) {
             tc_fence_after();
             const uint32_t tO = tmem + lane_off + C::kOCol + i * D;
@@ -332,7 +489,6 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
     setmaxnreg_inc<C::kRegSoftmax>();
     const int i = wg;
     const int t = threadIdx.x & 127;
-    const bool driver = (warp & 3) == 0;  // this warp issues tile i's MMAs (lane 0)
     const uint32_t tS = tmem + lane_off + C::kSCol + i * BC;
     const uint32_t tO = tmem + lane_off + C::kOCol + i * D;
     const int row = row0 + C::kBr * i + t;
@@ -341,65 +497,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
     // last key visible to this row
     const int lim = p.causal ? min(p.Nk - 1, row + (p.Nk - p.Nq)) : p.Nk - 1;
 
-    // MMA issue (warp-uniform arguments; lane 0 issues).
-    constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BC, false);  // K-major A (Q), B (K)
-    constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);    // B = V is MN-major
-    // Descriptor templates; the start-address field (bits 0-13, address >> 4)
-    // of a shared address below 256 KB never carries, so per-MMA offsets are
-    // plain 32-bit adds to the low word.
-    const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ + i * C::kQTileBytes), 16, 1024);
-    const uint64_t dk0 = smem_desc_sw128(smem_u32(sKV), 16, 1024);
-    const uint64_t dv0 = smem_desc_sw128(smem_u32(sKV), C::kKVChunkBytes, 1024);
-    const uint64_t hi_q = dq0 & 0xFFFFFFFF00000000ull, hi_k = dk0 & 0xFFFFFFFF00000000ull,
-                   hi_v = dv0 & 0xFFFFFFFF00000000ull;
-    const uint32_t lo_q = static_cast<uint32_t>(dq0), lo_k = static_cast<uint32_t>(dk0),
-                   lo_v = static_cast<uint32_t>(dv0);
-    auto issue_qk = [&](int jj) {  // S_i = Q_i K_jj^T, then release K's stage for tile i
-      const int stage = (2 * jj) % C::kStages;
-      const uint32_t k_lo = lo_k + ((stage * C::kKVTileBytes) >> 4);
-      if (lane == 0) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_q = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
-          const uint32_t off_k = ((kk / 4) * C::kKVChunkBytes + (kk % 4) * 32) >> 4;
-          mma_bf16_ss(tmem + C::kSCol + i * BC, hi_q | (lo_q + off_q), hi_k | (k_lo + off_k),
-                      kIdescQK, kk > 0);
-        }
-        mma_commit(bar_s + 8 * i);
-        mma_commit(bar_kv_empty + 16 * stage + 8 * i);
-      }
-      __syncwarp();
-    };
-    auto issue_pv = [&](int jj) {  // O_i += P_i V_jj, then release V's stage for tile i
-      const int stage = (2 * jj + 1) % C::kStages;
-      const uint32_t v_lo = lo_v + ((stage * C::kKVTileBytes) >> 4);
-      if (lane == 0) {
-#pragma unroll
-        for (int kk = 0; kk < BC / 16; ++kk) {
-          // 16 keys = two 8-row groups (SBO 1024 B); D columns in 64-wide chunks
-          // BC*128 B apart (LBO).
-          mma_bf16_ts(tmem + C::kOCol + i * D, tmem + C::kSCol + i * BC + kk * 8,
-                      hi_v | (v_lo + ((kk * 2048) >> 4)), kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar_o + 8 * i);
-        mma_commit(bar_kv_empty + 16 * stage + 8 * i);
-      }
-      __syncwarp();
-    };
-    auto kv_ready = [&](int pos) {
-      return warp_wait(bar_kv_full + 8 * (pos % C::kStages), (pos / C::kStages) & 1, wc);
-    };
-
     bool ok = true;
-    bool issued_any = false;
-    if (driver && n > 0) {
-      ok = warp_wait(bar_q, 0, wc) && kv_ready(0);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(0);
-        issued_any = true;
-      }
-    }
     float m = -INFINITY;
     float l = 0.f;
     for (int jj = 0; ok && jj < n; ++jj) {
@@ -413,6 +511,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
       uint32_t r[BC];
 #pragma unroll
       for (int h = 0; h < BC / 64; ++h) tmem_ld64_sync(tS + h * 64, r + h * 64);
+      tc_fence_before();
+      mbar_arrive(bar_sfree + 8 * i);  // S_i(j) may be overwritten by S_i(j+1)
       float s[BC];
 #pragma unroll
       for (int cc = 0; cc < BC; ++cc) s[cc] = __uint_as_float(r[cc]);
@@ -432,6 +532,12 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
       const float m_new = max3f(m, fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = (m_new == m) ? 1.f : ex2_approx((m - m_ref) * c);
+      // The correction must have read alpha_i(j-1) before the slot is reused
+      // (S_i(j) was issued before it ran, so this step can be ahead of it).
+      if (jj > 0 && !warp_wait(bar_afree + 8 * i, (jj - 1) & 1, wc)) {
+        ok = false;
+        break;
+      }
       ctl->alpha[i][t] = alpha;  // the correction warpgroup rescales O_i by it
       mbar_arrive(bar_alpha + 8 * i);
 
@@ -456,34 +562,24 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
       f2_unpack(fadd2(ls[0], ls[1]), lsum[0], lsum[1]);
       f2_unpack(fadd2(ls[2], ls[3]), lsum[2], lsum[3]);
       const float rowsum = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+      // P_i(j) -> shared memory (128-byte swizzle, row t), once O_i += P_i(j-1) V
+      // has finished reading the buffer.
+      if (jj > 0 && !warp_wait(bar_o + 8 * i, (jj - 1) & 1, wc)) {
+        ok = false;
+        break;
+      }
+      {
+        const uint32_t sp = smem_u32(sP + i * C::kPTileBytes) + t * 128;
 #pragma unroll
-      for (int h = 0; h < BC / 64; ++h) tmem_st32(tS + h * 32, pk + h * 32);
-      tmem_wait_st();
+        for (int u = 0; u < BC / 8; ++u)  // 16-byte unit u holds keys 8u..8u+7
+          st_shared_v4(sp + (u >> 3) * C::kQChunkBytes + (((u & 7) ^ (t & 7)) << 4), pk[4 * u],
+                       pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      }
+      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_pv + 8 * i);
       l = alpha * l + rowsum;
       m = m_new;
-
-      if (driver) {
-        // O_i += P_i V_j once all 128 rows wrote P and O_i is rescaled; then,
-        // when that MMA has completed (P_i aliases S_i), S_i = Q_i K_{j+1}^T.
-        ok = warp_wait(bar_pv + 8 * i, jj & 1, wc) && kv_ready(2 * jj + 1);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(jj);
-        if (jj + 1 < n) {
-          ok = warp_wait(bar_o + 8 * i, jj & 1, wc) && kv_ready(2 * jj + 2);
-          if (!ok) break;
-          tc_fence_after();
-          issue_qk(jj + 1);
-        }
-      }
-    }
-    if (driver && issued_any) {
-      // Everything this warp issued completes before TMEM may be freed.
-      if (lane == 0) mma_commit(bar_drain + 8 * i);
-      __syncwarp();
-      wait_own(bar_drain + 8 * i, 0, p.timeout_ns);
     }
     if (ok && n > 0) ok = warp_wait(bar_o + 8 * i, (n - 1) & 1, wc);
     const bool bad = named_bar_or(1 + i, 128, !ok || *wc.abort);
