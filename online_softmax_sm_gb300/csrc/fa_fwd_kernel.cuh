@@ -27,12 +27,13 @@
 //   last WG       warp 0: TMA producer (one thread): Q once, then K and V
 //                 tiles through a ring of shared-memory stages, K one step
 //                 ahead of V (see ring_pos_k / ring_pos_v).
-//                 Warp 1: MMA issuer.  Warp-uniform code, one elected lane
-//                 issues; a small scheduler issues whichever MMA has its
-//                 inputs: S_i = Q_i K_{j+1}^T as soon as every row of tile i
-//                 has read S_i(j) (so it overlaps that step's exponentials),
-//                 O_i += P_i V_j once P_i and the O rescale are in place.
-//                 Warp 2 allocates TMEM.  Warp 3 idles.
+//                 Warp 1 + i: MMA issuer of tile i (warp-uniform code, one
+//                 elected lane issues, blocking barrier waits):
+//                 S_i(j+1) = Q_i K_{j+1}^T as soon as every row of tile i has
+//                 read S_i(j) (so it overlaps that step's exponentials), then
+//                 O_i += P_i(j) V_j once P_i(j) and the O rescale are in place.
+//                 The two tiles' issuers run side by side and keep the tensor
+//                 queue fed.  Warp 3 allocates TMEM.
 // setmaxnreg moves registers from the producer and correction warpgroups to
 // the softmax warpgroups.
 // TMEM (fp32 columns): S_i at [i*BC, (i+1)*BC), O_i at [QT*BC + i*D, ..+D).
@@ -59,8 +60,8 @@ struct FwdCfg {
   static constexpr int kBr = 128;  // query rows per tile (= TMEM lanes)
   static constexpr int kCorrWG = QT;             // correction warpgroup
   static constexpr int kLoadWarp = 4 * (QT + 1);  // first warp of the last WG
-  static constexpr int kMmaWarp = kLoadWarp + 1;
-  static constexpr int kAllocWarp = kLoadWarp + 2;
+  static constexpr int kMmaWarp0 = kLoadWarp + 1;  // + i: issuer of tile i
+  static constexpr int kAllocWarp = kLoadWarp + 3;
   static constexpr int kThreads = 4 * (QT + 2) * 32;
   // Registers per thread at launch (65536 / threads, multiple of 8) and the
   // setmaxnreg split that moves them to the softmax warpgroups.  The split must
@@ -105,7 +106,7 @@ struct __align__(8) Ctl {
   uint64_t alpha_free[2];   // alpha_i(j) read by the correction (128 arrivals)
   uint64_t pv_ready[2];     // P_i(j) in shared memory and O_i rescaled (128 + 128 arrivals)
   uint64_t o_done[2];       // O_i += P_i(j) V_j completed (MMA commit)
-  uint64_t drain;           // every MMA issued has completed
+  uint64_t drain[2];        // every MMA of tile i's issuer has completed
   uint32_t tmem_base;
   int abort;
   float alpha[2][128];      // per-row rescale factor, softmax -> correction
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
   const uint32_t bar_afree = smem_u32(&ctl->alpha_free[0]);
   const uint32_t bar_pv = smem_u32(&ctl->pv_ready[0]);
   const uint32_t bar_o = smem_u32(&ctl->o_done[0]);
-  const uint32_t bar_drain = smem_u32(&ctl->drain);
+  const uint32_t bar_drain = smem_u32(&ctl->drain[0]);
 
   // ---- setup
   if (threadIdx.x == 0) {
@@ -238,8 +239,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
       mbar_init(bar_afree + 8 * i, 128);
       mbar_init(bar_pv + 8 * i, 256);
       mbar_init(bar_o + 8 * i, 1);
+      mbar_init(bar_drain + 8 * i, 1);
     }
-    mbar_init(bar_drain, 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -318,123 +319,81 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
       if (qbytes) wait_own(bar_q, 0, p.timeout_ns);
       }
       __syncwarp();
-    } else if (warp == C::kMmaWarp) {
-      // ============================================================ MMA issuer
+    } else if (warp >= C::kMmaWarp0 && warp < C::kMmaWarp0 + QT) {
+      // ====================================================== MMA issuer, tile i
+      const int i = warp - C::kMmaWarp0;
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BC, false);  // K-major A (Q), B (K)
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);    // A = P K-major, B = V MN-major
       // Descriptor templates; the start-address field (bits 0-13, address >> 4)
       // of a shared address below 256 KB never carries, so per-MMA offsets are
       // plain 32-bit adds to the low word.
-      const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dp0 = smem_desc_sw128(smem_u32(sP), 16, 1024);
+      const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ + i * C::kQTileBytes), 16, 1024);
+      const uint64_t dp0 = smem_desc_sw128(smem_u32(sP + i * C::kPTileBytes), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sKV), 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(sKV), C::kKVChunkBytes, 1024);
       const uint64_t hi_q = dq0 & 0xFFFFFFFF00000000ull, hi_p = dp0 & 0xFFFFFFFF00000000ull,
                      hi_k = dk0 & 0xFFFFFFFF00000000ull, hi_v = dv0 & 0xFFFFFFFF00000000ull;
       const uint32_t lo_q = static_cast<uint32_t>(dq0), lo_p = static_cast<uint32_t>(dp0),
                      lo_k = static_cast<uint32_t>(dk0), lo_v = static_cast<uint32_t>(dv0);
-      int qk[QT], pv[QT];  // next step whose S_i / O_i MMA is not issued yet
-#pragma unroll
-      for (int i = 0; i < QT; ++i) qk[i] = pv[i] = 0;
-      auto probe = [&](uint32_t bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_test(bar, parity));
-      };
+      const uint32_t tS = tmem + C::kSCol + i * BC, tO = tmem + C::kOCol + i * D;
+      const int n = n_i[i];
       const int n_cta = kv_end_cta - kv_begin;
-      bool ok = n_cta > 0;
-      if (ok) ok = warp_wait(bar_q, 0, wc);
-      if (ok) tc_fence_after();
-      uint32_t idle = 0;
-      uint64_t t_idle = 0;
-      int last = QT - 1;
-      while (ok) {
-        bool all_done = true, issued = false;
-        int sleep_i = -1;
+      auto kv_ready = [&](int pos) {
+        return warp_wait(bar_kv_full + 8 * (pos % C::kStages), (pos / C::kStages) & 1, wc);
+      };
+      auto issue_qk = [&](int q) {  // S_i(q) = Q_i K_q^T, then release K_q's slot for tile i
+        const int stage = ring_pos_k(q) % C::kStages;
+        const uint32_t k_lo = lo_k + ((stage * C::kKVTileBytes) >> 4);
 #pragma unroll
-        for (int r = 0; r < QT; ++r) {
-          const int i = (last + 1 + r) % QT;
-          if (pv[i] >= n_i[i]) continue;
-          all_done = false;
-          if (sleep_i < 0) sleep_i = i;
-          const int q = qk[i];
-          if (q < n_i[i] && q <= pv[i] + 1) {
-            // S_i(q) = Q_i K_q^T: needs K_q and every row done reading S_i(q-1).
-            const int pos = ring_pos_k(q);
-            const int stage = pos % C::kStages;
-            if (probe(bar_kv_full + 8 * stage, (pos / C::kStages) & 1) &&
-                (q == 0 || probe(bar_sfree + 8 * i, (q - 1) & 1))) {
-              tc_fence_after();
-              const uint32_t q_lo = lo_q + ((i * C::kQTileBytes) >> 4);
-              const uint32_t k_lo = lo_k + ((stage * C::kKVTileBytes) >> 4);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_q = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
+          const uint32_t off_k = ((kk / 4) * C::kKVChunkBytes + (kk % 4) * 32) >> 4;
+          mma_bf16_ss_elect(tS, hi_q | (lo_q + off_q), hi_k | (k_lo + off_k), kIdescQK, kk > 0);
+        }
+        mma_commit_elect(bar_s + 8 * i);
+        mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
+      };
+      auto issue_pv = [&](int v) {  // O_i += P_i(v) V_v, then release V_v's slot for tile i
+        const int stage = ring_pos_v(v, n_cta) % C::kStages;
+        const uint32_t v_lo = lo_v + ((stage * C::kKVTileBytes) >> 4);
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off_q = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
-                const uint32_t off_k = ((kk / 4) * C::kKVChunkBytes + (kk % 4) * 32) >> 4;
-                mma_bf16_ss_elect(tmem + C::kSCol + i * BC, hi_q | (q_lo + off_q),
-                                  hi_k | (k_lo + off_k), kIdescQK, kk > 0);
-              }
-              mma_commit_elect(bar_s + 8 * i);
-              mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
-              qk[i] = q + 1;
-              last = i;
-              issued = true;
-              break;
-            }
-          }
-          const int v = pv[i];
-          if (v < qk[i]) {
-            // O_i += P_i(v) V_v: needs V_v, P_i(v) in smem and O_i rescaled.
-            const int pos = ring_pos_v(v, n_cta);
-            const int stage = pos % C::kStages;
-            if (probe(bar_kv_full + 8 * stage, (pos / C::kStages) & 1) &&
-                probe(bar_pv + 8 * i, v & 1)) {
-              tc_fence_after();
-              const uint32_t p_lo = lo_p + ((i * C::kPTileBytes) >> 4);
-              const uint32_t v_lo = lo_v + ((stage * C::kKVTileBytes) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < BC / 16; ++kk) {
-                // P: 16 keys of the K-major tile.  V: 16 keys = two 8-row groups
-                // (SBO 1024 B); D columns in 64-wide chunks BC*128 B apart (LBO).
-                const uint32_t off_p = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
-                mma_bf16_ss_elect(tmem + C::kOCol + i * D, hi_p | (p_lo + off_p),
-                                  hi_v | (v_lo + ((kk * 2048) >> 4)), kIdescPV,
-                                  (v > 0 || kk > 0) ? 1u : 0u);
-              }
-              mma_commit_elect(bar_o + 8 * i);
-              mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
-              pv[i] = v + 1;
-              last = i;
-              issued = true;
-              break;
-            }
-          }
+        for (int kk = 0; kk < BC / 16; ++kk) {
+          // P: 16 keys of the K-major tile.  V: 16 keys = two 8-row groups
+          // (SBO 1024 B); D columns in 64-wide chunks BC*128 B apart (LBO).
+          const uint32_t off_p = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
+          mma_bf16_ss_elect(tO, hi_p | (lo_p + off_p), hi_v | (v_lo + ((kk * 2048) >> 4)), kIdescPV,
+                            (v > 0 || kk > 0) ? 1u : 0u);
         }
-        if (all_done) break;
-        if (issued) {
-          idle = 0;
-          continue;
-        }
-        // Nothing ready: sleep briefly on the next input tile sleep_i waits for
-        // rather than spin on issue slots the softmax warps need.
-        if (pv[sleep_i] < qk[sleep_i])
-          mbar_try_wait_hint(bar_pv + 8 * sleep_i, pv[sleep_i] & 1, 100);
-        else if (qk[sleep_i] > 0)
-          mbar_try_wait_hint(bar_sfree + 8 * sleep_i, (qk[sleep_i] - 1) & 1, 100);
-        if ((idle++ & 63) == 0) {
-          const uint64_t now = global_timer_ns();
-          if (idle == 1) t_idle = now;
-          if (__any_sync(0xffffffffu, *wc.abort != 0)) break;
-          if (now - t_idle > p.timeout_ns) {
-            if (lane == 0) {
-              *wc.abort = 1;
-              atomicExch(p.status, kDevTimeout);
-            }
-            break;
-          }
-        }
+        mma_commit_elect(bar_o + 8 * i);
+        mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
+      };
+      bool ok = n > 0;
+      bool issued = false;
+      if (ok) ok = warp_wait(bar_q, 0, wc) && kv_ready(ring_pos_k(0));
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0);
+        issued = true;
       }
-      // Everything issued above completes before TMEM may be freed.
-      mma_commit_elect(bar_drain);
-      wait_own(bar_drain, 0, p.timeout_ns);
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n) {
+          // S_i(j+1) once every row read S_i(j)
+          ok = warp_wait(bar_sfree + 8 * i, j & 1, wc) && kv_ready(ring_pos_k(j + 1));
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk(j + 1);
+        }
+        // O_i += P_i(j) V_j once P_i(j) is in shared memory and O_i rescaled
+        ok = warp_wait(bar_pv + 8 * i, j & 1, wc) && kv_ready(ring_pos_v(j, n_cta));
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(j);
+      }
+      if (issued) {
+        // Everything issued above completes before TMEM may be freed.
+        mma_commit_elect(bar_drain + 8 * i);
+        wait_own(bar_drain + 8 * i, 0, p.timeout_ns);
+      }
       __syncwarp();
     }
   } else if (wg == C::kCorrWG) {
