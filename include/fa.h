@@ -54,6 +54,7 @@ extern "C" {
 #define FA_ERR_CUDA (-3)           /* a CUDA call failed; fa_strerror() has details */
 #define FA_ERR_DEVICE_TIMEOUT (-4) /* a kernel wait ran out (fa_get_device_status) */
 #define FA_ERR_NO_MEMORY (-5)      /* the split-KV workspace could not be allocated */
+#define FA_ERR_SCRATCH_TOO_SMALL (-6) /* fa_fwd_split_noalloc: workspace over the fixed limit */
 
 /*
  * Attention forward, O and LSE.
@@ -137,6 +138,37 @@ int fa_get_device_status(void* stream);
 /* Static description of an FA_* code; for FA_ERR_CUDA, the text of the last
  * CUDA error seen by this thread.  Never NULL. */
 const char* fa_strerror(int code);
+
+/*
+ * Split-KV forward that allocates nothing.  No counterpart on the source
+ * pages: this is a deployment variant of fa_fwd with n_splits > 1.
+ *
+ * For callers that cannot allocate device memory on this path: code that is
+ * replayed from an already-captured CUDA graph, allocator-free runtimes, or
+ * hosts whose device memory is owned by their own pool.  fa_fwd takes its
+ * split-KV workspace with cudaMallocAsync; this call puts the same partial
+ * (m, l, O) triples in a fixed device array of FA_NOALLOC_SCRATCH_BYTES that
+ * every GPU loading the library holds until the process exits, then merges
+ * them exactly as fa_fwd does (fa_fwd_partial + fa_merge_splits).
+ *
+ * Arguments and results: as fa_fwd (q, k, v, o, lse, sizes, scale, causal,
+ * stream), with 2 <= n_splits <= 65535, clamped to ceil(Nk/128) like fa_fwd;
+ * if that leaves one split, the call is fa_fwd with n_splits = 1.
+ * The workspace needs about n_splits * B*H*Nq * (d + 2) * 4 bytes; a call
+ * that needs more than FA_NOALLOC_SCRATCH_BYTES returns
+ * FA_ERR_SCRATCH_TOO_SMALL before launching anything.
+ *
+ * No cudaMalloc, cudaFree or other allocating call is made.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.
+ * All calls share the one array and it keeps the last call's contents:
+ * calls that may overlap on the GPU (different streams, or different host
+ * threads without ordering) race on it and must be serialised by the caller.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int Nq, int Nk, int d, float scale, int causal, int n_splits,
+                         void* stream);
 
 /* Library ABI version (major * 100 + minor). */
 int fa_version(void);

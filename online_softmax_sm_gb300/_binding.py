@@ -22,6 +22,8 @@ FA_ERR_UNSUPPORTED = -2
 FA_ERR_CUDA = -3
 FA_ERR_DEVICE_TIMEOUT = -4
 FA_ERR_NO_MEMORY = -5
+FA_ERR_SCRATCH_TOO_SMALL = -6
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 class FaOpts(ctypes.Structure):
@@ -59,6 +61,8 @@ def _declare(L):
     L.fa_strerror.restype = ctypes.c_char_p
     L.fa_version.argtypes = []
     L.fa_version.restype = _i
+    L.fa_fwd_split_noalloc.argtypes = L.fa_fwd.argtypes
+    L.fa_fwd_split_noalloc.restype = _i
 
 
 def lib():
@@ -175,6 +179,25 @@ def merge_splits(m_part, l_part, o_part, out=None, lse=None, stream=None):
                                out.data_ptr(), lse.data_ptr(), B, H, Nq, d, S,
                                _stream_handle(dev, stream))
     _check(rc, "fa_merge_splits")
+    return out, lse
+
+
+def fwd_split_noalloc(q, k, v, n_splits: int, scale: float | None = None, causal: bool = False,
+                      out=None, lse=None, stream=None):
+    """fa_fwd_split_noalloc: split-KV forward whose workspace is the library's
+    fixed device scratch (no allocation on the call path).  Calls that may
+    overlap on the GPU share that scratch and must be serialised by the caller."""
+    B, H, Nq, Nk, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = d ** -0.5
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        rc = lib().fa_fwd_split_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                        lse.data_ptr(), B, H, Nq, Nk, d, float(scale),
+                                        int(bool(causal)), int(n_splits),
+                                        _stream_handle(q.device, stream))
+    _check(rc, "fa_fwd_split_noalloc")
     return out, lse
 
 

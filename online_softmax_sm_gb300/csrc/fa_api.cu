@@ -318,6 +318,8 @@ const char* fa_strerror(int code) {
     case FA_ERR_UNSUPPORTED: return "unsupported (head dim must be 64 or 128; device must be sm_103)";
     case FA_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out; the affected CTAs stopped without writing";
     case FA_ERR_NO_MEMORY: return "could not allocate the split-KV workspace";
+    case FA_ERR_SCRATCH_TOO_SMALL:
+      return "split-KV workspace larger than the fixed no-alloc scratch (FA_NOALLOC_SCRATCH_BYTES)";
     case FA_ERR_CUDA:
       std::snprintf(t_msg, sizeof(t_msg), "CUDA error %d: %s", static_cast<int>(t_last_cuda),
                     cudaGetErrorString(t_last_cuda));
