@@ -57,10 +57,19 @@ def parse():
 
 
 def workload_of(name: str) -> workloads.Workload:
+    """c1..c5 / c4_masked, a full workload name, or custom:B,H,Nq,Nk,d[,causal[,n_splits[,seed]]]
+    (smaller cases for profiling)."""
     if name in WORKLOAD_ALIASES:
         return WORKLOAD_ALIASES[name]
     if name in workloads.WORKLOADS:
         return workloads.WORKLOADS[name]
+    if name.startswith("custom:"):
+        f = [int(x) for x in name[len("custom:"):].split(",")]
+        B, H, Nq, Nk, d = f[:5]
+        causal = bool(f[5]) if len(f) > 5 else False
+        n_splits = f[6] if len(f) > 6 else 1
+        seed = f[7] if len(f) > 7 else 0
+        return workloads.custom(B, H, Nq, Nk, d, seed=seed, causal=causal, n_splits=n_splits)
     raise SystemExit(f"unknown workload {name}")
 
 
