@@ -194,7 +194,8 @@ def dist_setup(n_gpus: int):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        if not dist.is_initialized():
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return world, rank, local
 
 
@@ -205,6 +206,13 @@ def max_over_ranks(x: float, world: int, device) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(world: int, flops_per_rank: float, ms_local: float, device) -> tuple[float, float]:
+    """Replicas: every rank ran the same workload.  Returns (max ms over ranks,
+    whole-job TFLOP/s = world * flops / max time)."""
+    ms = max_over_ranks(ms_local, world, device)
+    return ms, world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
 def barrier(world: int):
@@ -371,8 +379,7 @@ def run_ours(args, w):
         raise SystemExit("device status reports a timed-out wait")
     step_ms = [a.elapsed_time(b) for a, b in evs]
     ms_local = statistics.mean(step_ms)
-    ms = max_over_ranks(ms_local, world, dev)
-    value = world * w.flops / (ms * 1e-3) / 1e12
+    ms, value = aggregate(world, w.flops, ms_local, dev)
 
     # ---- dominant kernel: the forward kernel (split: time it alone via fa_fwd_partial)
     peaks, peak_src = load_peaks()
