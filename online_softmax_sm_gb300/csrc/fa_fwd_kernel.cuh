@@ -398,27 +398,51 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
     }
   } else if (wg == C::kCorrWG) {
     // ========================================================= correction
+    // Serves the tiles in whatever order their inputs arrive: per tile,
+    // (1) read alpha_i(j) as soon as it is published and release the slot,
+    // (2) once O_i += P_i(j-1) V_{j-1} has completed, O_i <- alpha O_i, then
+    // let the MMA warp issue O_i += P_i(j) V_j.
     if constexpr (C::kRegCorr < C::kRegLaunch) setmaxnreg_dec<C::kRegCorr>();
     const int t = threadIdx.x & 127;
-    int n_max = 0;
+    int jn[QT];        // next step of tile i
+    bool have[QT];     // alpha_i(jn) read, waiting for the previous P.V
+    float alpha_r[QT];
 #pragma unroll
-    for (int i = 0; i < QT; ++i) n_max = max(n_max, n_i[i]);
+    for (int i = 0; i < QT; ++i) {
+      jn[i] = 0;
+      have[i] = false;
+      alpha_r[i] = 1.f;
+    }
+    auto probe = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_test(bar, parity));
+    };
+    uint32_t idle = 0;
+    uint64_t t_idle = 0;
     bool ok = true;
-    for (int jj = 0; ok && jj < n_max; ++jj) {
+    while (ok) {
+      bool done = true, progressed = false;
+      int sleep_i = -1;
 #pragma unroll
       for (int i = 0; i < QT; ++i) {
-        if (jj >= n_i[i]) continue;
-        if (!__all_sync(0xffffffffu, wait_bounded(bar_alpha + 8 * i, jj & 1, wc))) {
-          ok = false;
-          break;
+        const int j = jn[i];
+        if (j >= n_i[i]) continue;
+        done = false;
+        if (!have[i]) {
+          if (!probe(bar_alpha + 8 * i, j & 1)) {
+            if (sleep_i < 0) sleep_i = i;
+            continue;
+          }
+          alpha_r[i] = ctl->alpha[i][t];
+          mbar_arrive(bar_afree + 8 * i);  // the softmax may publish alpha_i(j+1)
+          have[i] = true;
+          progressed = true;
         }
-        const float alpha = ctl->alpha[i][t];
-        mbar_arrive(bar_afree + 8 * i);  // the softmax may publish alpha_i(j+1)
-        if (jj > 0 && !__all_sync(0xffffffffu, wait_bounded(bar_o + 8 * i, (jj - 1) & 1, wc))) {
-          ok = false;
-          break;
-        }
-        if (jj > 0) {
+        if (j > 0) {
+          if (!probe(bar_o + 8 * i, (j - 1) & 1)) {
+            if (sleep_i < 0) sleep_i = i;
+            continue;
+          }
+          const float alpha = alpha_r[i];
           if (__any_sync(0xffffffffu, alpha != 1.f)) {
             tc_fence_after();
             const uint32_t tO = tmem + lane_off + C::kOCol + i * D;
@@ -441,6 +465,34 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(bar_pv + 8 * i);
+        have[i] = false;
+        jn[i] = j + 1;
+        progressed = true;
+      }
+      if (done) break;
+      if (progressed) {
+        idle = 0;
+        continue;
+      }
+      // Nothing ready: sleep briefly on the first pending input.
+      {
+        const int i = sleep_i;
+        if (!have[i])
+          mbar_try_wait_hint(bar_alpha + 8 * i, jn[i] & 1, 100);
+        else
+          mbar_try_wait_hint(bar_o + 8 * i, (jn[i] - 1) & 1, 100);
+      }
+      if ((idle++ & 63) == 0) {
+        const uint64_t now = global_timer_ns();
+        if (idle == 1) t_idle = now;
+        if (__any_sync(0xffffffffu, *wc.abort != 0)) break;
+        if (now - t_idle > p.timeout_ns) {
+          if ((threadIdx.x & 31) == 0) {
+            *wc.abort = 1;
+            atomicExch(p.status, kDevTimeout);
+          }
+          break;
+        }
       }
     }
   } else {
