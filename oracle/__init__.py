@@ -9,6 +9,7 @@ The arithmetic lives in oracle.c (plain C, fp64); this module is ctypes
 marshalling plus per-head looping:
 
   attention(q, k, v, scale, causal, rows)     one head, three-pass definition
+  attention_window(q, k, v, scale, wl, wr)     one head, local (sliding-window) mask
   attention_bhnd(q, k, v, scale, causal, ...) [B,H,N,d] tensors, head by head
   online_blocks(s, v, blocks)                 blockwise (m, l, O) recurrence
   merge(m, l, o)                              two-block merge rule, folded
@@ -49,6 +50,9 @@ def _declare(lib):
     lib.oracle_attention.argtypes = [_dp, _i64, _dp, _dp, _i64, _i64, ctypes.c_double,
                                      ctypes.c_int, _ip, _i64, _dp, _dp, ctypes.c_int]
     lib.oracle_attention.restype = ctypes.c_int
+    lib.oracle_attention_window.argtypes = [_dp, _i64, _dp, _dp, _i64, _i64, ctypes.c_double,
+                                            _i64, _i64, _ip, _i64, _dp, _dp, ctypes.c_int]
+    lib.oracle_attention_window.restype = ctypes.c_int
     lib.oracle_online_blocks.argtypes = [_dp, _dp, _i64, _i64, _ip, _ip, _i64,
                                          _dp, _dp, _dp, _dp]
     lib.oracle_online_blocks.restype = ctypes.c_int
@@ -95,6 +99,32 @@ def attention(q, k, v, scale: float, causal: bool = False, rows: Sequence[int] |
                               _ptr(o), _ptr(lse), int(threads or default_threads()))
     if rc != 0:
         raise ValueError("oracle_attention: bad argument")
+    return o, lse
+
+
+def attention_window(q, k, v, scale: float, window_left: int, window_right: int,
+                     rows: Sequence[int] | None = None, threads: int | None = None, lib=None):
+    """One head with the local window: key j visible to query i iff
+    i + (nk - nq) - window_left <= j <= i + (nk - nq) + window_right (a negative
+    bound leaves that side open).  Returns (o, lse) like attention()."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    nq, d = q.shape
+    nk = k.shape[0]
+    assert k.shape == (nk, d) and v.shape == (nk, d)
+    if rows is None:
+        rows_arr, nrows = None, nq
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.shape[0]
+    o = np.empty((nrows, d), dtype=np.float64)
+    lse = np.empty((nrows,), dtype=np.float64)
+    rc = lib.oracle_attention_window(_ptr(q), nq, _ptr(k), _ptr(v), nk, d, float(scale),
+                                     int(window_left), int(window_right),
+                                     None if rows_arr is None else _ptr(rows_arr, _ip), nrows,
+                                     _ptr(o), _ptr(lse), int(threads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_attention_window: bad argument")
     return o, lse
 
 

@@ -27,8 +27,15 @@
  *                         Milakov & Gimelshein two-pass normaliser
  *                         ("Online Softmax 算法详解" section 2.2).
  *
+ *   oracle_attention_window
+ *                         the same with a local (sliding-window) mask.
+ *
  * Causal convention (not fixed by the pages; the reading used throughout):
  * key j is visible to query i iff j <= i + (nk - nq)  (bottom-right aligned).
+ * Local window (named but not defined by the pages, "Online Softmax 算法详解"
+ * section 3.2; the reading used throughout): key j is visible to query i iff
+ * i + off - wl <= j <= i + off + wr with off = nk - nq; a negative wl or wr
+ * leaves that side unbounded.  Causal is the window (-1, 0).
  *
  * All routines are re-entrant.  oracle_attention splits its rows over
  * `nthreads` POSIX threads (nthreads <= 0 means one thread).
@@ -46,12 +53,12 @@
 /* One query row.  s is caller scratch of nk doubles. */
 static void attention_row(const double *qi, const double *k, const double *v,
                           int64_t nk, int64_t d, double scale,
-                          int64_t last_visible, double *s, double *oi,
-                          double *lse_i)
+                          int64_t first_visible, int64_t last_visible,
+                          double *s, double *oi, double *lse_i)
 {
     /* Materialise the score row S_j = scale * <q_i, k_j>; -inf where masked. */
     for (int64_t j = 0; j < nk; ++j) {
-        if (j > last_visible) {
+        if (j > last_visible || j < first_visible) {
             s[j] = -INFINITY;
             continue;
         }
@@ -98,6 +105,7 @@ typedef struct {
     int64_t nq, nk, d;
     double scale;
     int causal;
+    int64_t wl, wr; /* window (used when causal == 2) */
     const int64_t *rows;
     int64_t row_begin, row_end;
     double *o, *lse;
@@ -114,10 +122,16 @@ static void *attention_worker(void *arg)
     }
     for (int64_t r = job->row_begin; r < job->row_end; ++r) {
         int64_t i = job->rows ? job->rows[r] : r;
+        int64_t first_visible = 0;
         int64_t last_visible = job->causal ? i + (job->nk - job->nq) : job->nk - 1;
+        if (job->causal == 2) { /* local window */
+            int64_t off = job->nk - job->nq;
+            first_visible = job->wl < 0 ? 0 : i + off - job->wl;
+            last_visible = job->wr < 0 ? job->nk - 1 : i + off + job->wr;
+        }
         attention_row(job->q + i * job->d, job->k, job->v, job->nk, job->d,
-                      job->scale, last_visible, s, job->o + r * job->d,
-                      job->lse + r);
+                      job->scale, first_visible, last_visible, s,
+                      job->o + r * job->d, job->lse + r);
     }
     free(s);
     job->status = 0;
@@ -130,10 +144,11 @@ static void *attention_worker(void *arg)
  * o [nrows][d], lse [nrows] : outputs, in the order of `rows`.
  * Returns 0, or -1 on a bad argument / allocation failure.
  */
-int oracle_attention(const double *q, int64_t nq, const double *k,
-                     const double *v, int64_t nk, int64_t d, double scale,
-                     int causal, const int64_t *rows, int64_t nrows,
-                     double *o, double *lse, int nthreads)
+static int run_attention(const double *q, int64_t nq, const double *k,
+                         const double *v, int64_t nk, int64_t d, double scale,
+                         int causal, int64_t wl, int64_t wr,
+                         const int64_t *rows, int64_t nrows, double *o,
+                         double *lse, int nthreads)
 {
     if (!q || !k || !v || !o || !lse || nq < 0 || nk < 0 || d <= 0 || nrows < 0)
         return -1;
@@ -160,6 +175,7 @@ int oracle_attention(const double *q, int64_t nq, const double *k,
         job->q = q; job->k = k; job->v = v;
         job->nq = nq; job->nk = nk; job->d = d;
         job->scale = scale; job->causal = causal;
+        job->wl = wl; job->wr = wr;
         job->rows = rows;
         job->row_begin = (int64_t)t * per < nrows ? (int64_t)t * per : nrows;
         job->row_end = job->row_begin + per < nrows ? job->row_begin + per : nrows;
@@ -189,6 +205,26 @@ int oracle_attention(const double *q, int64_t nq, const double *k,
     free(jobs);
     free(tids);
     return rc;
+}
+
+int oracle_attention(const double *q, int64_t nq, const double *k,
+                     const double *v, int64_t nk, int64_t d, double scale,
+                     int causal, const int64_t *rows, int64_t nrows,
+                     double *o, double *lse, int nthreads)
+{
+    return run_attention(q, nq, k, v, nk, d, scale, causal ? 1 : 0, -1, -1,
+                         rows, nrows, o, lse, nthreads);
+}
+
+/* As oracle_attention, with the local window [i + off - wl, i + off + wr]. */
+int oracle_attention_window(const double *q, int64_t nq, const double *k,
+                            const double *v, int64_t nk, int64_t d,
+                            double scale, int64_t wl, int64_t wr,
+                            const int64_t *rows, int64_t nrows, double *o,
+                            double *lse, int nthreads)
+{
+    return run_attention(q, nq, k, v, nk, d, scale, 2, wl, wr, rows, nrows, o,
+                         lse, nthreads);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -328,3 +328,68 @@ def test_alpha_at_most_one_and_exp_args_nonpositive():
     s = rng.standard_normal(200) * 20
     m, l, _, _ = oracle.online_blocks(s, np.ones(200), [(j, 10) for j in range(0, 200, 10)])
     assert 1.0 <= l <= 200.0 and m == s.max()
+
+
+# ------------------------------------------------------------ local window
+
+def _window_mask(nq, nk, wl, wr):
+    ii = np.arange(nq)[:, None] + (nk - nq)
+    jj = np.arange(nk)[None, :]
+    vis = np.ones((nq, nk), dtype=bool)
+    if wl >= 0:
+        vis &= jj >= ii - wl
+    if wr >= 0:
+        vis &= jj <= ii + wr
+    return vis
+
+
+def test_window_reduces_to_causal_and_full():
+    rng = np.random.default_rng(31)
+    for nq, nk in ((9, 9), (5, 12), (12, 5)):
+        q, k, v = rng.standard_normal((nq, 4)), rng.standard_normal((nk, 4)), rng.standard_normal((nk, 4))
+        oc, lc = oracle.attention(q, k, v, 0.7, True)
+        ow, lw = oracle.attention_window(q, k, v, 0.7, -1, 0)
+        np.testing.assert_array_equal(oc, ow)
+        np.testing.assert_array_equal(lc, lw)
+        of, lf = oracle.attention(q, k, v, 0.7, False)
+        ow, lw = oracle.attention_window(q, k, v, 0.7, -1, -1)
+        np.testing.assert_array_equal(of, ow)
+        np.testing.assert_array_equal(lf, lw)
+
+
+@pytest.mark.parametrize("nq,nk,wl,wr,seed", [
+    (10, 10, 2, 0, 0), (10, 10, 3, 3, 1), (6, 14, 4, 1, 2), (14, 6, 0, 2, 3), (8, 8, -1, 2, 4), (8, 8, 1, -1, 5),
+])
+def test_window_matches_scipy_softmax(nq, nk, wl, wr, seed):
+    rng = np.random.default_rng(seed)
+    d = 3
+    q, k, v = rng.standard_normal((nq, d)) * 2, rng.standard_normal((nk, d)), rng.standard_normal((nk, d))
+    o, lse = oracle.attention_window(q, k, v, 0.5, wl, wr)
+    S = np.where(_window_mask(nq, nk, wl, wr), 0.5 * (q @ k.T), -np.inf)
+    for i in range(nq):
+        if np.all(np.isneginf(S[i])):
+            assert np.all(o[i] == 0.0) and lse[i] == -np.inf
+            continue
+        np.testing.assert_allclose(o[i], sps.softmax(S[i]) @ v, rtol=1e-12, atol=1e-13)
+        assert abs(lse[i] - sps.logsumexp(S[i])) < 1e-12
+
+
+def test_window_of_one_key_and_uniform_counts():
+    rng = np.random.default_rng(32)
+    nq, nk, d = 7, 9, 5
+    q, k, v = rng.standard_normal((nq, d)), rng.standard_normal((nk, d)), rng.standard_normal((nk, d))
+    off = nk - nq
+    # window (0, 0): each row sees exactly key i + off
+    o, lse = oracle.attention_window(q, k, v, 0.25, 0, 0)
+    for i in range(nq):
+        np.testing.assert_array_equal(o[i], v[i + off])
+        assert abs(lse[i] - 0.25 * (q[i] @ k[i + off])) < 1e-14
+    # Q = 0: O is the mean of the visible keys' values, LSE = ln(count)
+    o, lse = oracle.attention_window(np.zeros((nq, d)), k, v, 1.0, 2, 1)
+    for i in range(nq):
+        lo, hi = max(0, i + off - 2), min(nk - 1, i + off + 1)
+        np.testing.assert_allclose(o[i], v[lo:hi + 1].mean(axis=0), rtol=1e-13, atol=1e-14)
+        assert abs(lse[i] - np.log(hi - lo + 1)) < 1e-14
+    # a window entirely past the key axis leaves the row empty
+    o, lse = oracle.attention_window(q[:3], k[:2], v[:2], 1.0, 0, 0)  # off = -1: row 0 sees key -1
+    assert np.all(o[0] == 0.0) and lse[0] == -np.inf

@@ -23,7 +23,12 @@ if shutil.which("gcc") is None:  # pragma: no cover
 # (name, original text, mutated text): each original must occur exactly once.
 MUTANTS = [
     ("drop_scale", "s[j] = scale * acc;", "s[j] = acc;"),
-    ("mask_off_by_one", "if (j > last_visible) {", "if (j >= last_visible) {"),
+    ("mask_off_by_one", "if (j > last_visible ||", "if (j >= last_visible ||"),
+    ("window_left_ignored", "if (j > last_visible || j < first_visible) {", "if (j > last_visible) {"),
+    ("window_left_off_by_one", "first_visible = job->wl < 0 ? 0 : i + off - job->wl;",
+     "first_visible = job->wl < 0 ? 0 : i + off - job->wl + 1;"),
+    ("window_right_off_by_one", "last_visible = job->wr < 0 ? job->nk - 1 : i + off + job->wr;",
+     "last_visible = job->wr < 0 ? job->nk - 1 : i + off + job->wr + 1;"),
     ("causal_offset_sign", "i + (job->nk - job->nq)", "i - (job->nk - job->nq)"),
     ("k_feature_index", "qi[c] * k[j * d + c]", "qi[c] * k[j * d + (d - 1 - c)]"),
     ("v_feature_index", "oi[c] += p * v[j * d + c];", "oi[c] += p * v[j * d + (d - 1 - c)];"),
@@ -63,6 +68,7 @@ def _pin_calls():
         "test_zero_queries_average_visible_values": [(False,), (True,)],
         "test_online_blocks_match_three_pass": [(0,)],
         "test_merge_of_random_partition_matches_full": [(0,)],
+        "test_window_matches_scipy_softmax": [(10, 10, 2, 0, 0), (6, 14, 4, 1, 2), (14, 6, 0, 2, 3)],
     }
     calls = []
     for name, fn in inspect.getmembers(pins, inspect.isfunction):
