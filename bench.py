@@ -39,7 +39,8 @@ from online_softmax_sm_gb300 import workloads  # noqa: E402
 METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and % of dense BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 WORKLOAD_ALIASES = {"c1": workloads.C1, "c2": workloads.C2, "c3": workloads.C3, "c4": workloads.C4,
-                    "c4_masked": workloads.C4_MASKED, "c5": workloads.C5}
+                    "c4_masked": workloads.C4_MASKED, "c5": workloads.C5,
+                    "local": workloads.LOCAL}
 
 
 def parse():
@@ -57,7 +58,8 @@ def parse():
 
 
 def workload_of(name: str) -> workloads.Workload:
-    """c1..c5 / c4_masked, a full workload name, or custom:B,H,Nq,Nk,d[,causal[,n_splits[,seed]]]
+    """c1..c5 / c4_masked / local, a full workload name, or
+    custom:B,H,Nq,Nk,d[,causal[,n_splits[,seed[,window_left,window_right]]]]
     (smaller cases for profiling)."""
     if name in WORKLOAD_ALIASES:
         return WORKLOAD_ALIASES[name]
@@ -69,7 +71,9 @@ def workload_of(name: str) -> workloads.Workload:
         causal = bool(f[5]) if len(f) > 5 else False
         n_splits = f[6] if len(f) > 6 else 1
         seed = f[7] if len(f) > 7 else 0
-        return workloads.custom(B, H, Nq, Nk, d, seed=seed, causal=causal, n_splits=n_splits)
+        window = (f[8], f[9]) if len(f) > 9 else None
+        return workloads.custom(B, H, Nq, Nk, d, seed=seed, causal=causal, n_splits=n_splits,
+                                window=window)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -221,6 +225,39 @@ def barrier(world: int):
         dist.barrier()
 
 
+def row_flops(w: workloads.Workload, rows) -> float:
+    """Algorithmic FLOPs of the listed query rows: 4*d per visible key."""
+    off = w.Nk - w.Nq
+    if w.window is not None:
+        wl, wr = w.window
+        tot = 0
+        for r in rows:
+            lo = 0 if wl < 0 else max(0, r + off - wl)
+            hi = w.Nk - 1 if wr < 0 else min(w.Nk - 1, r + off + wr)
+            tot += max(0, hi - lo + 1)
+        return 4.0 * w.d * tot
+    if not w.causal:
+        return 4.0 * w.Nk * w.d * len(rows)
+    return float(sum(4.0 * max(0, min(w.Nk, r + off + 1)) * w.d for r in rows))
+
+
+def oracle_rows(w: workloads.Workload, qh, kh, vh, rows, threads):
+    """The oracle on listed rows of one head, with the workload's mask."""
+    import oracle
+
+    if w.window is not None:
+        return oracle.attention_window(qh, kh, vh, w.scale, w.window[0], w.window[1], rows=rows,
+                                       threads=threads)
+    return oracle.attention(qh, kh, vh, w.scale, w.causal, rows=rows, threads=threads)
+
+
+def forward(fa, w: workloads.Workload, q, k, v, o, lse):
+    """One call of the library's public forward for this workload's mask."""
+    if w.window is not None:
+        return fa.fwd_local(q, k, v, w.window[0], w.window[1], w.scale, w.n_splits, out=o, lse=lse)
+    return fa.fwd(q, k, v, w.scale, w.causal, w.n_splits, out=o, lse=lse, bc=w.bc)
+
+
 def cpu_oracle_sample(w: workloads.Workload, q, k, v, target_s: float, seed: int = 0):
     """Time the oracle on a bounded row sample of the workload; returns a dict."""
     import numpy as np
@@ -234,17 +271,11 @@ def cpu_oracle_sample(w: workloads.Workload, q, k, v, target_s: float, seed: int
     head = (0, 0)
     qh, kh, vh = (x[head[0], head[1]].cpu().double().numpy() for x in (q, k, v))
 
-    def row_flops(rows):
-        if not w.causal:
-            return 4.0 * w.Nk * w.d * len(rows)
-        off = w.Nk - w.Nq
-        return float(sum(4.0 * max(0, min(w.Nk, r + off + 1)) * w.d for r in rows))
-
     calib_rows = sorted(rng.choice(w.Nq, size=min(w.Nq, 256), replace=False).tolist())
     t0 = time.perf_counter()
-    oracle.attention(qh, kh, vh, w.scale, w.causal, rows=calib_rows, threads=threads)
+    oracle_rows(w, qh, kh, vh, calib_rows, threads)
     dt = time.perf_counter() - t0
-    rate = row_flops(calib_rows) / max(dt, 1e-9)
+    rate = row_flops(w, calib_rows) / max(dt, 1e-9)
     want_flops = rate * target_s
     total_rows = B * H * w.Nq
     avg_row = w.flops / total_rows
@@ -267,9 +298,9 @@ def cpu_oracle_sample(w: workloads.Workload, q, k, v, target_s: float, seed: int
         qh, kh, vh = (x[b, h].cpu().double().numpy() for x in (q, k, v))
         rr = rows if rows is not None else list(range(w.Nq))
         ts = time.perf_counter()
-        oracle.attention(qh, kh, vh, w.scale, w.causal, rows=rows, threads=threads)
+        oracle_rows(w, qh, kh, vh, rows, threads)
         elapsed += time.perf_counter() - ts
-        flops += row_flops(rr)
+        flops += row_flops(w, rr)
     return {"tflops": flops / elapsed / 1e12, "seconds": elapsed, "rows": n_rows,
             "heads": len(plan), "threads": threads, "flops": flops}
 
@@ -290,7 +321,7 @@ def run_reference(args, w):
     qh, kh, vh = (x[0, 0].double().numpy() for x in (q, k, v))
     rows = sorted(rng.choice(w.Nq, size=min(w.Nq, 128), replace=False).tolist())
     t0 = time.perf_counter()
-    oracle.attention(qh, kh, vh, w.scale, w.causal, rows=rows, threads=threads)
+    oracle_rows(w, qh, kh, vh, rows, threads)
     dt = time.perf_counter() - t0
     avg_row = w.flops / (w.B * w.H * w.Nq)
     rows_per_step = int(max(32, min(w.Nq, len(rows) * per_step_s / max(dt, 1e-9))))
@@ -303,7 +334,7 @@ def run_reference(args, w):
             heads_np[(b, h)] = tuple(x[b, h].double().numpy() for x in (q, k, v))
         qh, kh, vh = heads_np[(b, h)]
         rr = sorted(rng.choice(w.Nq, size=rows_per_step, replace=False).tolist())
-        oracle.attention(qh, kh, vh, w.scale, w.causal, rows=rr, threads=threads)
+        oracle_rows(w, qh, kh, vh, rr, threads)
         return rr
 
     for i in range(args.warmup):
@@ -313,11 +344,7 @@ def run_reference(args, w):
         t0 = time.perf_counter()
         rr = step(args.warmup + i)
         times.append(time.perf_counter() - t0)
-        if w.causal:
-            off = w.Nk - w.Nq
-            flops += sum(4.0 * max(0, min(w.Nk, r + off + 1)) * w.d for r in rr)
-        else:
-            flops += 4.0 * w.Nk * w.d * len(rr)
+        flops += row_flops(w, rr)
     total = sum(times)
     value = flops / total / 1e12
     line = {
@@ -350,7 +377,7 @@ def run_ours(args, w):
     launches_per_step = 1 if w.n_splits <= 1 else 2
 
     def step():
-        fa.fwd(q, k, v, w.scale, w.causal, w.n_splits, out=o, lse=lse, bc=w.bc)
+        forward(fa, w, q, k, v, o, lse)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -383,7 +410,7 @@ def run_ours(args, w):
 
     # ---- dominant kernel: the forward kernel (split: time it alone via fa_fwd_partial)
     peaks, peak_src = load_peaks()
-    if w.n_splits > 1:
+    if w.n_splits > 1 and w.window is None:
         m_p = torch.empty((w.n_splits, w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
         l_p = torch.empty_like(m_p)
         o_p = torch.empty((w.n_splits, w.B, w.H, w.Nq, w.d), dtype=torch.float32, device=dev)
@@ -427,7 +454,7 @@ def run_ours(args, w):
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
-            fa.fwd(dq, dk, dv, w.scale, w.causal, w.n_splits, out=o, lse=lse, bc=w.bc)
+            forward(fa, w, dq, dk, dv, o, lse)
             ho.copy_(o, non_blocking=True)
             hl.copy_(lse, non_blocking=True)
 
@@ -464,6 +491,7 @@ def run_ours(args, w):
             "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
                        "causal": w.causal, "n_splits": w.n_splits, "scale": w.scale,
                        "q_mult": w.q_mult, "k_ramp": w.k_ramp, "seed": w.seed,
+                       "window": list(w.window) if w.window is not None else None,
                        "l2": "flushed before every timed step (512 MB write); inputs > L2",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "tensor_peak_frac": value / world / float(peaks["bf16_tflops"])},

@@ -76,6 +76,21 @@ extern "C" {
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
            int Nk, int d, float scale, int causal, int n_splits, void* stream);
 
+/*
+ * Attention forward with a local (sliding-window) mask, "causal, local" masks
+ * of "Online Softmax 算法详解" section 3.2 (which names the local mask without
+ * defining it).  With off = Nk - Nq, key j is visible to query i iff
+ *   i + off - window_left <= j <= i + off + window_right,
+ * and a bound of -1 leaves that side open: (-1, 0) is fa_fwd's causal mask and
+ * (-1, -1) the unmasked forward.  K/V tiles wholly outside a query tile's
+ * window are skipped.  Rows that see no key get O = 0 and LSE = -inf.
+ * Arguments otherwise as fa_fwd (n_splits > 1 = split-KV with merge);
+ * window_left, window_right in [-1, 2^30].
+ */
+int fa_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int Nq, int Nk, int d, float scale, int window_left, int window_right, int n_splits,
+                 void* stream);
+
 /* Options for fa_fwd_ex.  Zero-initialise, then set what you need. */
 typedef struct fa_opts {
   int bc;                     /* K/V tile rows: 0 = default (128), or 64 or 128 */

@@ -4,6 +4,7 @@ The compute path is libfa.so (hand-written CUDA, C ABI in include/fa.h); this
 package is its Python binding plus the seeded workload generators:
 
   fwd(q, k, v, scale, causal, n_splits)   -> (o, lse)       fa_fwd / fa_fwd_ex
+  fwd_local(q, k, v, wl, wr, ...)         -> (o, lse)       fa_fwd_local (sliding window)
   fwd_partial(q, k, v, n_splits, ...)     -> (m, l, o) parts fa_fwd_partial
   merge_splits(m_part, l_part, o_part)    -> (o, lse)       fa_merge_splits
   fwd_split_noalloc(q, k, v, n_splits)   -> (o, lse)       fa_fwd_split_noalloc
@@ -13,10 +14,10 @@ libfa.so is loaded on first use; importing the package loads nothing.
 """
 from ._binding import (FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT, FA_ERR_INVALID_ARG, FA_ERR_NO_MEMORY,
                        FA_ERR_SCRATCH_TOO_SMALL, FA_ERR_UNSUPPORTED, FA_OK, FAError, device_status,
-                       fwd, fwd_partial, fwd_split_noalloc, lib, merge_splits,
+                       fwd, fwd_local, fwd_partial, fwd_split_noalloc, lib, merge_splits,
                        split_workspace_bytes, strerror, version)
 
-__all__ = ["fwd", "fwd_partial", "merge_splits", "fwd_split_noalloc", "split_workspace_bytes",
+__all__ = ["fwd", "fwd_local", "fwd_partial", "merge_splits", "fwd_split_noalloc", "split_workspace_bytes",
            "device_status",
            "version", "strerror", "lib", "FAError", "FA_OK", "FA_ERR_INVALID_ARG",
            "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_NO_MEMORY",

@@ -63,6 +63,9 @@ def _declare(L):
     L.fa_version.restype = _i
     L.fa_fwd_split_noalloc.argtypes = L.fa_fwd.argtypes
     L.fa_fwd_split_noalloc.restype = _i
+    L.fa_fwd_local.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i,
+                               _i, _vp]
+    L.fa_fwd_local.restype = _i
 
 
 def lib():
@@ -140,6 +143,23 @@ def fwd(q, k, v, scale: float | None = None, causal: bool = False, n_splits: int
         else:
             rc = L.fa_fwd(*args)
     _check(rc, "fa_fwd")
+    return out, lse
+
+
+def fwd_local(q, k, v, window_left: int, window_right: int, scale: float | None = None,
+              n_splits: int = 1, out=None, lse=None, stream=None):
+    """fa_fwd_local: key j visible to query i iff
+    i + (Nk - Nq) - window_left <= j <= i + (Nk - Nq) + window_right (-1 = open side)."""
+    B, H, Nq, Nk, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = d ** -0.5
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        rc = lib().fa_fwd_local(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), B, H, Nq, Nk, d, float(scale), int(window_left),
+                                int(window_right), int(n_splits), _stream_handle(q.device, stream))
+    _check(rc, "fa_fwd_local")
     return out, lse
 
 

@@ -135,7 +135,7 @@ SplitLayout split_layout(long long rows, int d, int n_splits) {
 
 // Shared body of fa_fwd / fa_fwd_ex / fa_fwd_partial.
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
-             int Nk, int d, float scale, int causal, int n_splits, void* stream,
+             int Nk, int d, float scale, int wl, int wr, int n_splits, void* stream,
              const fa_opts* opts, float* m_part, float* l_part, float* o_part) {
   const bool partial = (m_part != nullptr);
   int rc = check_sizes(B, H, Nq, Nk, d, scale);
@@ -149,6 +149,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4)) return FA_ERR_INVALID_ARG;
   }
   if (n_splits < 1 || n_splits > 65535) return FA_ERR_INVALID_ARG;
+  if (wl < -1 || wr < -1 || wl > kMaxSeq || wr > kMaxSeq) return FA_ERR_INVALID_ARG;
   int bc = 128, qt_opt = 0, skip = -1;
   unsigned long long timeout = kDefaultTimeoutNs;
   if (opts) {
@@ -178,7 +179,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.partial = (partial || splits > 1) ? 1 : 0;
   p.kv_tiles = kv_tiles;
   p.tiles_per_split = (kv_tiles + splits - 1) / splits;
-  p.causal = causal ? 1 : 0;
+  p.causal = (wl < 0 && wr >= 0) ? 1 : 0;  // longest rows first
+  p.wl = wl;
+  p.wr = wr;
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.timeout_ns = timeout;
@@ -247,23 +250,30 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
            int Nk, int d, float scale, int causal, int n_splits, void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, stream, nullptr,
-                  nullptr, nullptr, nullptr);
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, -1, causal ? 0 : -1, n_splits, stream,
+                  nullptr, nullptr, nullptr, nullptr);
+}
+
+int fa_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int Nq, int Nk, int d, float scale, int window_left, int window_right, int n_splits,
+                 void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, window_left, window_right, n_splits,
+                  stream, nullptr, nullptr, nullptr, nullptr);
 }
 
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
               int Nq, int Nk, int d, float scale, int causal, int n_splits, void* stream,
               const fa_opts* opts) {
-  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, stream, opts, nullptr,
-                  nullptr, nullptr);
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, -1, causal ? 0 : -1, n_splits, stream,
+                  opts, nullptr, nullptr, nullptr);
 }
 
 int fa_fwd_partial(const void* q, const void* k, const void* v, float* m_part, float* l_part,
                    float* o_part, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                    int n_splits, void* stream) {
   if (!m_part) return FA_ERR_INVALID_ARG;
-  return fwd_impl(q, k, v, nullptr, nullptr, B, H, Nq, Nk, d, scale, causal, n_splits, stream,
-                  nullptr, m_part, l_part, o_part);
+  return fwd_impl(q, k, v, nullptr, nullptr, B, H, Nq, Nk, d, scale, -1, causal ? 0 : -1, n_splits,
+                  stream, nullptr, m_part, l_part, o_part);
 }
 
 int fa_merge_splits(const float* m_part, const float* l_part, const float* o_part, void* o,

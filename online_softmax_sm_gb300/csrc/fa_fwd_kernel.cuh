@@ -16,7 +16,11 @@
 // a row with l = 0 gets O = 0 and LSE = -inf (sections 7.2-7.3).
 //
 // CTA = QT query tiles of 128 rows of one (b, h), over one range of K/V tiles
-// (the whole key axis, or one split of it).  Warpgroup roles:
+// (the whole key axis, or one split of it).  The mask keeps, for query row r,
+// keys [r + off - wl, r + off + wr] (off = Nk - Nq, -1 = open side; causal is
+// (-1, 0)).  The CTA streams the K/V tiles from the first one any of its rows
+// can see; every query tile starts there and stops after its own last visible
+// tile, so the query tiles' ranges are prefixes of one stream.
 //   WG i < QT     tile i.  Thread t owns row t of the tile (TMEM lane t), so
 //                 row max and row sum are register-local (no shuffles).  Each
 //                 step: read S_i, publish alpha per row, write P_i (bf16) to
@@ -193,26 +197,38 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
   const int row0 = qg * (C::kBr * QT);
   const int kv_begin = split * p.tiles_per_split;
   const int kv_end = min(p.kv_tiles, kv_begin + p.tiles_per_split);
-  int n_i[QT];  // K/V steps of tile i: [kv_begin, kv_begin + n_i)
-  int kv_end_cta = kv_begin;
+  // K/V tiles [b_i, e_i) of this split hold keys visible to rows of query
+  // tile i (empty: e_i = b_i).  The CTA streams from cta_b = min b_i; tile i
+  // takes steps [0, n_i) of that stream, n_i = e_i - cta_b (its leading tiles
+  // before b_i are fully masked for it and cost one MMA pair each).
+  const int off = p.Nk - p.Nq;
+  int n_i[QT];
+  int cta_b = kv_end, kv_end_cta = kv_begin;
+  bool any_tile = false;  // a split past the last K/V tile has kv_begin >= kv_end
 #pragma unroll
   for (int i = 0; i < QT; ++i) {
     const int r_first = row0 + C::kBr * i;
-    int e = kv_begin;
+    n_i[i] = -1;  // end tile, -1 = none
     if (r_first < p.Nq) {
-      e = kv_end;
-      if (p.causal) {
-        // last key visible to the tile's last row: r_last + (Nk - Nq)
-        const int r_last = min(r_first + C::kBr, p.Nq) - 1;
-        const long long last_key = static_cast<long long>(r_last) + (p.Nk - p.Nq);
-        const int lim = last_key < 0 ? 0 : static_cast<int>(last_key / BC) + 1;
-        e = min(e, lim);
+      const int r_last = min(r_first + C::kBr, p.Nq) - 1;
+      // |r + off| < 2^30 and wl, wr <= 2^30: these sums stay within int
+      const int klo = p.wl < 0 ? 0 : max(0, r_first + off - p.wl);
+      const int khi = p.wr < 0 ? p.Nk - 1 : min(p.Nk - 1, r_last + off + p.wr);
+      if (khi >= klo) {
+        const int b = max(kv_begin, static_cast<int>(klo / BC));
+        const int e = min(kv_end, static_cast<int>(khi / BC) + 1);
+        if (e > b) {
+          n_i[i] = e;
+          any_tile = true;
+          cta_b = min(cta_b, b);
+          kv_end_cta = max(kv_end_cta, e);
+        }
       }
-      e = max(e, kv_begin);
     }
-    n_i[i] = e - kv_begin;
-    kv_end_cta = max(kv_end_cta, e);
   }
+  if (!any_tile) cta_b = kv_end_cta = kv_begin;  // nothing to stream
+#pragma unroll
+  for (int i = 0; i < QT; ++i) n_i[i] = n_i[i] < 0 ? 0 : n_i[i] - cta_b;
 
   const uint32_t bar_q = smem_u32(&ctl->q_full);
   const uint32_t bar_kv_full = smem_u32(&ctl->kv_full[0]);
@@ -282,7 +298,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
         }
       }
       uint32_t issued_mask = 0, issued_par = 0;
-      const int n_cta = kv_end_cta - kv_begin;
+      const int n_cta = kv_end_cta - cta_b;
       bool ok = true;
       for (int it = 0; ok && it < 2 * n_cta; ++it) {
         const int stage = it % C::kStages;
@@ -309,7 +325,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem_u32(sKV + stage * C::kKVTileBytes + c * C::kKVChunkBytes), map, full,
-                      c * 64, (kv_begin + step) * BC, bh);
+                      c * 64, (cta_b + step) * BC, bh);
         issued_mask |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (static_cast<uint32_t>(use & 1) << stage);
       }
@@ -337,7 +353,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
                      lo_k = static_cast<uint32_t>(dk0), lo_v = static_cast<uint32_t>(dv0);
       const uint32_t tS = tmem + C::kSCol + i * BC, tO = tmem + C::kOCol + i * D;
       const int n = n_i[i];
-      const int n_cta = kv_end_cta - kv_begin;
+      const int n_cta = kv_end_cta - cta_b;
       auto kv_ready = [&](int pos) {
         return warp_wait(bar_kv_full + 8 * (pos % C::kStages), (pos / C::kStages) & 1, wc);
       };
@@ -505,14 +521,29 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
     const int row = row0 + C::kBr * i + t;
     const int n = n_i[i];
     const float c = p.scale_log2;
-    // last key visible to this row
-    const int lim = p.causal ? min(p.Nk - 1, row + (p.Nk - p.Nq)) : p.Nk - 1;
+    // The row sits at key position rq = row + Nk - Nq; keys visible to it are
+    // [rq - wl, rq + wr] within [0, Nk), a -1 bound leaving that side open.
+    // (|rq| < 2^30 and wl, wr <= 2^30, so the sums below stay within int.)
+    // K/V tiles [jf_b, jf_e) hold only keys that every row of this query tile
+    // sees; they skip the mask (a test uniform across the warpgroup).
+    const int rq = row + off;
+    int jf_b = 0, jf_e;
+    {
+      const int tr_first = row0 + C::kBr * i + off;
+      const int tr_last = min(row0 + C::kBr * (i + 1), p.Nq) - 1 + off;
+      if (p.wl >= 0) {
+        const int lo = tr_last - p.wl;  // highest first-visible key of the tile's rows
+        jf_b = lo <= 0 ? 0 : (lo + BC - 1) / BC;
+      }
+      const int hi = p.wr < 0 ? p.Nk - 1 : min(p.Nk - 1, tr_first + p.wr);  // lowest last-visible key
+      jf_e = hi < 0 ? 0 : (hi + 1) / BC;
+    }
 
     bool ok = true;
     float m = -INFINITY;
     float l = 0.f;
     for (int jj = 0; ok && jj < n; ++jj) {
-      const int j = kv_begin + jj;
+      const int j = cta_b + jj;
       if (!warp_wait(bar_s + 8 * i, jj & 1, wc)) {
         ok = false;
         break;
@@ -527,11 +558,13 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
       float s[BC];
 #pragma unroll
       for (int cc = 0; cc < BC; ++cc) s[cc] = __uint_as_float(r[cc]);
-      const int key0 = j * BC;
-      if (key0 + BC - 1 > lim) {  // tail of the key axis or causal diagonal
+      if (j < jf_b || j >= jf_e) {  // key-axis tail, causal diagonal, window edge
+        const int key0 = j * BC;
+        const int lim = p.wr < 0 ? p.Nk - 1 : min(p.Nk - 1, rq + p.wr);
+        const int lim_lo = p.wl < 0 ? 0 : rq - p.wl;
 #pragma unroll
         for (int cc = 0; cc < BC; ++cc)
-          if (key0 + cc > lim) s[cc] = -INFINITY;
+          if (key0 + cc > lim || key0 + cc < lim_lo) s[cc] = -INFINITY;
       }
 
       // m' = max(m, rowmax S): four independent chains of three-input max

@@ -28,7 +28,8 @@ struct FwdParams {
   int n_splits;
   int tiles_per_split;  // K/V tiles per split
   int kv_tiles;         // ceil(Nk / BC)
-  int causal;
+  int causal;        // launch order only: heaviest query tiles first
+  int wl, wr;        // visible keys [r + off - wl, r + off + wr]; -1 = open side
   float scale;       // natural-units logit scale
   float scale_log2;  // scale * log2(e)
   unsigned long long timeout_ns;

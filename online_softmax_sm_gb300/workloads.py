@@ -16,6 +16,7 @@ from __future__ import annotations
 import dataclasses
 import math
 
+import numpy as np
 import torch
 
 
@@ -33,14 +34,31 @@ class Workload:
     q_mult: float = 1.0    # Q scaled by this (logit spread)
     k_ramp: bool = False   # K row j scaled by 1 + j/Nk (running max grows across tiles)
     seed: int = 0
+    # Local mask (window_left, window_right): key j visible to query i iff
+    # i + (Nk - Nq) - window_left <= j <= i + (Nk - Nq) + window_right, -1 = open
+    # side.  None: the plain or causal mask of `causal`.
+    window: tuple[int, int] | None = None
 
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.d)
 
+    def visible_pairs(self) -> int:
+        """Number of (query, key) pairs the mask leaves visible, per head."""
+        if self.window is None:
+            return self.Nq * self.Nk
+        wl, wr = self.window
+        i = np.arange(self.Nq, dtype=np.int64) + (self.Nk - self.Nq)
+        lo = np.zeros_like(i) if wl < 0 else np.maximum(i - wl, 0)
+        hi = np.full_like(i, self.Nk - 1) if wr < 0 else np.minimum(i + wr, self.Nk - 1)
+        return int(np.maximum(hi - lo + 1, 0).sum())
+
     @property
     def flops(self) -> float:
-        """Algorithmic FLOPs, 4*B*H*Nq*Nk*d, halved for causal."""
+        """Algorithmic FLOPs: 4*d per visible (query, key) pair; for causal
+        without a window, the usual 4*B*H*Nq*Nk*d / 2."""
+        if self.window is not None:
+            return 4.0 * self.B * self.H * self.d * self.visible_pairs()
         f = 4.0 * self.B * self.H * self.Nq * self.Nk * self.d
         return f / 2 if self.causal else f
 
@@ -69,8 +87,12 @@ C4 = Workload("causal_b1h32n16384d128_kramp", 1, 32, 16384, 16384, 128, causal=T
 C4_MASKED = Workload("causal_b1h32nq16384nk16128d128_kramp", 1, 32, 16384, 16384 - 256, 128,
                      causal=True, k_ramp=True, seed=3)
 C5 = Workload("splitkv_b16h32nq128nk32768d128_s16", 16, 32, 128, 32768, 128, n_splits=16, seed=4)
+# Local mask: causal sliding window of 4096 keys (the query's own key and the
+# 4095 before it) over a 16K sequence.
+LOCAL = Workload("local_b1h32n16384d128_w4096", 1, 32, 16384, 16384, 128, window=(4095, 0),
+                 k_ramp=True, seed=5)
 
-WORKLOADS = {w.name: w for w in (C1, C2, C3, C4, C4_MASKED, C5)}
+WORKLOADS = {w.name: w for w in (C1, C2, C3, C4, C4_MASKED, C5, LOCAL)}
 
 
 def generate(w: Workload, device="cpu", dtype=torch.bfloat16):
@@ -93,6 +115,7 @@ def generate(w: Workload, device="cpu", dtype=torch.bfloat16):
 
 
 def custom(B, H, Nq, Nk, d, seed=0, causal=False, n_splits=1, bc=0, q_mult=1.0, k_ramp=False,
-           name=None) -> Workload:
+           name=None, window=None) -> Workload:
     return Workload(name or f"b{B}h{H}nq{Nq}nk{Nk}d{d}", B, H, Nq, Nk, d, causal=causal,
-                    n_splits=n_splits, bc=bc, q_mult=q_mult, k_ramp=k_ramp, seed=seed)
+                    n_splits=n_splits, bc=bc, q_mult=q_mult, k_ramp=k_ramp, seed=seed,
+                    window=None if window is None else tuple(window))

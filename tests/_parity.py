@@ -77,16 +77,22 @@ def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def compare(q, k, v, o, lse, scale, causal, heads=None, rows=None, diff: Diff | None = None,
-            threads=None) -> Diff:
+            threads=None, window=None) -> Diff:
     """q/k/v/o: [B,H,N,d] (any device), lse [B,H,Nq].  heads: list of (b,h).
-    A bf16 `o` is compared with the half-ulp storage allowance, fp32 `o` without."""
+    A bf16 `o` is compared with the half-ulp storage allowance, fp32 `o` without.
+    window=(wl, wr): the oracle's local mask instead of `causal`."""
     diff = diff or Diff()
     bf16_out = (o.dtype == torch.bfloat16)
     B, H = q.shape[0], q.shape[1]
     heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
     for (b, h) in heads:
-        o_ref, lse_ref = oracle.attention(q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu(), scale, causal,
-                                          rows=rows, threads=threads)
+        if window is None:
+            o_ref, lse_ref = oracle.attention(q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu(), scale,
+                                              causal, rows=rows, threads=threads)
+        else:
+            o_ref, lse_ref = oracle.attention_window(q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu(),
+                                                     scale, window[0], window[1], rows=rows,
+                                                     threads=threads)
         og = o[b, h].cpu().double().numpy()
         lg = lse[b, h].cpu().double().numpy()
         if rows is not None:
