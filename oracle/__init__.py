@@ -60,6 +60,8 @@ def _declare(lib):
     lib.oracle_merge.restype = ctypes.c_int
     lib.oracle_softmax_two_pass.argtypes = [_dp, _i64, _dp, _dp]
     lib.oracle_softmax_two_pass.restype = ctypes.c_int
+    lib.oracle_softmax_rows.argtypes = [_dp, _i64, _i64, _ip, _i64, _dp, _dp, ctypes.c_int]
+    lib.oracle_softmax_rows.restype = ctypes.c_int
 
 
 def _f64(a) -> np.ndarray:
@@ -184,6 +186,27 @@ def merge(m, l, o, lib=None):
     if rc != 0:
         raise ValueError("oracle_merge: bad argument")
     return mo.value, lo.value, oo, lse.value
+
+
+def softmax_rows(x, rows: Sequence[int] | None = None, threads: int | None = None, lib=None):
+    """x [R, C]: softmax_two_pass of every row (or of the listed rows).
+    Returns (p [len(rows), C], lse [len(rows)])."""
+    lib = lib or load()
+    x = np.ascontiguousarray(_f64(x))
+    assert x.ndim == 2
+    R, C = x.shape
+    if rows is None:
+        sel, nsel = None, R
+    else:
+        sel = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nsel = sel.shape[0]
+    p = np.empty((nsel, C), dtype=np.float64)
+    lse = np.empty(nsel, dtype=np.float64)
+    rc = lib.oracle_softmax_rows(_ptr(x), R, C, None if sel is None else _ptr(sel, _ip),
+                                 nsel, _ptr(p), _ptr(lse), threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_softmax_rows: bad argument")
+    return p, lse
 
 
 def softmax_two_pass(x, lib=None):

@@ -26,6 +26,7 @@
  *   oracle_softmax_two_pass
  *                         Milakov & Gimelshein two-pass normaliser
  *                         ("Online Softmax 算法详解" section 2.2).
+ *   oracle_softmax_rows   the same over the rows of a matrix.
  *
  *   oracle_attention_window
  *                         the same with a local (sliding-window) mask.
@@ -373,5 +374,76 @@ int oracle_softmax_two_pass(const double *x, int64_t n, double *p, double *lse_o
     for (int64_t i = 0; i < n; ++i)
         p[i] = (l == 0.0) ? 0.0 : exp(x[i] - ref) / l;
     *lse_out = (l == 0.0) ? -INFINITY : m + log(l);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The two-pass normaliser over the rows of a matrix                          */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const double *x;
+    int64_t cols;
+    const int64_t *sel;
+    int64_t r_begin, r_end;
+    double *p, *lse;
+} softmax_rows_job;
+
+static void *softmax_rows_worker(void *arg)
+{
+    softmax_rows_job *job = (softmax_rows_job *)arg;
+    for (int64_t r = job->r_begin; r < job->r_end; ++r) {
+        int64_t i = job->sel ? job->sel[r] : r;
+        oracle_softmax_two_pass(job->x + i * job->cols, job->cols, job->p + r * job->cols,
+                                job->lse + r);
+    }
+    return NULL;
+}
+
+/*
+ * x [rows][cols] row-major fp64; sel[nsel] : rows to compute (NULL: all rows,
+ * nsel must equal rows).  p [nsel][cols], lse [nsel] : oracle_softmax_two_pass
+ * of each selected row, in the order of `sel`.  Rows are spread over
+ * `nthreads` POSIX threads.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_softmax_rows(const double *x, int64_t rows, int64_t cols, const int64_t *sel,
+                        int64_t nsel, double *p, double *lse, int nthreads)
+{
+    if (!x || !p || !lse || rows < 0 || cols < 0 || nsel < 0)
+        return -1;
+    if (!sel && nsel != rows)
+        return -1;
+    for (int64_t r = 0; sel && r < nsel; ++r)
+        if (sel[r] < 0 || sel[r] >= rows)
+            return -1;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > nsel)
+        nthreads = nsel > 0 ? (int)nsel : 1;
+    softmax_rows_job jobs[256];
+    pthread_t tids[256];
+    int created[256];
+    if (nthreads > 256)
+        nthreads = 256;
+    int64_t per = (nsel + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t].x = x;
+        jobs[t].cols = cols;
+        jobs[t].sel = sel;
+        jobs[t].r_begin = (int64_t)t * per < nsel ? (int64_t)t * per : nsel;
+        jobs[t].r_end = jobs[t].r_begin + per < nsel ? jobs[t].r_begin + per : nsel;
+        jobs[t].p = p;
+        jobs[t].lse = lse;
+        created[t] = 0;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        if (nthreads > 1 && pthread_create(&tids[t], NULL, softmax_rows_worker, &jobs[t]) == 0)
+            created[t] = 1;
+        else
+            softmax_rows_worker(&jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (created[t])
+            pthread_join(tids[t], NULL);
     return 0;
 }

@@ -198,6 +198,37 @@ def test_two_pass_softmax_matches_scipy():
     assert np.all(p == 0) and lse == -math.inf
 
 
+def test_softmax_rows_matches_scipy_rowwise():
+    """The two-pass normaliser over a matrix ("Online Softmax 算法详解"
+    section 2.2, row by row): scipy's softmax / logsumexp along axis 1, with
+    -inf entries, an all -inf row (p = 0, lse = -inf) and a row shifted by
+    1e4 (no overflow: exp is taken against the running max)."""
+    rng = np.random.default_rng(11)
+    for rows, cols in ((1, 1), (7, 33), (16, 257)):
+        x = rng.standard_normal((rows, cols)) * 20
+        x[rows // 2, :: 3] = -math.inf
+        if rows > 2:
+            x[1, :] = -math.inf
+            x[2, :] += 1e4
+        p, lse = oracle.softmax_rows(x, threads=3)
+        live = ~np.all(np.isneginf(x), axis=1)
+        np.testing.assert_allclose(p[live], sps.softmax(x[live], axis=1), rtol=1e-12, atol=1e-300)
+        np.testing.assert_allclose(lse[live], sps.logsumexp(x[live], axis=1), rtol=1e-14, atol=1e-11)
+        assert np.all(p[~live] == 0) and np.all(np.isneginf(lse[~live]))
+
+
+def test_softmax_rows_selection():
+    """A row selection returns exactly those rows, in the order given."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((9, 40)) * 5
+    p_all, l_all = oracle.softmax_rows(x, threads=2)
+    sel = [8, 0, 3, 3]
+    p_sub, l_sub = oracle.softmax_rows(x, rows=sel, threads=4)
+    np.testing.assert_array_equal(p_sub, p_all[sel])
+    np.testing.assert_array_equal(l_sub, l_all[sel])
+    np.testing.assert_allclose(p_sub, sps.softmax(x[sel], axis=1), rtol=1e-12)
+
+
 # ------------------------------------------------------------- closed forms
 
 def test_single_key():

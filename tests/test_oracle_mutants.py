@@ -53,6 +53,10 @@ MUTANTS = [
     ("merge_lse_no_max", "*lse_out = (l1 == 0.0) ? -INFINITY : m1 + log(l1);",
      "*lse_out = (l1 == 0.0) ? -INFINITY : log(l1);"),
     ("two_pass_no_rescale", "l = exp(m - ref) * l + exp(x[i] - ref);", "l = l + exp(x[i] - ref);"),
+    ("softmax_rows_selection_ignored", "oracle_softmax_two_pass(job->x + i * job->cols,",
+     "oracle_softmax_two_pass(job->x + r * job->cols,"),
+    ("softmax_rows_skips_a_row", "for (int64_t r = job->r_begin; r < job->r_end; ++r) {\n        int64_t i = job->sel",
+     "for (int64_t r = job->r_begin + 1; r < job->r_end; ++r) {\n        int64_t i = job->sel"),
 ]
 
 
