@@ -37,10 +37,14 @@ import torch  # noqa: E402
 from online_softmax_sm_gb300 import workloads  # noqa: E402
 
 METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and % of dense BF16 tensor peak"
+SOFTMAX_METRIC = "row softmax throughput (two-pass online normaliser), algorithmic GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 WORKLOAD_ALIASES = {"c1": workloads.C1, "c2": workloads.C2, "c3": workloads.C3, "c4": workloads.C4,
                     "c4_masked": workloads.C4_MASKED, "c5": workloads.C5,
                     "local": workloads.LOCAL}
+SOFTMAX_ALIASES = {"softmax_f32": workloads.SOFTMAX_F32,
+                   "softmax_bf16_vocab": workloads.SOFTMAX_BF16_VOCAB,
+                   "softmax_f32_long": workloads.SOFTMAX_F32_LONG}
 
 
 def parse():
@@ -508,8 +512,173 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def softmax_workload_of(name: str):
+    """softmax_f32 / softmax_bf16_vocab / softmax_f32_long, a full softmax
+    workload name, or softmax:ROWS,COLS,f32|bf16[,seed] (smaller cases)."""
+    if name in SOFTMAX_ALIASES:
+        return SOFTMAX_ALIASES[name]
+    if name.startswith("softmax:"):
+        f = name[len("softmax:"):].split(",")
+        rows, cols, dt = int(f[0]), int(f[1]), f[2]
+        seed = int(f[3]) if len(f) > 3 else 0
+        return workloads.SoftmaxWorkload(f"softmax_{dt}_r{rows}c{cols}", rows, cols, dt, seed=seed)
+    return workloads.SOFTMAX_WORKLOADS.get(name)
+
+
+def softmax_oracle_sample(sw, x, target_s: float, seed: int = 0):
+    """Time the oracle on seeded rows of x for about target_s seconds."""
+    import numpy as np
+
+    import oracle
+
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(seed)
+    calib = sorted(rng.choice(sw.rows, size=min(sw.rows, 8), replace=False).tolist())
+    xs = x[calib].cpu().double().numpy()
+    t0 = time.perf_counter()
+    oracle.softmax_rows(xs, threads=threads)
+    per_row = (time.perf_counter() - t0) / len(calib)
+    n = int(min(sw.rows, max(8, target_s / max(per_row, 1e-9))))
+    sel = sorted(rng.choice(sw.rows, size=n, replace=False).tolist())
+    xs = x[sel].cpu().double().numpy()
+    t0 = time.perf_counter()
+    oracle.softmax_rows(xs, threads=threads)
+    dt = time.perf_counter() - t0
+    nbytes = n * (2 * sw.cols * sw.elt + 4)
+    return {"gbs": nbytes / dt / 1e9, "seconds": dt, "rows": n, "threads": threads}
+
+
+def run_softmax(args, sw):
+    """The standalone row softmax: one fa_softmax_rows call per step."""
+    import online_softmax_sm_gb300 as fa
+
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        x = workloads.generate_logits(sw, device="cpu")
+        times, nbytes, threads, rows = [], 0, 0, 0
+        for i in range(args.warmup + args.steps):
+            r = softmax_oracle_sample(sw, x, 2.0, seed=i)
+            if i >= args.warmup:
+                times.append(r["seconds"])
+                nbytes += r["rows"] * (2 * sw.cols * sw.elt + 4)
+                threads, rows = r["threads"], r["rows"]
+        value = nbytes / sum(times) / 1e9
+        line = {"impl": "reference", "metric": SOFTMAX_METRIC, "value": value, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * sum(times) / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": sw.name, **sw.describe()},
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                 "sample": f"about {rows} seeded rows per step, fp64 two-pass oracle"},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    fa.lib()
+    x = workloads.generate_logits(sw, device=dev)
+    y = torch.empty_like(x)
+    lse = torch.empty(sw.rows, dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        fa.softmax_rows(x, out=y, lse=lse)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_region0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_region1 = time.time()
+    barrier(world)
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_local = statistics.mean(step_ms)
+    ms = max_over_ranks(ms_local, world, dev)
+    value = world * sw.io_bytes / (ms * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    achieved = sw.io_bytes / (ms_local * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                "frac": achieved / float(peaks["hbm_gbs"]), "traffic": recorded_traffic(sw.name),
+                "kernel": "fa_softmax_rows_kernel", "kernel_ms": ms_local,
+                "algorithmic_bytes_per_launch": sw.io_bytes, "peak_source": peak_src + " hbm_gbs"}
+
+    e2e = None
+    if not args.no_e2e:
+        hx = x.cpu().pin_memory()
+        hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dx = torch.empty_like(x)
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            fa.softmax_rows(dx, out=y, lse=lse)
+            hy.copy_(y, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        tt = []
+        for _ in range(max(5, min(args.steps, 20))):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            tt.append((a, b))
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in tt), world, dev)
+        e2e = {"value": world * sw.io_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": hx.numel() * hx.element_size(),
+               "d2h_bytes_per_step": hy.numel() * hy.element_size() + hl.numel() * hl.element_size(),
+               "ms_per_step": e_ms}
+        del dx
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = softmax_oracle_sample(sw, x, args.cpu_seconds)
+        cpu = {"value": r["gbs"], "unit": "GB/s", "cores": r["threads"], "kind": "oracle",
+               "sample": f"{r['rows']} seeded rows of this workload ({r['seconds']:.1f} s), "
+                         "fp64 two-pass oracle"}
+    if rank == 0:
+        line = {"metric": SOFTMAX_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": sw.dtype, "data": "synthetic",
+                "config": {"workload": sw.name, **sw.describe(),
+                           "l2": "flushed before every timed step (512 MB write); inputs > L2",
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps, "clocks": sampler.summary(t_region0, t_region1),
+                "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
+    sw = softmax_workload_of(args.workload)
+    if sw is not None:
+        run_softmax(args, sw)
+        return
     w = workload_of(args.workload)
     if args.impl == "reference":
         run_reference(args, w)

@@ -185,6 +185,32 @@ int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, void* o, f
                          int H, int Nq, int Nk, int d, float scale, int causal, int n_splits,
                          void* stream);
 
+/*
+ * Softmax over the rows of a matrix with the online normaliser, the two-pass
+ * scheme of "Online Softmax 算法详解" section 2.2: pass 1 keeps a running max m
+ * and a sum l rescaled by exp(m_old - m_new) whenever the max grows; pass 2
+ * writes y = exp(x - m) / l.  Not part of the attention forward: the same
+ * recurrence on a plain row operation.
+ *
+ * x     : in,  [rows][cols] dense row-major, fp32 (dtype FA_DTYPE_F32) or
+ *         bf16 (FA_DTYPE_BF16); entries finite or -inf.
+ * y     : out, same shape and dtype; may be x (in place).  bf16 results are
+ *         the fp32 values rounded to nearest even.
+ * lse   : out, fp32 [rows], ln sum_j exp(x_ij) (natural log), or NULL.
+ * A row with no finite entry gets y = 0 and lse = -inf.
+ * rows >= 0 (0: nothing is launched), 1 <= cols <= 2^30; x and y aligned to
+ * their element size (16-byte aligned rows take the vector path).
+ * Arithmetic in fp32 with exp as 2^(t log2 e) (ex2.approx): relative error of
+ * y about 1e-6 (1 + |x_ij| + |max_j x_ij|), see the tests.
+ * Rows up to 16384 fp32 / 32768 bf16 columns run one CTA per row; longer rows
+ * a cluster of up to 8 CTAs (up to 131072 fp32 / 262144 bf16 columns held on
+ * chip, x read once); longer still, pass 2 reads the row again.
+ */
+#define FA_DTYPE_F32 0
+#define FA_DTYPE_BF16 1
+int fa_softmax_rows(const void* x, void* y, float* lse, long long rows, int cols, int dtype,
+                    void* stream);
+
 /* Library ABI version (major * 100 + minor). */
 int fa_version(void);
 

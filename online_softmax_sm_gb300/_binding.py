@@ -23,6 +23,8 @@ FA_ERR_CUDA = -3
 FA_ERR_DEVICE_TIMEOUT = -4
 FA_ERR_NO_MEMORY = -5
 FA_ERR_SCRATCH_TOO_SMALL = -6
+FA_DTYPE_F32 = 0
+FA_DTYPE_BF16 = 1
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
@@ -66,6 +68,8 @@ def _declare(L):
     L.fa_fwd_local.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i,
                                _i, _vp]
     L.fa_fwd_local.restype = _i
+    L.fa_softmax_rows.argtypes = [_vp, _vp, _vp, ctypes.c_longlong, _i, _i, _vp]
+    L.fa_softmax_rows.restype = _i
 
 
 def lib():
@@ -218,6 +222,33 @@ def fwd_split_noalloc(q, k, v, n_splits: int, scale: float | None = None, causal
                                         int(bool(causal)), int(n_splits),
                                         _stream_handle(q.device, stream))
     _check(rc, "fa_fwd_split_noalloc")
+    return out, lse
+
+
+def softmax_rows(x, out=None, lse=None, want_lse: bool = True, stream=None):
+    """fa_softmax_rows over the last dimension of x (fp32 or bf16, contiguous).
+    Returns (y, lse) with lse fp32 of shape x.shape[:-1], or (y, None)."""
+    if not isinstance(x, torch.Tensor) or x.device.type != "cuda" or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if x.dtype == torch.float32:
+        dt = FA_DTYPE_F32
+    elif x.dtype == torch.bfloat16:
+        dt = FA_DTYPE_BF16
+    else:
+        raise ValueError("x must be float32 or bfloat16")
+    if x.dim() < 1 or x.shape[-1] < 1:
+        raise ValueError("x needs a non-empty last dimension")
+    cols = x.shape[-1]
+    rows = x.numel() // cols
+    out = torch.empty_like(x) if out is None else out
+    assert out.shape == x.shape and out.dtype == x.dtype and out.is_contiguous()
+    if want_lse and lse is None:
+        lse = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        rc = lib().fa_softmax_rows(x.data_ptr(), out.data_ptr(),
+                                   lse.data_ptr() if lse is not None else None, rows, cols, dt,
+                                   _stream_handle(x.device, stream))
+    _check(rc, "fa_softmax_rows")
     return out, lse
 
 

@@ -25,6 +25,7 @@ struct DevState {
   bool checked = false;
   bool supported = false;
   int* status = nullptr;
+  int num_sms = 0;
 };
 DevState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -69,6 +70,9 @@ int device_state(DevState** out) {
       return cuda_fail(e);
     st.supported = (major == 10 && minor == 3);
     if (st.supported) {
+      if ((e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev)) !=
+          cudaSuccess)
+        return cuda_fail(e);
       void* p = nullptr;
       if ((e = cudaGetSymbolAddress(&p, g_fa_status)) != cudaSuccess) return cuda_fail(e);
       st.status = static_cast<int*>(p);
@@ -298,6 +302,32 @@ int fa_merge_splits(const float* m_part, const float* l_part, const float* o_par
   mp.rows = static_cast<long long>(B) * H * Nq;
   mp.n_splits = n_splits;
   cudaError_t e = fa::launch_merge(d, mp, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_softmax_rows(const void* x, void* y, float* lse, long long rows, int cols, int dtype,
+                    void* stream) {
+  if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 1 || cols > kMaxSeq) return FA_ERR_INVALID_ARG;
+  const size_t elt = dtype == FA_DTYPE_F32 ? 4 : 2;
+  if (rows > 0 && (!x || !y || !aligned(x, elt) || !aligned(y, elt) || (lse && !aligned(lse, 4))))
+    return FA_ERR_INVALID_ARG;
+  DevState* dev = nullptr;
+  int rc = device_state(&dev);
+  if (rc != FA_OK) return rc;
+  if (rows == 0) return FA_OK;
+  fa::SoftmaxParams p{};
+  p.x = x;
+  p.y = y;
+  p.lse = lse;
+  p.rows = rows;
+  p.cols = cols;
+  p.status = dev->status;
+  p.timeout_ns = kDefaultTimeoutNs;
+  // 16-byte vectors when every row starts on a 16-byte boundary
+  const bool vec = aligned(x, 16) && aligned(y, 16) && (static_cast<size_t>(cols) * elt) % 16 == 0;
+  cudaError_t e = fa::launch_softmax_rows(p, dtype == FA_DTYPE_BF16, vec, dev->num_sms,
+                                          static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 

@@ -59,4 +59,21 @@ cudaError_t launch_fwd_d128_bc128(int qt, const CUtensorMap* maps, const FwdPara
                                   cudaStream_t s);
 cudaError_t launch_merge(int d, const MergeParams& p, cudaStream_t s);
 
+// Row softmax (fa_softmax.cu).  Row r's columns are split over `cluster`
+// CTAs, `chunk` columns each (a multiple of the 16-byte vector width).
+struct SoftmaxParams {
+  const void* x;
+  void* y;
+  float* lse;  // may be null
+  long long rows;
+  int cols;
+  int cluster;
+  int chunk;
+  int* status;                    // device status word (timed-out waits)
+  unsigned long long timeout_ns;  // bound of each wait
+};
+
+cudaError_t launch_softmax_rows(const SoftmaxParams& p, bool bf16, bool vec_io, int num_sms,
+                                cudaStream_t s);
+
 }  // namespace fa

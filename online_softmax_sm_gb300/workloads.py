@@ -95,6 +95,48 @@ LOCAL = Workload("local_b1h32n16384d128_w4096", 1, 32, 16384, 16384, 128, window
 WORKLOADS = {w.name: w for w in (C1, C2, C3, C4, C4_MASKED, C5, LOCAL)}
 
 
+@dataclasses.dataclass(frozen=True)
+class SoftmaxWorkload:
+    """Rows of logits for the standalone softmax: fp32 N(0, sigma^2) draws,
+    cast to `dtype` ("f32" or "bf16"), [rows, cols] contiguous."""
+    name: str
+    rows: int
+    cols: int
+    dtype: str = "f32"
+    sigma: float = 4.0
+    seed: int = 0
+
+    @property
+    def elt(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    @property
+    def io_bytes(self) -> int:
+        """Algorithmic HBM bytes: read x once, write y once and one fp32 LSE per row."""
+        return 2 * self.rows * self.cols * self.elt + 4 * self.rows
+
+    def describe(self) -> dict:
+        return dataclasses.asdict(self)
+
+
+# Attention-score rows (B*H*N rows of N scores: 32 heads x 1024 queries of a
+# 4096-token context) and a language-model head's logits over a 128K
+# vocabulary; the long-row case exceeds what a CTA cluster keeps on chip.
+SOFTMAX_F32 = SoftmaxWorkload("softmax_f32_r32768c4096", 32768, 4096, "f32", seed=7)
+SOFTMAX_BF16_VOCAB = SoftmaxWorkload("softmax_bf16_r4096c131072", 4096, 131072, "bf16", seed=8)
+SOFTMAX_F32_LONG = SoftmaxWorkload("softmax_f32_r256c1048576", 256, 1 << 20, "f32", seed=9)
+SOFTMAX_WORKLOADS = {w.name: w for w in (SOFTMAX_F32, SOFTMAX_BF16_VOCAB, SOFTMAX_F32_LONG)}
+
+
+def generate_logits(w: SoftmaxWorkload, device="cpu") -> torch.Tensor:
+    """Draw x for softmax workload `w` on `device`."""
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed)
+    x = torch.randn((w.rows, w.cols), generator=g, device=device, dtype=torch.float32)
+    x.mul_(w.sigma)
+    return x if w.dtype == "f32" else x.to(torch.bfloat16)
+
+
 def generate(w: Workload, device="cpu", dtype=torch.bfloat16):
     """Draw (q, k, v) for workload `w` on `device` ([B,H,N,d], contiguous)."""
     g = torch.Generator(device=device)
