@@ -14,17 +14,18 @@
 // same order, so every CTA of a row gets the same (M, L).  Pass 2 writes
 // y = exp(x - M) / L.
 //
-// Rows whose start is 16-byte aligned run fa_softmax_ring_kernel: the CTA's
-// columns of each row arrive through a ring of shared-memory stages filled by
-// 1-D bulk copies (TMA), issued several rows ahead, so loads overlap the
-// arithmetic and the stores of earlier rows.  The threads copy their slice
-// into registers and free the stage at once.  A row that fits the registers
-// of its CTA or cluster (up to 8 CTAs x 1024 threads x 16 fp32 or 32 bf16
-// values) is read from HBM once and pass 2 rescales the exponentials kept
-// from pass 1 by exp(m_thread - M) / L.  Longer rows are cut into sub-chunks
-// and pass 2 streams them through the ring again; pass 1 marks them to stay
-// in L2 for that second read.  Other rows run fa_softmax_rows_kernel, the
-// same arithmetic with element loads straight into registers.
+// A row that fits one CTA (up to 1024 threads x 16 fp32 or 32 bf16 values)
+// runs fa_softmax_rows_kernel: 16-byte (or element) loads straight into
+// registers, several CTAs per SM overlapping one another.  Longer rows with
+// 16-byte aligned starts run fa_softmax_ring_kernel on a cluster of up to 8
+// CTAs of 1024 threads: each CTA's columns of each row arrive through a ring
+// of shared-memory stages filled by 1-D bulk copies (TMA) issued rows ahead,
+// so loads overlap the arithmetic and the stores of earlier rows; the threads
+// copy their slice into registers and free the stage at once.  Either way a
+// row that fits the registers of its CTA or cluster is read from HBM once and
+// pass 2 rescales the exponentials kept from pass 1 by exp(m_thread - M) / L.
+// Longer rows are cut into sub-chunks and pass 2 streams them through the
+// ring again; pass 1 marks them to stay in L2 for that second read.
 //
 // Exponentials: exp(x - m) = 2^((x - m) log2 e), the difference taken first
 // (so the exponent's rounding error scales with |x - m|, not with |m|) and
@@ -511,7 +512,7 @@ cudaError_t launch_persistent(Kern kern, int threads, int smem, int per_sm,
 
 template <typename T, int kThreads>
 cudaError_t launch_ring(const SoftmaxParams& p, int num_sms, cudaStream_t s) {
-  constexpr int kStages = kThreads == 1024 ? 3 : 4;
+  constexpr int kStages = 3;  // 3 x 64 KB at 1024 threads
   constexpr int kSmem = kStages * kThreads * 64;
   auto kern = fa_softmax_ring_kernel<T, kThreads, kStages>;
   static std::atomic<int> cached{0};  // resident CTAs per SM (same on every sm_103 device)
@@ -547,28 +548,20 @@ template <typename T, bool kVecIO>
 cudaError_t launch_typed(SoftmaxParams p, int num_sms, cudaStream_t s) {
   constexpr int E = Io<T>::E;
   constexpr int kPer = 4 * E;
-  // One CTA per row if the row fits in 32..1024 threads x kPer values.
+  // One CTA per row if the row fits in 32..1024 threads x kPer values: the
+  // register kernel, several CTAs per SM overlapping each other's loads,
+  // reductions and stores (measured faster than the ring at these sizes).
   for (int t = 32; t <= 1024; t *= 2) {
     if (p.cols <= t * kPer) {
       p.cluster = 1;
       p.chunk = t * kPer;
-      if (kVecIO) {
-        switch (t) {
-          case 32: return launch_ring<T, 32>(p, num_sms, s);
-          case 64: return launch_ring<T, 64>(p, num_sms, s);
-          case 128: return launch_ring<T, 128>(p, num_sms, s);
-          case 256: return launch_ring<T, 256>(p, num_sms, s);
-          case 512: return launch_ring<T, 512>(p, num_sms, s);
-          default: return launch_ring<T, 1024>(p, num_sms, s);
-        }
-      }
       switch (t) {
-        case 32: return launch_one<T, 32, false>(p, num_sms, s);
-        case 64: return launch_one<T, 64, false>(p, num_sms, s);
-        case 128: return launch_one<T, 128, false>(p, num_sms, s);
-        case 256: return launch_one<T, 256, false>(p, num_sms, s);
-        case 512: return launch_one<T, 512, false>(p, num_sms, s);
-        default: return launch_one<T, 1024, false>(p, num_sms, s);
+        case 32: return launch_one<T, 32, kVecIO>(p, num_sms, s);
+        case 64: return launch_one<T, 64, kVecIO>(p, num_sms, s);
+        case 128: return launch_one<T, 128, kVecIO>(p, num_sms, s);
+        case 256: return launch_one<T, 256, kVecIO>(p, num_sms, s);
+        case 512: return launch_one<T, 512, kVecIO>(p, num_sms, s);
+        default: return launch_one<T, 1024, kVecIO>(p, num_sms, s);
       }
     }
   }
