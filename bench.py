@@ -91,10 +91,18 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+FWD_SOURCES = ["fa_fwd_kernel.cuh", "fa_fwd_d64_bc64.cu", "fa_fwd_d64_bc128.cu",
+               "fa_fwd_d128_bc64.cu", "fa_fwd_d128_bc128.cu", "fa_ptx.cuh", "fa_wait.cuh",
+               "fa_internal.h"]
+SOFTMAX_SOURCES = ["fa_softmax.cu", "fa_ptx.cuh", "fa_wait.cuh", "fa_internal.h"]
+
+
+def kernel_source_hash(files=None) -> str:
+    """Hash of the kernel sources `files` (names under csrc/; all when None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "online_softmax_sm_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    names = sorted(files) if files else sorted(os.listdir(csrc))
+    for fn in names:
         if fn.endswith((".cu", ".cuh", ".h")):
             with open(os.path.join(csrc, fn), "rb") as f:
                 h.update(fn.encode() + b"\0" + f.read())
@@ -103,7 +111,8 @@ def kernel_source_hash() -> str:
 
 def recorded_traffic(workload_name: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None if absent or taken on different kernel sources."""
+    summary, or None if absent or taken on different kernel sources (the
+    entry lists the source files its hash covers)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -111,7 +120,7 @@ def recorded_traffic(workload_name: str):
     except (OSError, ValueError):
         return None
     ent = rec.get(workload_name)
-    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash(ent.get("sources")):
         return None
     return ent.get("dram_bytes_per_launch")
 
