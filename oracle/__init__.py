@@ -62,6 +62,9 @@ def _declare(lib):
     lib.oracle_softmax_two_pass.restype = ctypes.c_int
     lib.oracle_softmax_rows.argtypes = [_dp, _i64, _i64, _ip, _i64, _dp, _dp, ctypes.c_int]
     lib.oracle_softmax_rows.restype = ctypes.c_int
+    lib.oracle_attention_bwd.argtypes = [_dp, _i64, _dp, _dp, _i64, _i64, ctypes.c_double, _i64,
+                                         _i64, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
+    lib.oracle_attention_bwd.restype = ctypes.c_int
 
 
 def _f64(a) -> np.ndarray:
@@ -186,6 +189,30 @@ def merge(m, l, o, lib=None):
     if rc != 0:
         raise ValueError("oracle_merge: bad argument")
     return mo.value, lo.value, oo, lse.value
+
+
+def attention_bwd(q, k, v, dout, scale: float, causal: bool = False, window=None,
+                  threads: int | None = None, lib=None):
+    """One head: gradients of attention.  q, dout [nq,d]; k, v [nk,d].
+    window=(wl, wr) overrides `causal` (causal = (-1, 0)).
+    Returns dict(dq, dk, dv, lse, dd) (dd = D_i = <dO_i, O_i>)."""
+    lib = lib or load()
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    nq, d = q.shape
+    nk = k.shape[0]
+    assert k.shape == (nk, d) and v.shape == (nk, d) and dout.shape == (nq, d)
+    wl, wr = window if window is not None else ((-1, 0) if causal else (-1, -1))
+    dq = np.empty((nq, d))
+    dk = np.empty((nk, d))
+    dv = np.empty((nk, d))
+    lse = np.empty(nq)
+    dd = np.empty(nq)
+    rc = lib.oracle_attention_bwd(_ptr(q), nq, _ptr(k), _ptr(v), nk, d, float(scale), int(wl), int(wr),
+                                  _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(lse), _ptr(dd),
+                                  threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd: bad argument")
+    return {"dq": dq, "dk": dk, "dv": dv, "lse": lse, "dd": dd}
 
 
 def softmax_rows(x, rows: Sequence[int] | None = None, threads: int | None = None, lib=None):

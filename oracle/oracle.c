@@ -27,6 +27,8 @@
  *                         Milakov & Gimelshein two-pass normaliser
  *                         ("Online Softmax 算法详解" section 2.2).
  *   oracle_softmax_rows   the same over the rows of a matrix.
+ *   oracle_attention_bwd  gradients dQ, dK, dV of the attention forward
+ *                         ("Online Softmax 算法详解" section 8.3).
  *
  *   oracle_attention_window
  *                         the same with a local (sliding-window) mask.
@@ -374,6 +376,182 @@ int oracle_softmax_two_pass(const double *x, int64_t n, double *p, double *lse_o
     for (int64_t i = 0; i < n; ++i)
         p[i] = (l == 0.0) ? 0.0 : exp(x[i] - ref) / l;
     *lse_out = (l == 0.0) ? -INFINITY : m + log(l);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Attention backward                                                         */
+/* ------------------------------------------------------------------------ */
+/*
+ * Gradients of O = softmax(scale * Q K^T + mask) V for one head, given dO
+ * ("Online Softmax 算法详解" section 8.3: recompute S, restore P from LSE,
+ * then dQ, dK, dV; the pages leave the gradient formulas to a page not in the
+ * set, so these are the derivative of the forward written out):
+ *   P_ij  = exp(scale * S_ij - LSE_i)          (0 where masked)
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = <dO_i, v_j>
+ *   D_i   = sum_j P_ij dP_ij                   (= <dO_i, O_i>)
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale sum_j dS_ij k_j
+ *   dK_j  = scale sum_i dS_ij q_i
+ * A row with no visible key (LSE = -inf) has P = 0 and contributes nothing
+ * (section 7.3).  Three sweeps: per row LSE and D; per key dK and dV; per row
+ * dQ -- each a plain loop, threads split the rows or the keys.
+ */
+typedef struct {
+    const double *q, *k, *v, *dout;
+    int64_t nq, nk, d;
+    double scale;
+    int64_t wl, wr;
+    double *lse, *dd; /* per row */
+    double *dq, *dk, *dv;
+    int64_t begin, end;
+    int sweep;
+} bwd_job;
+
+static int visible(int64_t i, int64_t j, int64_t nq, int64_t nk, int64_t wl, int64_t wr)
+{
+    int64_t off = nk - nq;
+    if (wl >= 0 && j < i + off - wl)
+        return 0;
+    if (wr >= 0 && j > i + off + wr)
+        return 0;
+    return 1;
+}
+
+static double dot(const double *a, const double *b, int64_t d)
+{
+    double acc = 0.0;
+    for (int64_t c = 0; c < d; ++c)
+        acc += a[c] * b[c];
+    return acc;
+}
+
+/* P_ij from the row's LSE; 0 if masked or the row is empty. */
+static double prob(const bwd_job *J, int64_t i, int64_t j)
+{
+    if (!visible(i, j, J->nq, J->nk, J->wl, J->wr) || J->lse[i] == -INFINITY)
+        return 0.0;
+    return exp(J->scale * dot(J->q + i * J->d, J->k + j * J->d, J->d) - J->lse[i]);
+}
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *J = (bwd_job *)arg;
+    const int64_t d = J->d;
+    if (J->sweep == 0) { /* rows: LSE_i, then D_i = sum_j P_ij dP_ij */
+        for (int64_t i = J->begin; i < J->end; ++i) {
+            double m = -INFINITY;
+            for (int64_t j = 0; j < J->nk; ++j)
+                if (visible(i, j, J->nq, J->nk, J->wl, J->wr)) {
+                    double sij = J->scale * dot(J->q + i * d, J->k + j * d, d);
+                    if (sij > m)
+                        m = sij;
+                }
+            if (m == -INFINITY) {
+                J->lse[i] = -INFINITY;
+                J->dd[i] = 0.0;
+                continue;
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < J->nk; ++j)
+                if (visible(i, j, J->nq, J->nk, J->wl, J->wr))
+                    l += exp(J->scale * dot(J->q + i * d, J->k + j * d, d) - m);
+            J->lse[i] = m + log(l);
+            double di = 0.0;
+            for (int64_t j = 0; j < J->nk; ++j) {
+                double p = prob(J, i, j);
+                if (p != 0.0)
+                    di += p * dot(J->dout + i * d, J->v + j * d, d);
+            }
+            J->dd[i] = di;
+        }
+    } else if (J->sweep == 1) { /* keys: dV_j and dK_j */
+        for (int64_t j = J->begin; j < J->end; ++j) {
+            double *dvj = J->dv + j * d, *dkj = J->dk + j * d;
+            for (int64_t c = 0; c < d; ++c)
+                dvj[c] = dkj[c] = 0.0;
+            for (int64_t i = 0; i < J->nq; ++i) {
+                double p = prob(J, i, j);
+                if (p == 0.0)
+                    continue;
+                double ds = p * (dot(J->dout + i * d, J->v + j * d, d) - J->dd[i]);
+                for (int64_t c = 0; c < d; ++c) {
+                    dvj[c] += p * J->dout[i * d + c];
+                    dkj[c] += J->scale * ds * J->q[i * d + c];
+                }
+            }
+        }
+    } else { /* rows: dQ_i */
+        for (int64_t i = J->begin; i < J->end; ++i) {
+            double *dqi = J->dq + i * d;
+            for (int64_t c = 0; c < d; ++c)
+                dqi[c] = 0.0;
+            for (int64_t j = 0; j < J->nk; ++j) {
+                double p = prob(J, i, j);
+                if (p == 0.0)
+                    continue;
+                double ds = p * (dot(J->dout + i * d, J->v + j * d, d) - J->dd[i]);
+                for (int64_t c = 0; c < d; ++c)
+                    dqi[c] += J->scale * ds * J->k[j * d + c];
+            }
+        }
+    }
+    return NULL;
+}
+
+static void run_sweep(bwd_job *base, int sweep, int64_t n, int nthreads)
+{
+    bwd_job jobs[256];
+    pthread_t tids[256];
+    int created[256];
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    if (nthreads > n)
+        nthreads = n > 0 ? (int)n : 1;
+    int64_t per = (n + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = *base;
+        jobs[t].sweep = sweep;
+        jobs[t].begin = (int64_t)t * per < n ? (int64_t)t * per : n;
+        jobs[t].end = jobs[t].begin + per < n ? jobs[t].begin + per : n;
+        created[t] = 0;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        if (nthreads > 1 && pthread_create(&tids[t], NULL, bwd_worker, &jobs[t]) == 0)
+            created[t] = 1;
+        else
+            bwd_worker(&jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (created[t])
+            pthread_join(tids[t], NULL);
+}
+
+/*
+ * q [nq][d], k, v [nk][d], dout [nq][d]: one head, fp64.  Mask: the window
+ * (wl, wr) of oracle_attention_window (causal = (-1, 0), none = (-1, -1)).
+ * Outputs dq [nq][d], dk, dv [nk][d], and lse [nq], dd [nq] (D_i).
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_attention_bwd(const double *q, int64_t nq, const double *k, const double *v,
+                         int64_t nk, int64_t d, double scale, int64_t wl, int64_t wr,
+                         const double *dout, double *dq, double *dk, double *dv, double *lse,
+                         double *dd, int nthreads)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || !lse || !dd || nq < 0 || nk < 0 || d <= 0)
+        return -1;
+    bwd_job J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.dout = dout;
+    J.nq = nq; J.nk = nk; J.d = d;
+    J.scale = scale; J.wl = wl; J.wr = wr;
+    J.lse = lse; J.dd = dd; J.dq = dq; J.dk = dk; J.dv = dv;
+    run_sweep(&J, 0, nq, nthreads);
+    run_sweep(&J, 1, nk, nthreads);
+    run_sweep(&J, 2, nq, nthreads);
     return 0;
 }
 

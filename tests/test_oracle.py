@@ -229,6 +229,70 @@ def test_softmax_rows_selection():
     np.testing.assert_allclose(p_sub, sps.softmax(x[sel], axis=1), rtol=1e-12)
 
 
+# ------------------------------------------------------------- backward
+
+def _loss_grads_fd(q, k, v, g, scale, window, h=1e-6):
+    """Central differences of L = sum(O * g) through the forward oracle."""
+    def loss(q_, k_, v_):
+        o, _ = oracle.attention_window(q_, k_, v_, scale, window[0], window[1])
+        return float(np.sum(o * g))
+    out = []
+    for which, arr in enumerate((q, k, v)):
+        grad = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            hi, lo = [x.copy() for x in (q, k, v)], [x.copy() for x in (q, k, v)]
+            hi[which][idx] += h
+            lo[which][idx] -= h
+            grad[idx] = (loss(*hi) - loss(*lo)) / (2 * h)
+        out.append(grad)
+    return out
+
+
+@pytest.mark.parametrize("nq,nk,d,window,seed", [
+    (3, 4, 2, (-1, -1), 0), (4, 4, 3, (-1, 0), 1), (5, 3, 2, (-1, 0), 2), (4, 6, 2, (1, 1), 3),
+    (6, 5, 3, (2, 0), 4)])
+def test_bwd_matches_finite_differences(nq, nk, d, window, seed):
+    """Gradients of sum(O * dO) against central differences of the forward
+    oracle (pinned independently above); includes masks that leave a row
+    with no visible key."""
+    rng = np.random.default_rng(seed)
+    q, k, v, g = (rng.standard_normal(sh) for sh in ((nq, d), (nk, d), (nk, d), (nq, d)))
+    scale = 0.8
+    r = oracle.attention_bwd(q, k, v, g, scale, window=window)
+    dq, dk, dv = _loss_grads_fd(q, k, v, g, scale, window)
+    np.testing.assert_allclose(r["dq"], dq, rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(r["dk"], dk, rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(r["dv"], dv, rtol=1e-6, atol=1e-8)
+
+
+def test_bwd_invariants_and_statistics():
+    """sum_j dK_j = 0 and sum_j dV_j = sum of dO over rows that see a key
+    (softmax rows sum to one); D_i = <dO_i, O_i>; LSE equals the forward's."""
+    rng = np.random.default_rng(21)
+    nq, nk, d = 9, 7, 4
+    q, k, v, g = (rng.standard_normal(sh) for sh in ((nq, d), (nk, d), (nk, d), (nq, d)))
+    for causal in (False, True):
+        r = oracle.attention_bwd(q, k, v, g, 0.5, causal=causal, threads=3)
+        o, lse = oracle.attention(q, k, v, 0.5, causal)
+        live = np.isfinite(lse)
+        np.testing.assert_allclose(r["dk"].sum(axis=0), 0.0, atol=1e-12)
+        np.testing.assert_allclose(r["dv"].sum(axis=0), g[live].sum(axis=0), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(r["dd"][live], np.sum(g * o, axis=1)[live], rtol=1e-12, atol=1e-12)
+        np.testing.assert_array_equal(np.isfinite(r["lse"]), live)
+        np.testing.assert_allclose(r["lse"][live], lse[live], rtol=1e-14)
+        assert np.all(r["dq"][~live] == 0.0)
+
+
+def test_bwd_single_key():
+    """One key: P = 1, so dS = 0 (dQ = dK = 0) and dV = sum_i dO_i."""
+    rng = np.random.default_rng(22)
+    q, g = rng.standard_normal((5, 3)), rng.standard_normal((5, 3))
+    k, v = rng.standard_normal((1, 3)), rng.standard_normal((1, 3))
+    r = oracle.attention_bwd(q, k, v, g, 1.3)
+    assert np.abs(r["dq"]).max() < 1e-15 and np.abs(r["dk"]).max() < 1e-15
+    np.testing.assert_allclose(r["dv"][0], g.sum(axis=0), rtol=1e-14)
+
+
 # ------------------------------------------------------------- closed forms
 
 def test_single_key():

@@ -55,6 +55,14 @@ MUTANTS = [
     ("two_pass_no_rescale", "l = exp(m - ref) * l + exp(x[i] - ref);", "l = l + exp(x[i] - ref);"),
     ("softmax_rows_selection_ignored", "oracle_softmax_two_pass(job->x + i * job->cols,",
      "oracle_softmax_two_pass(job->x + r * job->cols,"),
+    ("bwd_dq_no_scale", "dqi[c] += J->scale * ds * J->k[j * d + c];", "dqi[c] += ds * J->k[j * d + c];"),
+    ("bwd_dk_wrong_operand", "dkj[c] += J->scale * ds * J->q[i * d + c];",
+     "dkj[c] += J->scale * ds * J->k[j * d + c];"),
+    ("bwd_dv_wrong_operand", "dvj[c] += p * J->dout[i * d + c];", "dvj[c] += p * J->v[j * d + c];"),
+    ("bwd_D_without_p", "di += p * dot(J->dout + i * d, J->v + j * d, d);",
+     "di += dot(J->dout + i * d, J->v + j * d, d);"),
+    ("bwd_p_without_scale", "return exp(J->scale * dot(J->q + i * J->d, J->k + j * J->d, J->d) - J->lse[i]);",
+     "return exp(dot(J->q + i * J->d, J->k + j * J->d, J->d) - J->lse[i]);"),
     ("softmax_rows_skips_a_row", "for (int64_t r = job->r_begin; r < job->r_end; ++r) {\n        int64_t i = job->sel",
      "for (int64_t r = job->r_begin + 1; r < job->r_end; ++r) {\n        int64_t i = job->sel"),
 ]
@@ -73,6 +81,7 @@ def _pin_calls():
         "test_online_blocks_match_three_pass": [(0,)],
         "test_merge_of_random_partition_matches_full": [(0,)],
         "test_window_matches_scipy_softmax": [(10, 10, 2, 0, 0), (6, 14, 4, 1, 2), (14, 6, 0, 2, 3)],
+        "test_bwd_matches_finite_differences": [(3, 4, 2, (-1, -1), 0), (4, 6, 2, (1, 1), 3)],
     }
     calls = []
     for name, fn in inspect.getmembers(pins, inspect.isfunction):
