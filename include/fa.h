@@ -91,6 +91,35 @@ int fa_fwd_local(const void* q, const void* k, const void* v, void* o, float* ls
                  int Nq, int Nk, int d, float scale, int window_left, int window_right, int n_splits,
                  void* stream);
 
+/*
+ * Attention backward from the saved LSE ("Online Softmax 算法详解" section 8.3:
+ * recompute S = Q K^T, restore P = exp(scale S - LSE) without a second online
+ * softmax, then form the gradients).  With D_i = <dO_i, O_i>:
+ *   dV_j = sum_i P_ij dO_i,   dS_ij = P_ij (<dO_i, V_j> - D_i),
+ *   dK_j = scale sum_i dS_ij Q_i,   dQ_i = scale sum_j dS_ij K_j.
+ * A row with LSE = -inf (no visible key) contributes nothing (section 7.3).
+ *
+ * q, k, v, o : in, bf16, as fa_fwd (o = the forward's output)
+ * lse        : in, fp32 [B][H][Nq], the forward's LSE
+ * dout       : in, bf16 [B][H][Nq][d], gradient of the loss with respect to O
+ * dq, dk, dv : out, bf16, shapes of q, k, v; 16-byte aligned
+ * causal     : the mask of the forward call (bottom-right aligned)
+ * Two kernels after a small row pass: one per 128-key tile (dK, dV) and one per
+ * 128-query tile (dQ); S and dP are recomputed in both, and no result is
+ * accumulated atomically, so repeated calls give identical bits.  A fp32
+ * workspace of 2 * B*H*ceil(Nq/128)*128 floats is taken with cudaMallocAsync
+ * on `stream` and released on it (FA_ERR_NO_MEMORY if that fails).
+ * Arguments otherwise as fa_fwd.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+           float scale, int causal, void* stream);
+
+/* fa_bwd for a forward run with fa_fwd_local's window (window_left, window_right). */
+int fa_bwd_local(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
+                 int d, float scale, int window_left, int window_right, void* stream);
+
 /* Options for fa_fwd_ex.  Zero-initialise, then set what you need. */
 typedef struct fa_opts {
   int bc;                     /* K/V tile rows: 0 = default (128), or 64 or 128 */

@@ -9,17 +9,18 @@ package is its Python binding plus the seeded workload generators:
   merge_splits(m_part, l_part, o_part)    -> (o, lse)       fa_merge_splits
   fwd_split_noalloc(q, k, v, n_splits)   -> (o, lse)       fa_fwd_split_noalloc
   softmax_rows(x)                         -> (y, lse)       fa_softmax_rows (two-pass normaliser)
+  bwd(q, k, v, o, lse, dout, ...)         -> (dq, dk, dv)   fa_bwd / fa_bwd_local
   split_workspace_bytes(...), device_status(), version()
 
 libfa.so is loaded on first use; importing the package loads nothing.
 """
 from ._binding import (FA_DTYPE_BF16, FA_DTYPE_F32, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT,
                        FA_ERR_INVALID_ARG, FA_ERR_NO_MEMORY, FA_ERR_SCRATCH_TOO_SMALL,
-                       FA_ERR_UNSUPPORTED, FA_OK, FAError, device_status, fwd, fwd_local,
+                       FA_ERR_UNSUPPORTED, FA_OK, FAError, bwd, device_status, fwd, fwd_local,
                        fwd_partial, fwd_split_noalloc, lib, merge_splits, softmax_rows,
                        split_workspace_bytes, strerror, version)
 
-__all__ = ["fwd", "fwd_local", "fwd_partial", "merge_splits", "fwd_split_noalloc", "softmax_rows",
+__all__ = ["fwd", "fwd_local", "bwd", "fwd_partial", "merge_splits", "fwd_split_noalloc", "softmax_rows",
            "split_workspace_bytes", "device_status", "version", "strerror", "lib", "FAError",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
            "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_NO_MEMORY", "FA_ERR_SCRATCH_TOO_SMALL", "FA_DTYPE_F32",

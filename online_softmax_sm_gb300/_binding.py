@@ -70,6 +70,10 @@ def _declare(L):
     L.fa_fwd_local.restype = _i
     L.fa_softmax_rows.argtypes = [_vp, _vp, _vp, ctypes.c_longlong, _i, _i, _vp]
     L.fa_softmax_rows.restype = _i
+    L.fa_bwd.argtypes = [_vp] * 9 + [_i] * 5 + [ctypes.c_float, _i, _vp]
+    L.fa_bwd.restype = _i
+    L.fa_bwd_local.argtypes = [_vp] * 9 + [_i] * 5 + [ctypes.c_float, _i, _i, _vp]
+    L.fa_bwd_local.restype = _i
 
 
 def lib():
@@ -165,6 +169,33 @@ def fwd_local(q, k, v, window_left: int, window_right: int, scale: float | None 
                                 int(window_right), int(n_splits), _stream_handle(q.device, stream))
     _check(rc, "fa_fwd_local")
     return out, lse
+
+
+def bwd(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False, window=None,
+        dq=None, dk=None, dv=None, stream=None):
+    """fa_bwd / fa_bwd_local: (dq, dk, dv) bf16, shapes of q, k, v.  `o` and
+    `lse` are the forward's outputs; window=(wl, wr) selects fa_bwd_local."""
+    B, H, Nq, Nk, d = _check_qkv(q, k, v)
+    for name, t in (("o", o), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    args = [q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, float(scale)]
+    with torch.cuda.device(q.device):
+        sh = _stream_handle(q.device, stream)
+        if window is None:
+            rc = lib().fa_bwd(*args, int(bool(causal)), sh)
+        else:
+            rc = lib().fa_bwd_local(*args, int(window[0]), int(window[1]), sh)
+    _check(rc, "fa_bwd")
+    return dq, dk, dv
 
 
 def fwd_partial(q, k, v, n_splits: int, scale: float | None = None, causal: bool = False,

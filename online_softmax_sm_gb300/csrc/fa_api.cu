@@ -305,6 +305,85 @@ int fa_merge_splits(const float* m_part, const float* l_part, const float* o_par
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
+// Shared body of fa_bwd / fa_bwd_local.
+static int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
+                    int d, float scale, int wl, int wr, void* stream) {
+  int rc = check_sizes(B, H, Nq, Nk, d, scale);
+  if (rc != FA_OK) return rc;
+  if (wl < -1 || wr < -1 || wl > kMaxSeq || wr > kMaxSeq) return FA_ERR_INVALID_ARG;
+  const void* in[6] = {q, k, v, o, dout, lse};
+  void* out[3] = {dq, dk, dv};
+  for (const void* ptr : in)
+    if (!ptr) return FA_ERR_INVALID_ARG;
+  for (void* ptr : out)
+    if (!ptr || !aligned(ptr, 16)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  DevState* dev = nullptr;
+  if ((rc = device_state(&dev)) != FA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  const int nq_pad = (Nq + 127) / 128 * 128;
+
+  CUtensorMap maps[7];  // q, k, v, dout, dq, dk, dv
+  const void* bases[7] = {q, k, v, dout, dq, dk, dv};
+  const int rows[7] = {Nq, Nk, Nk, Nq, Nq, Nk, Nk};
+  for (int i = 0; i < 7; ++i)
+    if ((rc = make_map(&maps[i], bases[i], d, rows[i], BH, 128)) != FA_OK) return rc;
+
+  const size_t vec = align256(static_cast<size_t>(BH) * nq_pad * sizeof(float));
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, 2 * vec, s);
+  if (e != cudaSuccess) {
+    t_last_cuda = e;
+    return FA_ERR_NO_MEMORY;
+  }
+  fa::BwdPreParams pre{};
+  pre.o = o;
+  pre.dout = dout;
+  pre.lse = lse;
+  pre.lse2 = static_cast<float*>(ws);
+  pre.dd = reinterpret_cast<float*>(static_cast<char*>(ws) + vec);
+  pre.Nq = Nq;
+  pre.nq_pad = nq_pad;
+  pre.BH = BH;
+  fa::BwdParams p{};
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.BH = BH;
+  p.nq_pad = nq_pad;
+  p.wl = wl;
+  p.wr = wr;
+  p.causal = (wl < 0 && wr >= 0) ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.lse2 = pre.lse2;
+  p.dd = pre.dd;
+  p.timeout_ns = kDefaultTimeoutNs;
+  p.status = dev->status;
+  e = d == 64 ? fa::launch_bwd_d64(maps, p, pre, s) : fa::launch_bwd_d128(maps, p, pre, s);
+  cudaError_t e2 = cudaFreeAsync(ws, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (e2 != cudaSuccess) return cuda_fail(e2);
+  return FA_OK;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+           float scale, int causal, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, -1, causal ? 0 : -1,
+                  stream);
+}
+
+int fa_bwd_local(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
+                 int d, float scale, int window_left, int window_right, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, window_left,
+                  window_right, stream);
+}
+
 int fa_softmax_rows(const void* x, void* y, float* lse, long long rows, int cols, int dtype,
                     void* stream) {
   if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;

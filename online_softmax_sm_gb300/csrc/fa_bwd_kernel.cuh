@@ -1,0 +1,723 @@
+// fa_bwd_kernel.cuh -- attention backward from the saved LSE, for sm_103a.
+//
+// "Online Softmax 算法详解" section 8.3: the backward recomputes S = Q K^T,
+// restores P = exp(scale S - LSE) from the LSE the forward saved (no second
+// online softmax), and forms the gradients.  Written out (the derivative of
+// O = softmax(scale S) V):
+//   dV_j = sum_i P_ij dO_i          dP_ij = <dO_i, V_j>        D_i = <dO_i, O_i>
+//   dS_ij = P_ij (dP_ij - D_i)      dK_j = scale sum_i dS_ij Q_i
+//   dQ_i = scale sum_j dS_ij K_j
+// A row whose LSE is -inf (no visible key) has P = 0 (section 7.3).
+//
+// Two kernels, no atomics (dQ would otherwise need fp32 reductions from every
+// key tile of a head):
+//   fa_bwd_dkdv_kernel  one 128-key tile per CTA, K_j and V_j in shared memory,
+//     looping over the query tiles that see it.  S^T = K_j Q_i^T and
+//     dP^T = V_j dO_i^T go to TMEM; thread t of the compute warpgroups owns key
+//     t (TMEM lane t) and writes P^T and dS^T (bf16 pairs) back into the columns
+//     it has just read; dV_j += P^T dO_i and dK_j += dS^T Q_i then take them as
+//     the TMEM A operand.  One TMEM buffer each (512 columns at d = 128): S^T of
+//     step i+1 waits for dV of step i, dP^T for dK.
+//   fa_bwd_dq_kernel  one 128-row query tile per CTA, Q_i and dO_i in shared
+//     memory, looping over the key tiles it sees: S = Q_i K_j^T and
+//     dP = dO_i V_j^T (two dP buffers), dS (bf16) back into dP's columns, and
+//     dQ_i += dS K_j.  S of step j+1 is issued as soon as S of step j is read.
+//   S and dP are recomputed by both: 7 MMAs per tile pair instead of 5.
+// fa_bwd_pre_kernel  D_i and LSE * log2(e) per row (+inf for a row with no
+//   visible key or past Nq, so exp2(S c - lse2) is exactly 0 there), padded to
+//   whole 128-row tiles so the kernels copy them in 512-byte pieces.
+//
+// The two compute warpgroups split the 128 columns of S / dP: warpgroup h
+// takes columns [64h, 64h + 64) and writes its bf16 pairs into columns
+// [64h, 64h + 32) of the same region, so no warpgroup overwrites columns the
+// other still has to read.  The A operand's K-slice kk (16 elements = 8
+// columns) is therefore at column 64 (kk / 4) + 8 (kk % 4).
+//
+// Every wait is bounded (fa_wait.cuh); a wait that runs out stops the CTA
+// without writing its outputs.
+#pragma once
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+#include "fa_wait.cuh"
+
+namespace fa {
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kRows = 128;               // rows of a Q / K / V / dO tile
+  static constexpr int kChunks = D / 64;          // 64-column (128-byte) swizzle chunks
+  static constexpr int kChunkBytes = kRows * 128;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kVecBytes = kRows * 4;     // lse2 or dd of one tile
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kStageBytesA = 2 * kTileBytes + 2 * kVecBytes;  // Q_i, dO_i, lse2, dd
+  static constexpr int kStageBytesB = 2 * kTileBytes;                  // K_j, V_j
+  static constexpr int kCtlBytes = 1024;
+  static constexpr int kSmemA = 1024 + 2 * kTileBytes + kStages * kStageBytesA + kCtlBytes;
+  static constexpr int kSmemB = 1024 + 2 * kTileBytes + kStages * kStageBytesB + kCtlBytes;
+  static_assert(kSmemA <= 227 * 1024 && kSmemB <= 227 * 1024, "shared memory");
+  static_assert(kStageBytesA % 1024 == 0, "stage alignment");
+  static constexpr int kThreads = 384;  // two compute warpgroups + load / MMA / alloc warps
+  static constexpr int kLoadWarp = 8, kMmaWarp = 9, kAllocWarp = 10;
+  static constexpr int kTmemCols = 512;
+  // dK/dV kernel: S^T / P^T, dP^T / dS^T, then the two accumulators.
+  static constexpr int kS = 0, kDP = 128, kDV = 256, kDK = 256 + D;
+  // dQ kernel: S, two dP / dS buffers, dQ.
+  static constexpr int kDP0 = 128, kDP1 = 256, kDQ = 384;
+};
+
+struct __align__(8) BwdCtl {
+  uint64_t fixed_full;  // K_j, V_j (dK/dV) or Q_i, dO_i (dQ) landed
+  uint64_t full[4];     // ring stage landed
+  uint64_t empty[4];    // every MMA reading the stage completed
+  uint64_t s_full;      // S(^T) of this step in TMEM
+  uint64_t s_free;      // dQ kernel: S read by all 256 compute threads
+  uint64_t dp_full[2];  // dP(^T) in TMEM (buffer)
+  uint64_t ready[2];    // bf16 P^T / dS^T (or dS) written back to TMEM (256 arrivals)
+  uint64_t done_a;      // dK/dV kernel: dV MMA done (S columns free)
+  uint64_t done_b[2];   // dK MMA done (dP columns free) / dQ MMA of a buffer done
+  uint64_t drain;       // every MMA of the CTA completed
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Masks: key k is visible to query q iff q + off - wl <= k <= q + off + wr
+// (off = Nk - Nq, -1 = open side).
+__device__ __forceinline__ bool bwd_visible(int q, int k, const BwdParams& p) {
+  const int qa = q + p.Nk - p.Nq;
+  return (p.wl < 0 || k >= qa - p.wl) && (p.wr < 0 || k <= qa + p.wr) && k < p.Nk;
+}
+
+// Every (query, key) pair of the 128 x 128 tile pair is visible (a test that
+// is the same for every thread, so the mask loop is skipped as a whole).
+__device__ __forceinline__ bool bwd_tile_all_visible(int q0, int key0, const BwdParams& p) {
+  const int off = p.Nk - p.Nq;
+  const int q_last = min(q0 + 127, p.Nq - 1);
+  const int k_last = key0 + 127;
+  return k_last < p.Nk && (p.wl < 0 || key0 >= q_last + off - p.wl) &&
+         (p.wr < 0 || k_last <= q0 + off + p.wr);
+}
+
+// Shared-memory descriptors of a [128 rows][D] bf16 tile (128-byte swizzle):
+// as a K-major operand (K = D) and as an MN-major B operand (N = D, K = rows).
+template <int D>
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
+  return smem_desc_sw128(saddr, 16, 1024);
+}
+template <int D>
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr) {
+  return smem_desc_sw128(saddr, BwdCfg<D>::kChunkBytes, 1024);
+}
+// K-slice kk (16 elements) of a K-major tile: chunk kk / 4, 32 bytes per slice.
+template <int D>
+__device__ __forceinline__ uint32_t kslice_kmajor(int kk) {
+  return static_cast<uint32_t>((kk / 4) * BwdCfg<D>::kChunkBytes + (kk % 4) * 32) >> 4;
+}
+// K-slice kk (16 rows) of an MN-major tile: two 8-row groups of 1024 bytes.
+__device__ __forceinline__ uint32_t kslice_mnmajor(int kk) {
+  return static_cast<uint32_t>(kk * 2048) >> 4;
+}
+// TMEM column of K-slice kk of a bf16 A operand written by the two warpgroups.
+__device__ __forceinline__ uint32_t a_col(int kk) {
+  return static_cast<uint32_t>(64 * (kk / 4) + 8 * (kk % 4));
+}
+
+// Stage a [128][D] bf16 tile row for a TMA store: row t, columns
+// [c0, c0 + 32) (packed pairs w[16]) into the 128-byte-swizzled layout.
+template <int D>
+__device__ __forceinline__ void stage_row32(uint32_t tile, int t, int c0, const uint32_t* w) {
+  const int chunk = c0 / 64;
+  const int u0 = (c0 % 64) / 8;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int u = u0 + q;
+    st_shared_v4(tile + chunk * BwdCfg<D>::kChunkBytes + t * 128 + ((u ^ (t & 7)) << 4), w[4 * q],
+                 w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+}
+
+// ===================================================================== dK, dV
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_dk,
+                       const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + C::kTileBytes;
+  uint8_t* sRing = sV + C::kTileBytes;  // stage: Q_i, dO_i, lse2[128], dd[128]
+  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sRing + C::kStages * C::kStageBytesA);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int kt = blockIdx.x;  // key tile
+  const int bh = blockIdx.y;
+  const int key0 = kt * C::kRows;
+  const int off = p.Nk - p.Nq;
+  // query tiles with a row that sees a key of this tile
+  const int k_last = min(key0 + C::kRows, p.Nk) - 1;
+  const int qlo = p.wr < 0 ? 0 : max(0, key0 - off - p.wr);
+  const int qhi = p.wl < 0 ? p.Nq - 1 : min(p.Nq - 1, k_last - off + p.wl);
+  const int i_lo = qlo / C::kRows;
+  const int n = qhi >= qlo ? qhi / C::kRows + 1 - i_lo : 0;
+
+  const uint32_t bar_fixed = smem_u32(&ctl->fixed_full);
+  const uint32_t bar_full = smem_u32(&ctl->full[0]);
+  const uint32_t bar_empty = smem_u32(&ctl->empty[0]);
+  const uint32_t bar_s = smem_u32(&ctl->s_full);
+  const uint32_t bar_dp = smem_u32(&ctl->dp_full[0]);
+  const uint32_t bar_ready = smem_u32(&ctl->ready[0]);
+  const uint32_t bar_dv = smem_u32(&ctl->done_a);
+  const uint32_t bar_dk = smem_u32(&ctl->done_b[0]);
+  const uint32_t bar_drain = smem_u32(&ctl->drain);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_fixed, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_ready, 256);
+    mbar_init(bar_dv, 1);
+    mbar_init(bar_dk, 1);
+    mbar_init(bar_drain, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kAllocWarp) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const WaitCtx wc{&ctl->abort, p.status, p.timeout_ns};
+
+  if (warp == C::kLoadWarp) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      // (n = 0: no query sees this key tile; nothing is loaded, dK = dV = 0)
+      if (n > 0) {
+        mbar_arrive_expect_tx(bar_fixed, 2 * C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(smem_u32(sK + c * C::kChunkBytes), &tm_k, bar_fixed, c * 64, key0, bh);
+          tma_load_3d(smem_u32(sV + c * C::kChunkBytes), &tm_v, bar_fixed, c * 64, key0, bh);
+        }
+      }
+      const uint64_t pol = l2_policy_evict_last();
+      uint32_t issued_mask = 0, issued_par = 0;
+      bool ok = true;
+      for (int s = 0; ok && s < n; ++s) {
+        const int st = s % C::kStages, use = s / C::kStages;
+        if (use > 0 && !wait_bounded(bar_empty + 8 * st, (use - 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        const int q0 = (i_lo + s) * C::kRows;
+        uint8_t* base = sRing + st * C::kStageBytesA;
+        const uint32_t full = bar_full + 8 * st;
+        mbar_arrive_expect_tx(full, 2 * C::kTileBytes + 2 * C::kVecBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(smem_u32(base + c * C::kChunkBytes), &tm_q, full, c * 64, q0, bh);
+          tma_load_3d(smem_u32(base + C::kTileBytes + c * C::kChunkBytes), &tm_do, full, c * 64, q0,
+                      bh);
+        }
+        const size_t vrow = static_cast<size_t>(bh) * p.nq_pad + q0;
+        bulk_load(smem_u32(base + 2 * C::kTileBytes), p.lse2 + vrow, C::kVecBytes, full, pol);
+        bulk_load(smem_u32(base + 2 * C::kTileBytes + C::kVecBytes), p.dd + vrow, C::kVecBytes,
+                  full, pol);
+        issued_mask |= 1u << st;
+        issued_par = (issued_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+      }
+      for (int s = 0; s < C::kStages; ++s)
+        if ((issued_mask >> s) & 1u) wait_own(bar_full + 8 * s, (issued_par >> s) & 1u, p.timeout_ns);
+      if (n > 0) wait_own(bar_fixed, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == C::kMmaWarp) {
+    // --------------------------------------------------------- MMA issuer
+    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // A = K or V, B = Q or dO (K-major)
+    constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, true);   // B = dO or Q (MN-major)
+    const uint64_t dK = desc_kmajor<D>(smem_u32(sK));
+    const uint64_t dV = desc_kmajor<D>(smem_u32(sV));
+    bool ok = n > 0 && warp_wait(bar_fixed, 0, wc);
+    bool issued = false;
+    for (int s = 0; ok && s < n; ++s) {
+      const int st = s % C::kStages;
+      const uint32_t base = smem_u32(sRing + st * C::kStageBytesA);
+      ok = warp_wait(bar_full + 8 * st, (s / C::kStages) & 1, wc);
+      // S^T columns hold P^T of step s-1 until dV of step s-1 has read them
+      if (ok && s > 0) ok = warp_wait(bar_dv, (s - 1) & 1, wc);
+      if (!ok) break;
+      tc_fence_after();
+      {
+        const uint64_t dQk = desc_kmajor<D>(base);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss_elect(tmem + C::kS, dK + kslice_kmajor<D>(kk), dQk + kslice_kmajor<D>(kk),
+                            kIdescS, kk > 0);
+        mma_commit_elect(bar_s);
+      }
+      if (s > 0) ok = warp_wait(bar_dk, (s - 1) & 1, wc);  // dP^T columns hold dS^T of s-1
+      if (!ok) break;
+      tc_fence_after();
+      {
+        const uint64_t dOk = desc_kmajor<D>(base + C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss_elect(tmem + C::kDP, dV + kslice_kmajor<D>(kk), dOk + kslice_kmajor<D>(kk),
+                            kIdescS, kk > 0);
+        mma_commit_elect(bar_dp);
+      }
+      issued = true;
+      ok = warp_wait(bar_ready, s & 1, wc);  // P^T and dS^T written back
+      if (!ok) break;
+      tc_fence_after();
+      {
+        const uint64_t dOmn = desc_mnmajor<D>(base + C::kTileBytes);
+        const uint64_t dQmn = desc_mnmajor<D>(base);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_i (K = 128 queries)
+          mma_bf16_ts_elect(tmem + C::kDV, tmem + C::kS + a_col(kk), dOmn + kslice_mnmajor(kk),
+                            kIdescAcc, (s > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_elect(bar_dv);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_i
+          mma_bf16_ts_elect(tmem + C::kDK, tmem + C::kDP + a_col(kk), dQmn + kslice_mnmajor(kk),
+                            kIdescAcc, (s > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_elect(bar_dk);
+        mma_commit_elect(bar_empty + 8 * st);
+      }
+    }
+    // everything issued completes before the epilogue reads TMEM / TMEM is freed
+    mma_commit_elect(bar_drain);
+    if (issued) wait_own(bar_drain, 0, p.timeout_ns);
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------ compute warpgroups
+    const int h = warp >> 2;             // column half
+    const int t = (warp & 3) * 32 + lane;  // key row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int key = key0 + t;
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int s = 0; ok && s < n; ++s) {
+      const int st = s % C::kStages;
+      const int q0 = (i_lo + s) * C::kRows;
+      const float* lse2v = reinterpret_cast<const float*>(sRing + st * C::kStageBytesA + 2 * C::kTileBytes);
+      const float* ddv = lse2v + C::kRows;
+      // S^T, dP^T in TMEM; the stage's own barrier (complete by now) makes the
+      // bulk-copied lse2 / dd visible to these threads
+      ok = warp_wait(bar_s, s & 1, wc) && warp_wait(bar_dp, s & 1, wc) &&
+           warp_wait(bar_full + 8 * st, (s / C::kStages) & 1, wc);
+      if (!ok) break;
+      tc_fence_after();
+      const bool all_vis = bwd_tile_all_visible(q0, key0, p);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col = 64 * h + 32 * cc;
+        uint32_t sr[32], dr[32];
+        tmem_ld32_sync(tmem + lane_off + C::kS + col, sr);
+        tmem_ld32_sync(tmem + lane_off + C::kDP + col, dr);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          float pp[2], ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int qc = col + k + e;
+            float pv = ex2_approx(fmaf(__uint_as_float(sr[k + e]), c, -lse2v[qc]));
+            if (!all_vis && !bwd_visible(q0 + qc, key, p)) pv = 0.f;
+            pp[e] = pv;
+            ds[e] = pv * (__uint_as_float(dr[k + e]) - ddv[qc]);
+          }
+          pk[k >> 1] = pack_bf16x2(pp[0], pp[1]);
+          dk[k >> 1] = pack_bf16x2(ds[0], ds[1]);
+        }
+        tmem_st16(tmem + lane_off + C::kS + 64 * h + 16 * cc, pk);
+        tmem_st16(tmem + lane_off + C::kDP + 64 * h + 16 * cc, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_ready);
+    }
+    // ---- epilogue: dV, dK (x scale) -> bf16 -> the K / V buffers -> TMA store
+    if (ok && n > 0) ok = warp_wait(bar_drain, 0, wc);
+    const bool bad = named_bar_or(1, 256, !ok || *wc.abort);
+    if (!bad) {
+      if (n > 0) tc_fence_after();
+      const uint32_t stK = smem_u32(sK), stV = smem_u32(sV);
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {  // 0: dV, 1: dK
+        const float mul = part ? p.scale : 1.f;
+        const uint32_t src = tmem + lane_off + (part ? C::kDK : C::kDV);
+#pragma unroll
+        for (int cc = 0; cc < D / 2; cc += 32) {
+          const int col = h * (D / 2) + cc;
+          uint32_t r[32];
+          if (n > 0) {
+            tmem_ld32_sync(src + col, r);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) r[k] = 0u;
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            w[k] = pack_bf16x2(__uint_as_float(r[2 * k]) * mul, __uint_as_float(r[2 * k + 1]) * mul);
+          stage_row32<D>(part ? stK : stV, t, col, w);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 256);
+      if (threadIdx.x == 0) {
+#pragma unroll
+        for (int ch = 0; ch < C::kChunks; ++ch) {
+          tma_store_3d(&tm_dk, stK + ch * C::kChunkBytes, ch * 64, key0, bh);
+          tma_store_3d(&tm_dv, stV + ch * C::kChunkBytes, ch * 64, key0, bh);
+        }
+        tma_store_commit();
+        tma_store_wait_read();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kAllocWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ========================================================================= dQ
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+  uint8_t* sQ = smem;
+  uint8_t* sDO = sQ + C::kTileBytes;
+  uint8_t* sRing = sDO + C::kTileBytes;  // stage: K_j, V_j
+  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sRing + C::kStages * C::kStageBytesB);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qt = p.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int bh = blockIdx.y;
+  const int q0 = qt * C::kRows;
+  const int off = p.Nk - p.Nq;
+  // key tiles holding a key some row of this tile sees
+  const int q_last = min(q0 + C::kRows, p.Nq) - 1;
+  const int klo = p.wl < 0 ? 0 : max(0, q0 + off - p.wl);
+  const int khi = p.wr < 0 ? p.Nk - 1 : min(p.Nk - 1, q_last + off + p.wr);
+  const int j_lo = klo / C::kRows;
+  const int n = khi >= klo ? khi / C::kRows + 1 - j_lo : 0;
+
+  const uint32_t bar_fixed = smem_u32(&ctl->fixed_full);
+  const uint32_t bar_full = smem_u32(&ctl->full[0]);
+  const uint32_t bar_empty = smem_u32(&ctl->empty[0]);
+  const uint32_t bar_s = smem_u32(&ctl->s_full);
+  const uint32_t bar_sfree = smem_u32(&ctl->s_free);
+  const uint32_t bar_dp = smem_u32(&ctl->dp_full[0]);     // + 8 b
+  const uint32_t bar_ready = smem_u32(&ctl->ready[0]);    // + 8 b
+  const uint32_t bar_dq = smem_u32(&ctl->done_b[0]);      // + 8 b
+  const uint32_t bar_drain = smem_u32(&ctl->drain);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_fixed, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_sfree, 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_dp + 8 * b, 1);
+      mbar_init(bar_ready + 8 * b, 256);
+      mbar_init(bar_dq + 8 * b, 1);
+    }
+    mbar_init(bar_drain, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kAllocWarp) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const WaitCtx wc{&ctl->abort, p.status, p.timeout_ns};
+
+  if (warp == C::kLoadWarp) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      if (n > 0) {
+        mbar_arrive_expect_tx(bar_fixed, 2 * C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(smem_u32(sQ + c * C::kChunkBytes), &tm_q, bar_fixed, c * 64, q0, bh);
+          tma_load_3d(smem_u32(sDO + c * C::kChunkBytes), &tm_do, bar_fixed, c * 64, q0, bh);
+        }
+      }
+      uint32_t issued_mask = 0, issued_par = 0;
+      for (int j = 0; j < n; ++j) {
+        const int st = j % C::kStages, use = j / C::kStages;
+        if (use > 0 && !wait_bounded(bar_empty + 8 * st, (use - 1) & 1, wc)) break;
+        const int k0 = (j_lo + j) * C::kRows;
+        uint8_t* base = sRing + st * C::kStageBytesB;
+        const uint32_t full = bar_full + 8 * st;
+        mbar_arrive_expect_tx(full, 2 * C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(smem_u32(base + c * C::kChunkBytes), &tm_k, full, c * 64, k0, bh);
+          tma_load_3d(smem_u32(base + C::kTileBytes + c * C::kChunkBytes), &tm_v, full, c * 64, k0,
+                      bh);
+        }
+        issued_mask |= 1u << st;
+        issued_par = (issued_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+      }
+      for (int s = 0; s < C::kStages; ++s)
+        if ((issued_mask >> s) & 1u) wait_own(bar_full + 8 * s, (issued_par >> s) & 1u, p.timeout_ns);
+      if (n > 0) wait_own(bar_fixed, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == C::kMmaWarp) {
+    // --------------------------------------------------------- MMA issuer
+    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
+    constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, true);  // B = K_j (MN-major)
+    const uint64_t dQk = desc_kmajor<D>(smem_u32(sQ));
+    const uint64_t dOk = desc_kmajor<D>(smem_u32(sDO));
+    auto issue_s = [&](int j) {  // S = Q_i K_j^T
+      const uint64_t dKk = desc_kmajor<D>(smem_u32(sRing + (j % C::kStages) * C::kStageBytesB));
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16_ss_elect(tmem + C::kS, dQk + kslice_kmajor<D>(kk), dKk + kslice_kmajor<D>(kk),
+                          kIdescS, kk > 0);
+      mma_commit_elect(bar_s);
+    };
+    auto issue_dp = [&](int j) {  // dP = dO_i V_j^T into buffer j & 1
+      const uint64_t dVk =
+          desc_kmajor<D>(smem_u32(sRing + (j % C::kStages) * C::kStageBytesB + C::kTileBytes));
+      const uint32_t dst = tmem + ((j & 1) ? C::kDP1 : C::kDP0);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16_ss_elect(dst, dOk + kslice_kmajor<D>(kk), dVk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
+      mma_commit_elect(bar_dp + 8 * (j & 1));
+    };
+    bool ok = n > 0 && warp_wait(bar_fixed, 0, wc) && warp_wait(bar_full, 0, wc);
+    bool issued = false;
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
+      issue_dp(0);
+      issued = true;
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      if (j + 1 < n) {
+        const int st1 = (j + 1) % C::kStages;
+        ok = warp_wait(bar_full + 8 * st1, ((j + 1) / C::kStages) & 1, wc) &&
+             warp_wait(bar_sfree, j & 1, wc);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(j + 1);
+        // buffer (j+1) & 1 was last read by the dQ MMA of step j-1
+        if (j >= 1) ok = warp_wait(bar_dq + 8 * ((j + 1) & 1), ((j - 1) >> 1) & 1, wc);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dp(j + 1);
+      }
+      ok = warp_wait(bar_ready + 8 * (j & 1), (j >> 1) & 1, wc);  // dS of step j written back
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t dKmn = desc_mnmajor<D>(smem_u32(sRing + (j % C::kStages) * C::kStageBytesB));
+      const uint32_t src = tmem + ((j & 1) ? C::kDP1 : C::kDP0);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j (K = 128 keys)
+        mma_bf16_ts_elect(tmem + C::kDQ, src + a_col(kk), dKmn + kslice_mnmajor(kk), kIdescDQ,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_elect(bar_dq + 8 * (j & 1));
+      mma_commit_elect(bar_empty + 8 * (j % C::kStages));
+    }
+    mma_commit_elect(bar_drain);
+    if (issued) wait_own(bar_drain, 0, p.timeout_ns);
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------ compute warpgroups
+    const int h = warp >> 2;
+    const int t = (warp & 3) * 32 + lane;  // query row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int row = q0 + t;
+    const size_t vrow = static_cast<size_t>(bh) * p.nq_pad + row;
+    const float lse2 = p.lse2[vrow];
+    const float dd = p.dd[vrow];
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; ok && j < n; ++j) {
+      const int key0 = (j_lo + j) * C::kRows;
+      ok = warp_wait(bar_s, j & 1, wc);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[64];
+      tmem_ld32_sync(tmem + lane_off + C::kS + 64 * h, sr);
+      tmem_ld32_sync(tmem + lane_off + C::kS + 64 * h + 32, sr + 32);
+      tc_fence_before();
+      mbar_arrive(bar_sfree);  // S may be overwritten by S of step j+1
+      const uint32_t dpc = tmem + lane_off + ((j & 1) ? C::kDP1 : C::kDP0);
+      ok = warp_wait(bar_dp + 8 * (j & 1), (j >> 1) & 1, wc);
+      if (!ok) break;
+      tc_fence_after();
+      const bool all_vis = bwd_tile_all_visible(q0, key0, p);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col = 64 * h + 32 * cc;
+        uint32_t dr[32];
+        tmem_ld32_sync(dpc + col, dr);
+        uint32_t dk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          float ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float pv = ex2_approx(fmaf(__uint_as_float(sr[32 * cc + k + e]), c, -lse2));
+            if (!all_vis && !bwd_visible(row, key0 + col + k + e, p)) pv = 0.f;
+            ds[e] = pv * (__uint_as_float(dr[k + e]) - dd);
+          }
+          dk[k >> 1] = pack_bf16x2(ds[0], ds[1]);
+        }
+        tmem_st16(dpc + 64 * h + 16 * cc, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_ready + 8 * (j & 1));
+    }
+    // ---- epilogue: dQ x scale -> bf16 -> the Q buffer -> TMA store
+    if (ok && n > 0) ok = warp_wait(bar_drain, 0, wc);
+    const bool bad = named_bar_or(1, 256, !ok || *wc.abort);
+    if (!bad && q0 < p.Nq) {
+      if (n > 0) tc_fence_after();
+      const uint32_t stQ = smem_u32(sQ);
+#pragma unroll
+      for (int cc = 0; cc < D / 2; cc += 32) {
+        const int col = h * (D / 2) + cc;
+        uint32_t r[32];
+        if (n > 0) {
+          tmem_ld32_sync(tmem + lane_off + C::kDQ + col, r);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) r[k] = 0u;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w[k] = pack_bf16x2(__uint_as_float(r[2 * k]) * p.scale, __uint_as_float(r[2 * k + 1]) * p.scale);
+        stage_row32<D>(stQ, t, col, w);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 256);
+      if (threadIdx.x == 0) {
+#pragma unroll
+        for (int ch = 0; ch < C::kChunks; ++ch)
+          tma_store_3d(&tm_dq, stQ + ch * C::kChunkBytes, ch * 64, q0, bh);
+        tma_store_commit();
+        tma_store_wait_read();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kAllocWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ================================================================ preprocess
+// D_i = <dO_i, O_i> (fp32 over bf16 inputs) and lse2_i = LSE_i log2(e), or
+// +inf where LSE_i = -inf; rows in [Nq, nq_pad) get D = 0, lse2 = +inf.
+// d/8 lanes per row, one 16-byte load of O and of dO each.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdPreParams p) {
+  constexpr int kLanes = D / 8;
+  const long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = g / kLanes;
+  const int part = static_cast<int>(g % kLanes);
+  const long long rows = static_cast<long long>(p.BH) * p.nq_pad;
+  const bool live = row < rows;
+  const long long bh = live ? row / p.nq_pad : 0;
+  const int r = live ? static_cast<int>(row % p.nq_pad) : 0;
+  float acc = 0.f;
+  if (live && r < p.Nq) {
+    const size_t e = (static_cast<size_t>(bh) * p.Nq + r) * D + part * 8;
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.o) + e));
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout) + e));
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc = fmaf(__uint_as_float(wa[k] << 16), __uint_as_float(wb[k] << 16), acc);
+      acc = fmaf(__uint_as_float(wa[k] & 0xFFFF0000u), __uint_as_float(wb[k] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int o = kLanes / 2; o > 0; o >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, o, kLanes);
+  if (live && part == 0) {
+    float l2 = INFINITY;
+    if (r < p.Nq) {
+      const float lse = p.lse[static_cast<size_t>(bh) * p.Nq + r];
+      l2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
+    } else {
+      acc = 0.f;
+    }
+    p.lse2[row] = l2;
+    p.dd[row] = acc;
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_t(const CUtensorMap* maps, const BwdParams& p, const BwdPreParams& pre,
+                         cudaStream_t s) {
+  using C = BwdCfg<D>;
+  {
+    const long long threads = static_cast<long long>(pre.BH) * pre.nq_pad * (D / 8);
+    fa_bwd_pre_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(pre);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // maps: q, k, v, dout, dq, dk, dv
+  auto ka = fa_bwd_dkdv_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemA);
+  if (e != cudaSuccess) return e;
+  const dim3 grid_a((p.Nk + C::kRows - 1) / C::kRows, p.BH);
+  ka<<<grid_a, C::kThreads, C::kSmemA, s>>>(maps[0], maps[3], maps[1], maps[2], maps[5], maps[6], p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  auto kb = fa_bwd_dq_kernel<D>;
+  e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemB);
+  if (e != cudaSuccess) return e;
+  const dim3 grid_b((p.Nq + C::kRows - 1) / C::kRows, p.BH);
+  kb<<<grid_b, C::kThreads, C::kSmemB, s>>>(maps[0], maps[3], maps[1], maps[2], maps[4], p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa
