@@ -38,6 +38,7 @@ from online_softmax_sm_gb300 import workloads  # noqa: E402
 
 METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and % of dense BF16 tensor peak"
 SOFTMAX_METRIC = "row softmax throughput (two-pass online normaliser), algorithmic GB/s"
+BWD_METRIC = "attention bwd TFLOPS (bf16, 1×GB300; 2.5x the forward's FLOPs) and % of dense BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 WORKLOAD_ALIASES = {"c1": workloads.C1, "c2": workloads.C2, "c3": workloads.C3, "c4": workloads.C4,
                     "c4_masked": workloads.C4_MASKED, "c5": workloads.C5,
@@ -265,7 +266,8 @@ def oracle_rows(w: workloads.Workload, qh, kh, vh, rows, threads):
 
 
 def forward(fa, w: workloads.Workload, q, k, v, o, lse):
-    """One call of the library's public forward for this workload's mask."""
+    """One call of the library's public forward for this workload's mask
+    (o, lse: output buffers, or None to allocate)."""
     if w.window is not None:
         return fa.fwd_local(q, k, v, w.window[0], w.window[1], w.scale, w.n_splits, out=o, lse=lse)
     return fa.fwd(q, k, v, w.scale, w.causal, w.n_splits, out=o, lse=lse, bc=w.bc)
@@ -682,8 +684,96 @@ def run_softmax(args, sw):
         dist.destroy_process_group()
 
 
+def run_bwd(args, w):
+    """The attention backward: one fa_bwd call per step (row pass + dK/dV
+    kernel + dQ kernel), O, LSE and dO resident.  Algorithmic FLOPs: the five
+    products S, dP, dV, dK, dQ = 2.5 x the forward's."""
+    import online_softmax_sm_gb300 as fa
+
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "metric": BWD_METRIC,
+                              "unavailable": "the backward reference arm is not timed; the oracle's "
+                                             "gradients are the parity reference in the tests"}),
+                  flush=True)
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    fa.lib()
+    q, k, v = workloads.generate(w, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 1000)
+    do = torch.randn(q.shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    o, lse = forward(fa, w, q, k, v, None, None)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    window = w.window if w.window is not None else None
+    flops = 2.5 * w.flops
+
+    def step():
+        fa.bwd(q, k, v, o, lse, do, w.scale, causal=w.causal, window=window, dq=dq, dk=dk, dv=dv)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.device_status(dev) != fa.FA_OK:
+        raise SystemExit("device status reports a timed-out wait")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_region0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_region1 = time.time()
+    barrier(world)
+    sampler.stop()
+    if fa.device_status(dev) != fa.FA_OK:
+        raise SystemExit("device status reports a timed-out wait")
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_local = statistics.mean(step_ms)
+    ms, value = aggregate(world, flops, ms_local, dev)
+    peaks, peak_src = load_peaks()
+    achieved = flops / (ms_local * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": float(peaks["bf16_tflops"]),
+                "unit": "TFLOP/s", "frac": achieved / float(peaks["bf16_tflops"]),
+                "traffic": recorded_traffic(w.name + ":bwd"),
+                "kernel": "fa_bwd_pre + fa_bwd_dkdv_kernel + fa_bwd_dq_kernel", "kernel_ms": ms_local,
+                "algorithmic_flops_per_launch": flops,
+                "peak_source": peak_src + " bf16_tflops (burst: one step timed alone)"}
+    if rank == 0:
+        line = {"metric": BWD_METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": w.name + ":bwd", "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk,
+                           "d": w.d, "causal": w.causal,
+                           "window": list(w.window) if w.window is not None else None,
+                           "l2": "flushed before every timed step (512 MB write); inputs > L2",
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                "roofline": roofline, "cpu_baseline": None, "e2e": None,
+                "gpu_launches": 3 * args.steps, "clocks": sampler.summary(t_region0, t_region1),
+                "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
+    if args.workload.endswith(":bwd"):
+        run_bwd(args, workload_of(args.workload[: -len(":bwd")]))
+        return
     sw = softmax_workload_of(args.workload)
     if sw is not None:
         run_softmax(args, sw)

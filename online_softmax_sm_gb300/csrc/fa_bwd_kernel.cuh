@@ -12,12 +12,16 @@
 // Two kernels, no atomics (dQ would otherwise need fp32 reductions from every
 // key tile of a head):
 //   fa_bwd_dkdv_kernel  one 128-key tile per CTA, K_j and V_j in shared memory,
-//     looping over the query tiles that see it.  S^T = K_j Q_i^T and
-//     dP^T = V_j dO_i^T go to TMEM; thread t of the compute warpgroups owns key
-//     t (TMEM lane t) and writes P^T and dS^T (bf16 pairs) back into the columns
-//     it has just read; dV_j += P^T dO_i and dK_j += dS^T Q_i then take them as
-//     the TMEM A operand.  One TMEM buffer each (512 columns at d = 128): S^T of
-//     step i+1 waits for dV of step i, dP^T for dK.
+//     looping over the query tiles that see it, each as two half-steps of 64
+//     queries.  S^T = K_j Q^T and dP^T = V_j dO^T of a half-step go to TMEM
+//     buffer b (two buffers of 64 + 64 columns, then dV and dK: 512 columns at
+//     d = 128); compute warpgroup b owns buffer b (queries [64b, 64b + 64) of
+//     every tile): thread t owns key t (TMEM lane t) and writes P^T and dS^T
+//     (bf16 pairs) back into the columns it has just read; dV_j += P^T dO and
+//     dK_j += dS^T Q then take them as the TMEM A operand.  The MMA warp issues
+//     dV, dK of half-step h, then S^T of h+2 once dV(h) is done and dP^T of h+2
+//     once dK(h) is done: each follows the previous MMA on the tensor pipe, and
+//     each warpgroup has two half-steps of MMA time for its exponentials.
 //   fa_bwd_dq_kernel  one 128-row query tile per CTA, Q_i and dO_i in shared
 //     memory, looping over the key tiles it sees: S = Q_i K_j^T and
 //     dP = dO_i V_j^T (two dP buffers), dS (bf16) back into dP's columns, and
@@ -27,11 +31,11 @@
 //   visible key or past Nq, so exp2(S c - lse2) is exactly 0 there), padded to
 //   whole 128-row tiles so the kernels copy them in 512-byte pieces.
 //
-// The two compute warpgroups split the 128 columns of S / dP: warpgroup h
-// takes columns [64h, 64h + 64) and writes its bf16 pairs into columns
-// [64h, 64h + 32) of the same region, so no warpgroup overwrites columns the
-// other still has to read.  The A operand's K-slice kk (16 elements = 8
-// columns) is therefore at column 64 (kk / 4) + 8 (kk % 4).
+// In the dQ kernel the two compute warpgroups split the 128 columns of S / dP:
+// warpgroup h takes columns [64h, 64h + 64) and writes its bf16 pairs into
+// columns [64h, 64h + 32) of the same region, so no warpgroup overwrites
+// columns the other still has to read.  The A operand's K-slice kk (16
+// elements = 8 columns) is therefore at column 64 (kk / 4) + 8 (kk % 4).
 //
 // Every wait is bounded (fa_wait.cuh); a wait that runs out stops the CTA
 // without writing its outputs.
@@ -61,8 +65,14 @@ struct BwdCfg {
   static_assert(kStageBytesA % 1024 == 0, "stage alignment");
   static constexpr int kThreads = 384;  // two compute warpgroups + load / MMA / alloc warps
   static constexpr int kLoadWarp = 8, kMmaWarp = 9, kAllocWarp = 10;
+  // dK/dV kernel registers: launched with 168 per thread, then setmaxnreg
+  // moves them to the compute warpgroups (the split adds up to the launch
+  // budget, or setmaxnreg.inc could never be granted).
+  static constexpr int kRegLaunchA = 168, kRegComputeA = 216, kRegOtherA = 72;
+  static_assert(2 * kRegComputeA + kRegOtherA == 3 * kRegLaunchA, "setmaxnreg split");
   static constexpr int kTmemCols = 512;
-  // dK/dV kernel: S^T / P^T, dP^T / dS^T, then the two accumulators.
+  // dK/dV kernel: S^T / P^T buffers at 64 b, dP^T / dS^T at 128 + 64 b, then
+  // the two accumulators.
   static constexpr int kS = 0, kDP = 128, kDV = 256, kDK = 256 + D;
   // dQ kernel: S, two dP / dS buffers, dQ.
   static constexpr int kDP0 = 128, kDP1 = 256, kDQ = 384;
@@ -72,12 +82,12 @@ struct __align__(8) BwdCtl {
   uint64_t fixed_full;  // K_j, V_j (dK/dV) or Q_i, dO_i (dQ) landed
   uint64_t full[4];     // ring stage landed
   uint64_t empty[4];    // every MMA reading the stage completed
-  uint64_t s_full;      // S(^T) of this step in TMEM
+  uint64_t s_full[2];   // S(^T) of this step in TMEM (dK/dV: per buffer)
   uint64_t s_free;      // dQ kernel: S read by all 256 compute threads
   uint64_t dp_full[2];  // dP(^T) in TMEM (buffer)
-  uint64_t ready[2];    // bf16 P^T / dS^T (or dS) written back to TMEM (256 arrivals)
-  uint64_t done_a;      // dK/dV kernel: dV MMA done (S columns free)
-  uint64_t done_b[2];   // dK MMA done (dP columns free) / dQ MMA of a buffer done
+  uint64_t ready[2];    // bf16 P^T / dS^T (or dS) written back to TMEM
+  uint64_t done_a[2];   // dK/dV kernel: dV MMA of a buffer done (its S columns free)
+  uint64_t done_b[2];   // dK MMA of a buffer done (dP columns free) / dQ MMA of a buffer done
   uint64_t drain;       // every MMA of the CTA completed
   uint32_t tmem_base;
   int abort;
@@ -172,10 +182,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const uint32_t bar_fixed = smem_u32(&ctl->fixed_full);
   const uint32_t bar_full = smem_u32(&ctl->full[0]);
   const uint32_t bar_empty = smem_u32(&ctl->empty[0]);
-  const uint32_t bar_s = smem_u32(&ctl->s_full);
+  // per buffer b: + 8 b
+  const uint32_t bar_s = smem_u32(&ctl->s_full[0]);
   const uint32_t bar_dp = smem_u32(&ctl->dp_full[0]);
   const uint32_t bar_ready = smem_u32(&ctl->ready[0]);
-  const uint32_t bar_dv = smem_u32(&ctl->done_a);
+  const uint32_t bar_dv = smem_u32(&ctl->done_a[0]);
   const uint32_t bar_dk = smem_u32(&ctl->done_b[0]);
   const uint32_t bar_drain = smem_u32(&ctl->drain);
 
@@ -185,11 +196,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_s, 1);
-    mbar_init(bar_dp, 1);
-    mbar_init(bar_ready, 256);
-    mbar_init(bar_dv, 1);
-    mbar_init(bar_dk, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_s + 8 * b, 1);
+      mbar_init(bar_dp + 8 * b, 1);
+      mbar_init(bar_ready + 8 * b, 128);
+      mbar_init(bar_dv + 8 * b, 1);
+      mbar_init(bar_dk + 8 * b, 1);
+    }
     mbar_init(bar_drain, 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -204,7 +217,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
   const WaitCtx wc{&ctl->abort, p.status, p.timeout_ns};
 
-  if (warp == C::kLoadWarp) {
+  if (warp >= 8) {
+   setmaxnreg_dec<C::kRegOtherA>();
+   if (warp == C::kLoadWarp) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
       // (n = 0: no query sees this key tile; nothing is loaded, dK = dV = 0)
@@ -249,110 +264,149 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     __syncwarp();
   } else if (warp == C::kMmaWarp) {
     // --------------------------------------------------------- MMA issuer
-    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // A = K or V, B = Q or dO (K-major)
-    constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, true);   // B = dO or Q (MN-major)
+    // Half-step hs = 2 s + b covers queries [64 b, 64 b + 64) of query tile
+    // s and uses TMEM buffer b.
+    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false);  // A = K or V, B = Q or dO rows (K-major)
+    constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, true);  // B = dO or Q rows (MN-major)
     const uint64_t dK = desc_kmajor<D>(smem_u32(sK));
     const uint64_t dV = desc_kmajor<D>(smem_u32(sV));
-    bool ok = n > 0 && warp_wait(bar_fixed, 0, wc);
+    const int nh = 2 * n;
+    auto stage_base = [&](int hs) {
+      return smem_u32(sRing + ((hs >> 1) % C::kStages) * C::kStageBytesA);
+    };
+    // S^T = K_j Q_h^T into buffer hs & 1 (Q_h: 64 rows, 8 KB into every chunk)
+    auto issue_s = [&](int hs) {
+      const uint64_t dQk = desc_kmajor<D>(stage_base(hs) + (hs & 1) * 64 * 128);
+      const uint32_t dst = tmem + C::kS + 64 * (hs & 1);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16_ss_elect(dst, dK + kslice_kmajor<D>(kk), dQk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
+      mma_commit_elect(bar_s + 8 * (hs & 1));
+    };
+    auto issue_dp = [&](int hs) {  // dP^T = V_j dO_h^T
+      const uint64_t dOk = desc_kmajor<D>(stage_base(hs) + C::kTileBytes + (hs & 1) * 64 * 128);
+      const uint32_t dst = tmem + C::kDP + 64 * (hs & 1);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16_ss_elect(dst, dV + kslice_kmajor<D>(kk), dOk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
+      mma_commit_elect(bar_dp + 8 * (hs & 1));
+    };
+    bool ok = n > 0 && warp_wait(bar_fixed, 0, wc) && warp_wait(bar_full, 0, wc);
     bool issued = false;
-    for (int s = 0; ok && s < n; ++s) {
-      const int st = s % C::kStages;
-      const uint32_t base = smem_u32(sRing + st * C::kStageBytesA);
-      ok = warp_wait(bar_full + 8 * st, (s / C::kStages) & 1, wc);
-      // S^T columns hold P^T of step s-1 until dV of step s-1 has read them
-      if (ok && s > 0) ok = warp_wait(bar_dv, (s - 1) & 1, wc);
-      if (!ok) break;
+    if (ok) {
       tc_fence_after();
-      {
-        const uint64_t dQk = desc_kmajor<D>(base);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss_elect(tmem + C::kS, dK + kslice_kmajor<D>(kk), dQk + kslice_kmajor<D>(kk),
-                            kIdescS, kk > 0);
-        mma_commit_elect(bar_s);
-      }
-      if (s > 0) ok = warp_wait(bar_dk, (s - 1) & 1, wc);  // dP^T columns hold dS^T of s-1
-      if (!ok) break;
-      tc_fence_after();
-      {
-        const uint64_t dOk = desc_kmajor<D>(base + C::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss_elect(tmem + C::kDP, dV + kslice_kmajor<D>(kk), dOk + kslice_kmajor<D>(kk),
-                            kIdescS, kk > 0);
-        mma_commit_elect(bar_dp);
-      }
+      issue_s(0);
+      issue_dp(0);
+      issue_s(1);
+      issue_dp(1);
       issued = true;
-      ok = warp_wait(bar_ready, s & 1, wc);  // P^T and dS^T written back
+    }
+    for (int hs = 0; ok && hs < nh; ++hs) {
+      const int b = hs & 1;
+      const uint32_t par = static_cast<uint32_t>((hs >> 1) & 1);
+      ok = warp_wait(bar_ready + 8 * b, par, wc);  // P^T and dS^T of hs written back
       if (!ok) break;
       tc_fence_after();
       {
+        const uint32_t base = stage_base(hs);
         const uint64_t dOmn = desc_mnmajor<D>(base + C::kTileBytes);
         const uint64_t dQmn = desc_mnmajor<D>(base);
+        const uint32_t pa = tmem + C::kS + 64 * b, da = tmem + C::kDP + 64 * b;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_i (K = 128 queries)
-          mma_bf16_ts_elect(tmem + C::kDV, tmem + C::kS + a_col(kk), dOmn + kslice_mnmajor(kk),
-                            kIdescAcc, (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_elect(bar_dv);
+        for (int kk = 0; kk < 4; ++kk)  // dV += P^T dO_h (K = 64 queries: rows 64 b + 16 kk)
+          mma_bf16_ts_elect(tmem + C::kDV, pa + 8 * kk, dOmn + kslice_mnmajor(4 * b + kk), kIdescAcc,
+                            (hs > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_elect(bar_dv + 8 * b);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_i
-          mma_bf16_ts_elect(tmem + C::kDK, tmem + C::kDP + a_col(kk), dQmn + kslice_mnmajor(kk),
-                            kIdescAcc, (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_elect(bar_dk);
-        mma_commit_elect(bar_empty + 8 * st);
+        for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q_h
+          mma_bf16_ts_elect(tmem + C::kDK, da + 8 * kk, dQmn + kslice_mnmajor(4 * b + kk), kIdescAcc,
+                            (hs > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_elect(bar_dk + 8 * b);
+        if (b == 1) mma_commit_elect(bar_empty + 8 * ((hs >> 1) % C::kStages));  // tile done
+      }
+      const int nx = hs + 2;
+      if (nx < nh) {
+        // buffer b again: S^T once dV(hs) has read P^T, dP^T once dK(hs) has read dS^T
+        if (b == 0) ok = warp_wait(bar_full + 8 * ((nx >> 1) % C::kStages), ((nx >> 1) / C::kStages) & 1, wc);
+        ok = ok && warp_wait(bar_dv + 8 * b, par, wc);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(nx);
+        ok = warp_wait(bar_dk + 8 * b, par, wc);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dp(nx);
       }
     }
     // everything issued completes before the epilogue reads TMEM / TMEM is freed
     mma_commit_elect(bar_drain);
     if (issued) wait_own(bar_drain, 0, p.timeout_ns);
     __syncwarp();
-  } else if (warp < 8) {
+   }
+  } else {
+    setmaxnreg_inc<C::kRegComputeA>();
     // ------------------------------------------------ compute warpgroups
-    const int h = warp >> 2;             // column half
+    const int h = warp >> 2;               // buffer / query half of every tile
     const int t = (warp & 3) * 32 + lane;  // key row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int key = key0 + t;
     const float c = p.scale_log2;
+    const uint32_t tS = tmem + lane_off + C::kS + 64 * h;
+    const uint32_t tDP = tmem + lane_off + C::kDP + 64 * h;
     bool ok = true;
     for (int s = 0; ok && s < n; ++s) {
       const int st = s % C::kStages;
-      const int q0 = (i_lo + s) * C::kRows;
-      const float* lse2v = reinterpret_cast<const float*>(sRing + st * C::kStageBytesA + 2 * C::kTileBytes);
+      const int q0 = (i_lo + s) * C::kRows + 64 * h;  // this half's first query
+      const float* lse2v = reinterpret_cast<const float*>(sRing + st * C::kStageBytesA + 2 * C::kTileBytes) + 64 * h;
       const float* ddv = lse2v + C::kRows;
-      // S^T, dP^T in TMEM; the stage's own barrier (complete by now) makes the
-      // bulk-copied lse2 / dd visible to these threads
-      ok = warp_wait(bar_s, s & 1, wc) && warp_wait(bar_dp, s & 1, wc) &&
+      // S^T, dP^T of this half in TMEM; the stage's own barrier (complete by
+      // now) makes the bulk-copied lse2 / dd visible to these threads
+      ok = warp_wait(bar_s + 8 * h, s & 1, wc) && warp_wait(bar_dp + 8 * h, s & 1, wc) &&
            warp_wait(bar_full + 8 * st, (s / C::kStages) & 1, wc);
       if (!ok) break;
       tc_fence_after();
-      const bool all_vis = bwd_tile_all_visible(q0, key0, p);
+      const bool all_vis = bwd_tile_all_visible(q0, key0, p);  // (a superset test: 128 queries)
+      // the whole half-step's S^T and dP^T rows (64 + 64 columns) at once
+      uint32_t srow[64], drow[64];
+      tmem_ld64_sync(tS, srow);
+      tmem_ld64_sync(tDP, drow);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const int col = 64 * h + 32 * cc;
-        uint32_t sr[32], dr[32];
-        tmem_ld32_sync(tmem + lane_off + C::kS + col, sr);
-        tmem_ld32_sync(tmem + lane_off + C::kDP + col, dr);
+        const uint32_t* sr = srow + 32 * cc;
+        const uint32_t* dr = drow + 32 * cc;
+        float lv[32], dv[32];
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(lse2v + 32 * cc + k);
+          const float4 d4 = *reinterpret_cast<const float4*>(ddv + 32 * cc + k);
+          lv[k] = a4.x, lv[k + 1] = a4.y, lv[k + 2] = a4.z, lv[k + 3] = a4.w;
+          dv[k] = d4.x, dv[k + 1] = d4.y, dv[k + 2] = d4.z, dv[k + 3] = d4.w;
+        }
+        float pv[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pv[k] = ex2_approx(fmaf(__uint_as_float(sr[k]), c, -lv[k]));
+        // edge tiles only: the mask in a block of its own, so fully visible
+        // tiles run the loop above with no per-element test
+        if (!all_vis) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (!bwd_visible(q0 + 32 * cc + k, key, p)) pv[k] = 0.f;
+        }
         uint32_t pk[16], dk[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          float pp[2], ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int qc = col + k + e;
-            float pv = ex2_approx(fmaf(__uint_as_float(sr[k + e]), c, -lse2v[qc]));
-            if (!all_vis && !bwd_visible(q0 + qc, key, p)) pv = 0.f;
-            pp[e] = pv;
-            ds[e] = pv * (__uint_as_float(dr[k + e]) - ddv[qc]);
-          }
-          pk[k >> 1] = pack_bf16x2(pp[0], pp[1]);
-          dk[k >> 1] = pack_bf16x2(ds[0], ds[1]);
+          const float d0 = pv[k] * (__uint_as_float(dr[k]) - dv[k]);
+          const float d1 = pv[k + 1] * (__uint_as_float(dr[k + 1]) - dv[k + 1]);
+          pk[k >> 1] = pack_bf16x2(pv[k], pv[k + 1]);
+          dk[k >> 1] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(tmem + lane_off + C::kS + 64 * h + 16 * cc, pk);
-        tmem_st16(tmem + lane_off + C::kDP + 64 * h + 16 * cc, dk);
+        // pairs into columns already read: chunk cc -> [16 cc, 16 cc + 16)
+        tmem_st16(tS + 16 * cc, pk);
+        tmem_st16(tDP + 16 * cc, dk);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_ready);
+      mbar_arrive(bar_ready + 8 * h);
     }
     // ---- epilogue: dV, dK (x scale) -> bf16 -> the K / V buffers -> TMA store
     if (ok && n > 0) ok = warp_wait(bar_drain, 0, wc);
@@ -436,7 +490,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const uint32_t bar_fixed = smem_u32(&ctl->fixed_full);
   const uint32_t bar_full = smem_u32(&ctl->full[0]);
   const uint32_t bar_empty = smem_u32(&ctl->empty[0]);
-  const uint32_t bar_s = smem_u32(&ctl->s_full);
+  const uint32_t bar_s = smem_u32(&ctl->s_full[0]);
   const uint32_t bar_sfree = smem_u32(&ctl->s_free);
   const uint32_t bar_dp = smem_u32(&ctl->dp_full[0]);     // + 8 b
   const uint32_t bar_ready = smem_u32(&ctl->ready[0]);    // + 8 b
@@ -594,18 +648,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const int col = 64 * h + 32 * cc;
         uint32_t dr[32];
         tmem_ld32_sync(dpc + col, dr);
+        float pv[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pv[k] = ex2_approx(fmaf(__uint_as_float(sr[32 * cc + k]), c, -lse2));
+        if (!all_vis) {  // edge tiles only
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (!bwd_visible(row, key0 + col + k, p)) pv[k] = 0.f;
+        }
         uint32_t dk[16];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          float ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float pv = ex2_approx(fmaf(__uint_as_float(sr[32 * cc + k + e]), c, -lse2));
-            if (!all_vis && !bwd_visible(row, key0 + col + k + e, p)) pv = 0.f;
-            ds[e] = pv * (__uint_as_float(dr[k + e]) - dd);
-          }
-          dk[k >> 1] = pack_bf16x2(ds[0], ds[1]);
-        }
+        for (int k = 0; k < 32; k += 2)
+          dk[k >> 1] = pack_bf16x2(pv[k] * (__uint_as_float(dr[k]) - dd),
+                                   pv[k + 1] * (__uint_as_float(dr[k + 1]) - dd));
         tmem_st16(dpc + 64 * h + 16 * cc, dk);
       }
       tmem_wait_st();
@@ -707,6 +762,12 @@ cudaError_t launch_bwd_t(const CUtensorMap* maps, const BwdParams& p, const BwdP
   }
   // maps: q, k, v, dout, dq, dk, dv
   auto ka = fa_bwd_dkdv_kernel<D>;
+  // The setmaxnreg split assumes exactly kRegLaunchA registers per thread at launch.
+  static const bool regs_ok = [&] {
+    cudaFuncAttributes attr{};
+    return cudaFuncGetAttributes(&attr, ka) == cudaSuccess && attr.numRegs == C::kRegLaunchA;
+  }();
+  if (!regs_ok) return cudaErrorInvalidKernelImage;
   cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemA);
   if (e != cudaSuccess) return e;
   const dim3 grid_a((p.Nk + C::kRows - 1) / C::kRows, p.BH);
