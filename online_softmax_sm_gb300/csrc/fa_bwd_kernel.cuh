@@ -57,14 +57,21 @@ struct BwdCfg {
   static constexpr int kVecBytes = kRows * 4;     // lse2 or dd of one tile
   static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kStageBytesA = 2 * kTileBytes + 2 * kVecBytes;  // Q_i, dO_i, lse2, dd
-  static constexpr int kStageBytesB = 2 * kTileBytes;                  // K_j, V_j
+  // dQ kernel: K_j and V_j in separate slots of a ring, K_j at position 2 j
+  // and V_j at 2 j + 1; each slot is released by its own last reader.
+  static constexpr int kSlotsFit = (227 * 1024 - 1024 - 2 * kTileBytes - 1024) / kTileBytes;
+  static constexpr int kSlotsB = kSlotsFit > 8 ? 8 : kSlotsFit;
+  static constexpr int kStageBytesB = kTileBytes;
   static constexpr int kCtlBytes = 1024;
   static constexpr int kSmemA = 1024 + 2 * kTileBytes + kStages * kStageBytesA + kCtlBytes;
-  static constexpr int kSmemB = 1024 + 2 * kTileBytes + kStages * kStageBytesB + kCtlBytes;
+  static constexpr int kSmemB = 1024 + 2 * kTileBytes + kSlotsB * kStageBytesB + kCtlBytes;
+  static_assert(kSlotsB >= 4, "dQ kernel ring");
   static_assert(kSmemA <= 227 * 1024 && kSmemB <= 227 * 1024, "shared memory");
   static_assert(kStageBytesA % 1024 == 0, "stage alignment");
   static constexpr int kThreads = 384;  // two compute warpgroups + load / MMA / alloc warps
-  static constexpr int kLoadWarp = 8, kMmaWarp = 9, kAllocWarp = 10;
+  // Two MMA issuers: one for the products that fill S / dP, one for the
+  // products that consume P / dS (dK/dV kernel: dV, dK; dQ kernel: dQ).
+  static constexpr int kLoadWarp = 8, kMmaWarp = 9, kAllocWarp = 10, kMmaWarp2 = 11;
   // dK/dV kernel registers: launched with 168 per thread, then setmaxnreg
   // moves them to the compute warpgroups (the split adds up to the launch
   // budget, or setmaxnreg.inc could never be granted).
@@ -80,8 +87,8 @@ struct BwdCfg {
 
 struct __align__(8) BwdCtl {
   uint64_t fixed_full;  // K_j, V_j (dK/dV) or Q_i, dO_i (dQ) landed
-  uint64_t full[4];     // ring stage landed
-  uint64_t empty[4];    // every MMA reading the stage completed
+  uint64_t full[8];     // ring stage / slot landed
+  uint64_t empty[8];    // every MMA reading the stage / slot completed
   uint64_t s_full[2];   // S(^T) of this step in TMEM (dK/dV: per buffer)
   uint64_t s_free;      // dQ kernel: S read by all 256 compute threads
   uint64_t dp_full[2];  // dP(^T) in TMEM (buffer)
@@ -203,7 +210,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_init(bar_dv + 8 * b, 1);
       mbar_init(bar_dk + 8 * b, 1);
     }
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, 2);  // one commit per MMA issuer
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -262,52 +269,66 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (n > 0) wait_own(bar_fixed, 0, p.timeout_ns);
     }
     __syncwarp();
-  } else if (warp == C::kMmaWarp) {
-    // --------------------------------------------------------- MMA issuer
+  } else if (warp == C::kMmaWarp || warp == C::kMmaWarp2) {
+    // --------------------------------------------------------- MMA issuers
     // Half-step hs = 2 s + b covers queries [64 b, 64 b + 64) of query tile
-    // s and uses TMEM buffer b.
+    // s and uses TMEM buffer b.  Warp kMmaWarp2 fills buffers (S^T, dP^T);
+    // warp kMmaWarp consumes them (dV, dK).  Between the two only barriers:
+    // S^T of hs+2 once dV of hs has read P^T, dP^T once dK has read dS^T.
     constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false);  // A = K or V, B = Q or dO rows (K-major)
     constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, true);  // B = dO or Q rows (MN-major)
-    const uint64_t dK = desc_kmajor<D>(smem_u32(sK));
-    const uint64_t dV = desc_kmajor<D>(smem_u32(sV));
     const int nh = 2 * n;
     auto stage_base = [&](int hs) {
       return smem_u32(sRing + ((hs >> 1) % C::kStages) * C::kStageBytesA);
     };
-    // S^T = K_j Q_h^T into buffer hs & 1 (Q_h: 64 rows, 8 KB into every chunk)
-    auto issue_s = [&](int hs) {
-      const uint64_t dQk = desc_kmajor<D>(stage_base(hs) + (hs & 1) * 64 * 128);
-      const uint32_t dst = tmem + C::kS + 64 * (hs & 1);
+    bool ok = n > 0 && warp_wait(bar_fixed, 0, wc);
+    if (warp == C::kMmaWarp2) {
+      const uint64_t dK = desc_kmajor<D>(smem_u32(sK));
+      const uint64_t dV = desc_kmajor<D>(smem_u32(sV));
+      // S^T = K_j Q_h^T into buffer hs & 1 (Q_h: 64 rows, 8 KB into every chunk)
+      auto issue_s = [&](int hs) {
+        const uint64_t dQk = desc_kmajor<D>(stage_base(hs) + (hs & 1) * 64 * 128);
+        const uint32_t dst = tmem + C::kS + 64 * (hs & 1);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_bf16_ss_elect(dst, dK + kslice_kmajor<D>(kk), dQk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
-      mma_commit_elect(bar_s + 8 * (hs & 1));
-    };
-    auto issue_dp = [&](int hs) {  // dP^T = V_j dO_h^T
-      const uint64_t dOk = desc_kmajor<D>(stage_base(hs) + C::kTileBytes + (hs & 1) * 64 * 128);
-      const uint32_t dst = tmem + C::kDP + 64 * (hs & 1);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss_elect(dst, dK + kslice_kmajor<D>(kk), dQk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
+        mma_commit_elect(bar_s + 8 * (hs & 1));
+      };
+      auto issue_dp = [&](int hs) {  // dP^T = V_j dO_h^T
+        const uint64_t dOk = desc_kmajor<D>(stage_base(hs) + C::kTileBytes + (hs & 1) * 64 * 128);
+        const uint32_t dst = tmem + C::kDP + 64 * (hs & 1);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_bf16_ss_elect(dst, dV + kslice_kmajor<D>(kk), dOk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
-      mma_commit_elect(bar_dp + 8 * (hs & 1));
-    };
-    bool ok = n > 0 && warp_wait(bar_fixed, 0, wc) && warp_wait(bar_full, 0, wc);
-    bool issued = false;
-    if (ok) {
-      tc_fence_after();
-      issue_s(0);
-      issue_dp(0);
-      issue_s(1);
-      issue_dp(1);
-      issued = true;
-    }
-    for (int hs = 0; ok && hs < nh; ++hs) {
-      const int b = hs & 1;
-      const uint32_t par = static_cast<uint32_t>((hs >> 1) & 1);
-      ok = warp_wait(bar_ready + 8 * b, par, wc);  // P^T and dS^T of hs written back
-      if (!ok) break;
-      tc_fence_after();
-      {
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss_elect(dst, dV + kslice_kmajor<D>(kk), dOk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
+        mma_commit_elect(bar_dp + 8 * (hs & 1));
+      };
+      if (ok) ok = warp_wait(bar_full, 0, wc);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+        issue_s(1);
+        issue_dp(1);
+      }
+      for (int hs = 0; ok && hs + 2 < nh; ++hs) {
+        const int b = hs & 1, nx = hs + 2;
+        const uint32_t par = static_cast<uint32_t>((hs >> 1) & 1);
+        if (b == 0) ok = warp_wait(bar_full + 8 * ((nx >> 1) % C::kStages), ((nx >> 1) / C::kStages) & 1, wc);
+        ok = ok && warp_wait(bar_dv + 8 * b, par, wc);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(nx);
+        ok = warp_wait(bar_dk + 8 * b, par, wc);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dp(nx);
+      }
+    } else {
+      for (int hs = 0; ok && hs < nh; ++hs) {
+        const int b = hs & 1;
+        ok = warp_wait(bar_ready + 8 * b, static_cast<uint32_t>((hs >> 1) & 1), wc);
+        if (!ok) break;
+        tc_fence_after();
         const uint32_t base = stage_base(hs);
         const uint64_t dOmn = desc_mnmajor<D>(base + C::kTileBytes);
         const uint64_t dQmn = desc_mnmajor<D>(base);
@@ -322,25 +343,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_bf16_ts_elect(tmem + C::kDK, da + 8 * kk, dQmn + kslice_mnmajor(4 * b + kk), kIdescAcc,
                             (hs > 0 || kk > 0) ? 1u : 0u);
         mma_commit_elect(bar_dk + 8 * b);
-        if (b == 1) mma_commit_elect(bar_empty + 8 * ((hs >> 1) % C::kStages));  // tile done
-      }
-      const int nx = hs + 2;
-      if (nx < nh) {
-        // buffer b again: S^T once dV(hs) has read P^T, dP^T once dK(hs) has read dS^T
-        if (b == 0) ok = warp_wait(bar_full + 8 * ((nx >> 1) % C::kStages), ((nx >> 1) / C::kStages) & 1, wc);
-        ok = ok && warp_wait(bar_dv + 8 * b, par, wc);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s(nx);
-        ok = warp_wait(bar_dk + 8 * b, par, wc);
-        if (!ok) break;
-        tc_fence_after();
-        issue_dp(nx);
+        // both halves of the tile done: S^T / dP^T (the other warp) completed
+        // before their P^T / dS^T were written back, so this commit covers
+        // every read of the stage
+        if (b == 1) mma_commit_elect(bar_empty + 8 * ((hs >> 1) % C::kStages));
       }
     }
     // everything issued completes before the epilogue reads TMEM / TMEM is freed
     mma_commit_elect(bar_drain);
-    if (issued) wait_own(bar_drain, 0, p.timeout_ns);
+    if (n > 0) wait_own(bar_drain, 0, p.timeout_ns);
     __syncwarp();
    }
   } else {
@@ -471,8 +482,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint8_t* sQ = smem;
   uint8_t* sDO = sQ + C::kTileBytes;
-  uint8_t* sRing = sDO + C::kTileBytes;  // stage: K_j, V_j
-  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sRing + C::kStages * C::kStageBytesB);
+  uint8_t* sRing = sDO + C::kTileBytes;  // slots: K_j at position 2 j, V_j at 2 j + 1
+  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sRing + C::kSlotsB * C::kStageBytesB);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -499,7 +510,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_fixed, 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kSlotsB; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
@@ -510,7 +521,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_init(bar_ready + 8 * b, 256);
       mbar_init(bar_dq + 8 * b, 1);
     }
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, 2);  // one commit per MMA issuer
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -536,86 +547,84 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
       }
       uint32_t issued_mask = 0, issued_par = 0;
-      for (int j = 0; j < n; ++j) {
-        const int st = j % C::kStages, use = j / C::kStages;
-        if (use > 0 && !wait_bounded(bar_empty + 8 * st, (use - 1) & 1, wc)) break;
-        const int k0 = (j_lo + j) * C::kRows;
-        uint8_t* base = sRing + st * C::kStageBytesB;
-        const uint32_t full = bar_full + 8 * st;
-        mbar_arrive_expect_tx(full, 2 * C::kTileBytes);
+      for (int pos = 0; pos < 2 * n; ++pos) {
+        const int sl = pos % C::kSlotsB, use = pos / C::kSlotsB;
+        if (use > 0 && !wait_bounded(bar_empty + 8 * sl, (use - 1) & 1, wc)) break;
+        const int k0 = (j_lo + (pos >> 1)) * C::kRows;
+        uint8_t* base = sRing + sl * C::kStageBytesB;
+        const uint32_t full = bar_full + 8 * sl;
+        const CUtensorMap* map = (pos & 1) ? &tm_v : &tm_k;
+        mbar_arrive_expect_tx(full, C::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(smem_u32(base + c * C::kChunkBytes), &tm_k, full, c * 64, k0, bh);
-          tma_load_3d(smem_u32(base + C::kTileBytes + c * C::kChunkBytes), &tm_v, full, c * 64, k0,
-                      bh);
-        }
-        issued_mask |= 1u << st;
-        issued_par = (issued_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem_u32(base + c * C::kChunkBytes), map, full, c * 64, k0, bh);
+        issued_mask |= 1u << sl;
+        issued_par = (issued_par & ~(1u << sl)) | (static_cast<uint32_t>(use & 1) << sl);
       }
-      for (int s = 0; s < C::kStages; ++s)
+      for (int s = 0; s < C::kSlotsB; ++s)
         if ((issued_mask >> s) & 1u) wait_own(bar_full + 8 * s, (issued_par >> s) & 1u, p.timeout_ns);
       if (n > 0) wait_own(bar_fixed, 0, p.timeout_ns);
     }
     __syncwarp();
-  } else if (warp == C::kMmaWarp) {
-    // --------------------------------------------------------- MMA issuer
+  } else if (warp == C::kMmaWarp || warp == C::kMmaWarp2) {
+    // --------------------------------------------------------- MMA issuers
+    // Warp kMmaWarp: S(j) = Q_i K_j^T once every row has read S(j-1), and
+    // dP(j) = dO_i V_j^T into buffer j & 1 once dQ(j-2) has read that buffer.
+    // Warp kMmaWarp2: dQ += dS(j) K_j once dS(j) is written back.
     constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
     constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, true);  // B = K_j (MN-major)
-    const uint64_t dQk = desc_kmajor<D>(smem_u32(sQ));
-    const uint64_t dOk = desc_kmajor<D>(smem_u32(sDO));
-    auto issue_s = [&](int j) {  // S = Q_i K_j^T
-      const uint64_t dKk = desc_kmajor<D>(smem_u32(sRing + (j % C::kStages) * C::kStageBytesB));
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_bf16_ss_elect(tmem + C::kS, dQk + kslice_kmajor<D>(kk), dKk + kslice_kmajor<D>(kk),
-                          kIdescS, kk > 0);
-      mma_commit_elect(bar_s);
+    auto slot = [&](int pos) { return smem_u32(sRing + (pos % C::kSlotsB) * C::kStageBytesB); };
+    auto slot_full = [&](int pos) {
+      return warp_wait(bar_full + 8 * (pos % C::kSlotsB), (pos / C::kSlotsB) & 1, wc);
     };
-    auto issue_dp = [&](int j) {  // dP = dO_i V_j^T into buffer j & 1
-      const uint64_t dVk =
-          desc_kmajor<D>(smem_u32(sRing + (j % C::kStages) * C::kStageBytesB + C::kTileBytes));
-      const uint32_t dst = tmem + ((j & 1) ? C::kDP1 : C::kDP0);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_bf16_ss_elect(dst, dOk + kslice_kmajor<D>(kk), dVk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
-      mma_commit_elect(bar_dp + 8 * (j & 1));
-    };
-    bool ok = n > 0 && warp_wait(bar_fixed, 0, wc) && warp_wait(bar_full, 0, wc);
-    bool issued = false;
-    if (ok) {
-      tc_fence_after();
-      issue_s(0);
-      issue_dp(0);
-      issued = true;
-    }
-    for (int j = 0; ok && j < n; ++j) {
-      if (j + 1 < n) {
-        const int st1 = (j + 1) % C::kStages;
-        ok = warp_wait(bar_full + 8 * st1, ((j + 1) / C::kStages) & 1, wc) &&
-             warp_wait(bar_sfree, j & 1, wc);
+    bool ok = n > 0 && warp_wait(bar_fixed, 0, wc);
+    if (warp == C::kMmaWarp) {
+      const uint64_t dQk = desc_kmajor<D>(smem_u32(sQ));
+      const uint64_t dOk = desc_kmajor<D>(smem_u32(sDO));
+      for (int j = 0; ok && j < n; ++j) {
+        ok = slot_full(2 * j) && (j == 0 || warp_wait(bar_sfree, (j - 1) & 1, wc));
         if (!ok) break;
         tc_fence_after();
-        issue_s(j + 1);
-        // buffer (j+1) & 1 was last read by the dQ MMA of step j-1
-        if (j >= 1) ok = warp_wait(bar_dq + 8 * ((j + 1) & 1), ((j - 1) >> 1) & 1, wc);
+        {
+          const uint64_t dKk = desc_kmajor<D>(slot(2 * j));
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss_elect(tmem + C::kS, dQk + kslice_kmajor<D>(kk), dKk + kslice_kmajor<D>(kk),
+                              kIdescS, kk > 0);
+          mma_commit_elect(bar_s);
+        }
+        ok = slot_full(2 * j + 1) &&
+             (j < 2 || warp_wait(bar_dq + 8 * (j & 1), ((j - 2) >> 1) & 1, wc));
         if (!ok) break;
         tc_fence_after();
-        issue_dp(j + 1);
+        {
+          const uint64_t dVk = desc_kmajor<D>(slot(2 * j + 1));
+          const uint32_t dst = tmem + ((j & 1) ? C::kDP1 : C::kDP0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss_elect(dst, dOk + kslice_kmajor<D>(kk), dVk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
+          mma_commit_elect(bar_dp + 8 * (j & 1));
+          mma_commit_elect(bar_empty + 8 * ((2 * j + 1) % C::kSlotsB));  // V_j read
+        }
       }
-      ok = warp_wait(bar_ready + 8 * (j & 1), (j >> 1) & 1, wc);  // dS of step j written back
-      if (!ok) break;
-      tc_fence_after();
-      const uint64_t dKmn = desc_mnmajor<D>(smem_u32(sRing + (j % C::kStages) * C::kStageBytesB));
-      const uint32_t src = tmem + ((j & 1) ? C::kDP1 : C::kDP0);
+    } else {
+      for (int j = 0; ok && j < n; ++j) {
+        ok = warp_wait(bar_ready + 8 * (j & 1), (j >> 1) & 1, wc);  // dS(j) written back
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t dKmn = desc_mnmajor<D>(slot(2 * j));
+        const uint32_t src = tmem + ((j & 1) ? C::kDP1 : C::kDP0);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j (K = 128 keys)
-        mma_bf16_ts_elect(tmem + C::kDQ, src + a_col(kk), dKmn + kslice_mnmajor(kk), kIdescDQ,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_elect(bar_dq + 8 * (j & 1));
-      mma_commit_elect(bar_empty + 8 * (j % C::kStages));
+        for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j (K = 128 keys)
+          mma_bf16_ts_elect(tmem + C::kDQ, src + a_col(kk), dKmn + kslice_mnmajor(kk), kIdescDQ,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_elect(bar_dq + 8 * (j & 1));
+        // K_j: S(j) (the other warp) completed before dS(j) could exist
+        mma_commit_elect(bar_empty + 8 * ((2 * j) % C::kSlotsB));
+      }
     }
     mma_commit_elect(bar_drain);
-    if (issued) wait_own(bar_drain, 0, p.timeout_ns);
+    if (n > 0) wait_own(bar_drain, 0, p.timeout_ns);
     __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------ compute warpgroups
