@@ -65,6 +65,12 @@ def _declare(lib):
     lib.oracle_attention_bwd.argtypes = [_dp, _i64, _dp, _dp, _i64, _i64, ctypes.c_double, _i64,
                                          _i64, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
     lib.oracle_attention_bwd.restype = ctypes.c_int
+    lib.oracle_e4m3.argtypes = [ctypes.c_double]
+    lib.oracle_e4m3.restype = ctypes.c_double
+    lib.oracle_attention_fp8.argtypes = [_dp, _i64, _dp, _dp, _i64, _i64, ctypes.c_double,
+                                         ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                         ctypes.c_int, _i64, _ip, _i64, _dp, _dp]
+    lib.oracle_attention_fp8.restype = ctypes.c_int
 
 
 def _f64(a) -> np.ndarray:
@@ -189,6 +195,39 @@ def merge(m, l, o, lib=None):
     if rc != 0:
         raise ValueError("oracle_merge: bad argument")
     return mo.value, lo.value, oo, lse.value
+
+
+def e4m3(x, lib=None):
+    """Nearest FP8 E4M3 value (ties to even, saturating at 448), elementwise."""
+    lib = lib or load()
+    x = np.asarray(x, dtype=np.float64)
+    return np.vectorize(lambda t: lib.oracle_e4m3(float(t)), otypes=[np.float64])(x)
+
+
+def attention_fp8(q8, k8, v8, scale: float, q_descale: float = 1.0, k_descale: float = 1.0,
+                  v_descale: float = 1.0, causal: bool = False, block: int = 128,
+                  rows: Sequence[int] | None = None, lib=None):
+    """One head of the FP8 forward with Max_offset = 8 (E4M3 values in q8, k8,
+    v8 as any float array).  Returns (o [len(rows), d], lse [len(rows)])."""
+    lib = lib or load()
+    q, k, v = _f64(q8), _f64(k8), _f64(v8)
+    nq, d = q.shape
+    nk = k.shape[0]
+    assert k.shape == (nk, d) and v.shape == (nk, d)
+    if rows is None:
+        rows_arr, nrows = None, nq
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.shape[0]
+    o = np.empty((nrows, d))
+    lse = np.empty(nrows)
+    rc = lib.oracle_attention_fp8(_ptr(q), nq, _ptr(k), _ptr(v), nk, d, float(scale), float(q_descale),
+                                  float(k_descale), float(v_descale), int(bool(causal)), int(block),
+                                  None if rows_arr is None else _ptr(rows_arr, _ip), nrows, _ptr(o),
+                                  _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_attention_fp8: bad argument")
+    return o, lse
 
 
 def attention_bwd(q, k, v, dout, scale: float, causal: bool = False, window=None,

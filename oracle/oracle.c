@@ -29,6 +29,8 @@
  *   oracle_softmax_rows   the same over the rows of a matrix.
  *   oracle_attention_bwd  gradients dQ, dK, dV of the attention forward
  *                         ("Online Softmax 算法详解" section 8.3).
+ *   oracle_attention_fp8  the FP8 (E4M3) forward with Max_offset = 8
+ *                         ("Online Softmax 算法详解" section 6); oracle_e4m3.
  *
  *   oracle_attention_window
  *                         the same with a local (sliding-window) mask.
@@ -376,6 +378,137 @@ int oracle_softmax_two_pass(const double *x, int64_t n, double *p, double *lse_o
     for (int64_t i = 0; i < n; ++i)
         p[i] = (l == 0.0) ? 0.0 : exp(x[i] - ref) / l;
     *lse_out = (l == 0.0) ? -INFINITY : m + log(l);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 (E4M3) forward with Max_offset = 8                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Round a non-negative value to the nearest FP8 E4M3 value (ties to even),
+ * saturating at the largest finite value 448: 1 sign bit, 4 exponent bits
+ * (bias 7), 3 mantissa bits; normals (1 + f/8) 2^e for e in [-6, 8],
+ * subnormals f 2^-9 for f in 1..7.  Negative inputs round their magnitude.
+ */
+double oracle_e4m3(double x)
+{
+    if (x != x)
+        return x;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return x < 0 ? -448.0 : 448.0;
+    double spacing;
+    if (a < ldexp(1.0, -6)) {
+        spacing = ldexp(1.0, -9); /* subnormal grid */
+    } else {
+        int e;
+        frexp(a, &e); /* a = f 2^e, f in [0.5, 1): exponent of the leading bit is e - 1 */
+        spacing = ldexp(1.0, (e - 1) - 3);
+    }
+    double r = nearbyint(a / spacing) * spacing; /* default rounding mode: ties to even */
+    if (r > 448.0)
+        r = 448.0;
+    return x < 0 ? -r : r;
+}
+
+/*
+ * One head, FP8 inputs: q, k, v hold E4M3 values (exact in fp64) whose real
+ * values are q * q_descale, k * k_descale, v * v_descale.  The online steps of
+ * "Online Softmax 算法详解" section 6 over key blocks of `block` keys, in order:
+ *   s_j   = scale * q_descale * k_descale * <q_i, k_j>        (-inf where masked)
+ *   m'    = max(m, max_j s_j);   alpha = exp(m - m')  (0 while m = -inf)
+ *   P'_j  = 2^((s_j - m') log2(e) + 8)                          (Max_offset = 8: P' in [0, 256])
+ *   l    <- alpha l + sum_j P'_j          (the sum of the unquantised P')
+ *   acc  <- alpha acc + sum_j E4M3(P'_j) v_j                    (P cast to FP8 for the P.V product)
+ * then sum_scale: l <- l / 2^8, LSE = m + ln l, O = acc * (v_descale / 2^8) / l
+ * (the final_scale that undoes the 2^8 in P); a row with l = 0 gets O = 0,
+ * LSE = -inf.  s is in natural-log units of the scaled logits, as in
+ * oracle_attention.  Causal: bottom-right aligned, as elsewhere.
+ */
+static void attention_fp8_row(const double *qi, const double *k, const double *v, int64_t nk,
+                              int64_t d, double scale_qk, double v_descale, int64_t last_visible,
+                              int64_t block, double *s, double *acc, double *oi, double *lse_i)
+{
+    const double log2e = 1.4426950408889634;
+    for (int64_t j = 0; j < nk; ++j) {
+        if (j > last_visible) {
+            s[j] = -INFINITY;
+            continue;
+        }
+        double t = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            t += k[j * d + c] * qi[c];
+        s[j] = scale_qk * t;
+    }
+    double m = -INFINITY, l = 0.0;
+    for (int64_t c = 0; c < d; ++c)
+        acc[c] = 0.0;
+    for (int64_t j0 = 0; j0 < nk; j0 += block) {
+        int64_t j1 = j0 + block < nk ? j0 + block : nk;
+        double m_new = m;
+        for (int64_t j = j0; j < j1; ++j)
+            if (s[j] > m_new)
+                m_new = s[j];
+        if (m_new == -INFINITY)
+            continue; /* nothing visible yet */
+        double alpha = (m == -INFINITY) ? 0.0 : exp(m - m_new);
+        l *= alpha;
+        for (int64_t c = 0; c < d; ++c)
+            acc[c] *= alpha;
+        for (int64_t j = j0; j < j1; ++j) {
+            if (s[j] == -INFINITY)
+                continue;
+            double pp = exp2((s[j] - m_new) * log2e + 8.0);
+            l += pp;
+            double p8 = oracle_e4m3(pp);
+            for (int64_t c = 0; c < d; ++c)
+                acc[c] += p8 * v[j * d + c];
+        }
+        m = m_new;
+    }
+    l *= 1.0 / 256.0; /* sum_scale */
+    if (l == 0.0) {
+        for (int64_t c = 0; c < d; ++c)
+            oi[c] = 0.0;
+        *lse_i = -INFINITY;
+        return;
+    }
+    const double final_scale = v_descale / 256.0;
+    for (int64_t c = 0; c < d; ++c)
+        oi[c] = acc[c] * final_scale / l;
+    *lse_i = log(l) + m;
+}
+
+int oracle_attention_fp8(const double *q, int64_t nq, const double *k, const double *v,
+                         int64_t nk, int64_t d, double scale, double q_descale, double k_descale,
+                         double v_descale, int causal, int64_t block, const int64_t *rows,
+                         int64_t nrows, double *o, double *lse)
+{
+    if (!q || !k || !v || !o || !lse || nq < 0 || nk < 0 || d <= 0 || nrows < 0 || block < 1)
+        return -1;
+    if (!rows && nrows != nq)
+        return -1;
+    double *s = (double *)malloc((size_t)(nk > 0 ? nk : 1) * sizeof(double));
+    double *acc = (double *)malloc((size_t)d * sizeof(double));
+    if (!s || !acc) {
+        free(s);
+        free(acc);
+        return -1;
+    }
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= nq) {
+            free(s);
+            free(acc);
+            return -1;
+        }
+        int64_t last = causal ? i + (nk - nq) : nk - 1;
+        attention_fp8_row(q + i * d, k, v, nk, d, scale * q_descale * k_descale, v_descale, last,
+                          block, s, acc, o + r * d, lse + r);
+    }
+    free(s);
+    free(acc);
     return 0;
 }
 

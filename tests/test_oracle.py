@@ -229,6 +229,79 @@ def test_softmax_rows_selection():
     np.testing.assert_allclose(p_sub, sps.softmax(x[sel], axis=1), rtol=1e-12)
 
 
+# ------------------------------------------------------------- FP8 forward
+
+def _torch_e4m3(x):
+    """torch's float8_e4m3fn cast of x given as float32 values (torch casts
+    through float32, so only float32 inputs are rounded exactly once)."""
+    import torch
+    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
+    return torch.tensor(x32).to(torch.float8_e4m3fn).double().numpy()
+
+
+def test_e4m3_rounding_matches_torch():
+    """oracle_e4m3 against torch's float8_e4m3fn cast on [0, 448]: random
+    values, every representable value, every midpoint (ties to even) and the
+    subnormal range."""
+    rng = np.random.default_rng(31)
+    grid = np.unique(_torch_e4m3(np.linspace(0, 448, 20000)))
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+    x = np.concatenate([rng.uniform(0, 448, 5000), rng.uniform(0, 0.02, 2000), grid, mids,
+                        np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1000))])
+    x = x.astype(np.float32).astype(np.float64)  # float32-representable inputs
+    np.testing.assert_array_equal(oracle.e4m3(x), _torch_e4m3(x))
+    np.testing.assert_array_equal(oracle.e4m3(-x), -_torch_e4m3(x))
+
+
+def _e4m3_values(rng, shape, scale):
+    return _torch_e4m3(rng.standard_normal(shape) * scale)
+
+
+def test_fp8_single_block_closed_form():
+    """With one key block the running max is the row max: P' = 256 exp(s - m)
+    exactly, O = sum_j E4M3(P'_j) v_j v_descale / sum_j P'_j, LSE = logsumexp(s)
+    (torch's E4M3 cast and scipy's logsumexp)."""
+    rng = np.random.default_rng(32)
+    nq, nk, d = 6, 50, 8
+    q, k, v = (_e4m3_values(rng, (n, d), 2.0) for n in (nq, nk, nk))
+    scale, qd, kd, vd = 0.3, 0.5, 1.25, 0.75
+    o, lse = oracle.attention_fp8(q, k, v, scale, qd, kd, vd, block=64)
+    s_ = scale * qd * kd * (q @ k.T)
+    pp = 256.0 * np.exp(s_ - s_.max(axis=1, keepdims=True))
+    o_ref = (_torch_e4m3(pp) @ v) * vd / pp.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse, sps.logsumexp(s_, axis=1), rtol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_exact_when_every_p_is_representable(causal):
+    """Integer logits with scale = ln 2 make every P' = 2^(s - m + 8) a power of
+    two inside the E4M3 range and every alpha a power of two: the FP8 steps then
+    lose nothing, and O, LSE equal the fp64 attention oracle (several blocks)."""
+    rng = np.random.default_rng(33)
+    nq, nk, d = 40, 70, 4
+    q = rng.integers(-1, 2, size=(nq, d)).astype(np.float64)
+    k = rng.integers(-1, 2, size=(nk, d)).astype(np.float64)
+    v = _e4m3_values(rng, (nk, d), 1.0)
+    o8, l8 = oracle.attention_fp8(q, k, v, math.log(2.0), causal=causal, block=16)
+    o, lse = oracle.attention(q, k, v, math.log(2.0), causal)
+    np.testing.assert_allclose(o8, o, rtol=1e-13, atol=1e-15)
+    fin = np.isfinite(lse)
+    np.testing.assert_array_equal(np.isfinite(l8), fin)
+    np.testing.assert_allclose(l8[fin], lse[fin], rtol=1e-13)
+
+
+def test_fp8_descales_are_scalings():
+    """Doubling the E4M3 values of Q while halving q_descale (and the same for
+    V) changes nothing."""
+    rng = np.random.default_rng(34)
+    q, k, v = (_e4m3_values(rng, (n, 8), 1.0) for n in (20, 300, 300))
+    a = oracle.attention_fp8(q, k, v, 0.35, 1.0, 1.0, 1.0, block=128)
+    b = oracle.attention_fp8(2 * q, k, 2 * v, 0.35, 0.5, 1.0, 0.5, block=128)
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(a[1], b[1], rtol=1e-14)
+
+
 # ------------------------------------------------------------- backward
 
 def _loss_grads_fd(q, k, v, g, scale, window, h=1e-6):

@@ -55,6 +55,14 @@ MUTANTS = [
     ("two_pass_no_rescale", "l = exp(m - ref) * l + exp(x[i] - ref);", "l = l + exp(x[i] - ref);"),
     ("softmax_rows_selection_ignored", "oracle_softmax_two_pass(job->x + i * job->cols,",
      "oracle_softmax_two_pass(job->x + r * job->cols,"),
+    ("fp8_k_feature_index", "t += k[j * d + c] * qi[c];", "t += k[j * d + (d - 1 - c)] * qi[c];"),
+    ("fp8_lse_no_max", "*lse_i = log(l) + m;", "*lse_i = log(l);"),
+    ("fp8_no_sum_scale", "    l *= 1.0 / 256.0; /* sum_scale */", "    /* l not rescaled */"),
+    ("fp8_no_final_scale", "const double final_scale = v_descale / 256.0;", "const double final_scale = v_descale;"),
+    ("fp8_no_quantisation", "double p8 = oracle_e4m3(pp);", "double p8 = pp;"),
+    ("fp8_acc_not_rescaled", "        acc[c] *= alpha;\n", "        acc[c] *= 1.0;\n"),
+    ("fp8_no_max_offset", "double pp = exp2((s[j] - m_new) * log2e + 8.0);", "double pp = exp2((s[j] - m_new) * log2e);"),
+    ("e4m3_ties_away", "double r = nearbyint(a / spacing) * spacing;", "double r = round(a / spacing) * spacing;"),
     ("bwd_dq_no_scale", "dqi[c] += J->scale * ds * J->k[j * d + c];", "dqi[c] += ds * J->k[j * d + c];"),
     ("bwd_dk_wrong_operand", "dkj[c] += J->scale * ds * J->q[i * d + c];",
      "dkj[c] += J->scale * ds * J->k[j * d + c];"),
@@ -82,6 +90,7 @@ def _pin_calls():
         "test_merge_of_random_partition_matches_full": [(0,)],
         "test_window_matches_scipy_softmax": [(10, 10, 2, 0, 0), (6, 14, 4, 1, 2), (14, 6, 0, 2, 3)],
         "test_bwd_matches_finite_differences": [(3, 4, 2, (-1, -1), 0), (4, 6, 2, (1, 1), 3)],
+        "test_fp8_exact_when_every_p_is_representable": [(False,), (True,)],
     }
     calls = []
     for name, fn in inspect.getmembers(pins, inspect.isfunction):
