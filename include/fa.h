@@ -120,6 +120,23 @@ int fa_bwd_local(const void* q, const void* k, const void* v, const void* o, con
                  const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
                  int d, float scale, int window_left, int window_right, void* stream);
 
+/*
+ * FP8 (E4M3) attention forward with Max_offset = 8 ("Online Softmax 算法详解"
+ * section 6).  q, k, v hold E4M3 bytes (bf16 layout, one byte per element);
+ * their real values are q * q_descale, k * k_descale, v * v_descale.  The
+ * online recurrence runs as in fa_fwd on S = scale q_descale k_descale Q K^T,
+ * except that P' = 2^((S - m) log2(e) + 8) in [0, 256] is cast to E4M3 (round
+ * to nearest even, saturating) for the P.V product; the row sum accumulates the
+ * fp32 P' and is scaled by 2^-8 at the end (sum_scale), O by
+ * final_scale = v_descale 2^-8.
+ * o   : out, bf16 [B][H][Nq][d];  lse : out, fp32 [B][H][Nq] (natural log)
+ * d must be 128 (FA_ERR_UNSUPPORTED otherwise); descales finite and > 0;
+ * causal as in fa_fwd; no split-KV.  Arguments otherwise as fa_fwd.
+ */
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Nq, int Nk, int d, float scale, float q_descale, float k_descale,
+               float v_descale, int causal, void* stream);
+
 /* Options for fa_fwd_ex.  Zero-initialise, then set what you need. */
 typedef struct fa_opts {
   int bc;                     /* K/V tile rows: 0 = default (128), or 64 or 128 */

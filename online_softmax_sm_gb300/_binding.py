@@ -70,6 +70,8 @@ def _declare(L):
     L.fa_fwd_local.restype = _i
     L.fa_softmax_rows.argtypes = [_vp, _vp, _vp, ctypes.c_longlong, _i, _i, _vp]
     L.fa_softmax_rows.restype = _i
+    L.fa_fwd_fp8.argtypes = [_vp] * 5 + [_i] * 5 + [ctypes.c_float] * 4 + [_i, _vp]
+    L.fa_fwd_fp8.restype = _i
     L.fa_bwd.argtypes = [_vp] * 9 + [_i] * 5 + [ctypes.c_float, _i, _vp]
     L.fa_bwd.restype = _i
     L.fa_bwd_local.argtypes = [_vp] * 9 + [_i] * 5 + [ctypes.c_float, _i, _i, _vp]
@@ -168,6 +170,30 @@ def fwd_local(q, k, v, window_left: int, window_right: int, scale: float | None 
                                 lse.data_ptr(), B, H, Nq, Nk, d, float(scale), int(window_left),
                                 int(window_right), int(n_splits), _stream_handle(q.device, stream))
     _check(rc, "fa_fwd_local")
+    return out, lse
+
+
+def fwd_fp8(q8, k8, v8, scale: float | None = None, q_descale: float = 1.0, k_descale: float = 1.0,
+            v_descale: float = 1.0, causal: bool = False, out=None, lse=None, stream=None):
+    """fa_fwd_fp8: q8, k8, v8 float8_e4m3fn [B, H, N, 128].  Returns (o bf16, lse fp32)."""
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cuda" or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if t.dtype != torch.float8_e4m3fn:
+            raise ValueError(f"{name} must be float8_e4m3fn")
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    if k8.shape != (B, H, Nk, d) or v8.shape != k8.shape:
+        raise ValueError("k8 and v8 must be [B, H, Nk, d] matching q8")
+    if scale is None:
+        scale = d ** -0.5
+    out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device) if lse is None else lse
+    with torch.cuda.device(q8.device):
+        rc = lib().fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                              B, H, Nq, Nk, d, float(scale), float(q_descale), float(k_descale),
+                              float(v_descale), int(bool(causal)), _stream_handle(q8.device, stream))
+    _check(rc, "fa_fwd_fp8")
     return out, lse
 
 

@@ -88,18 +88,23 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // 3-D bf16 map over [batch][rows][inner] with a (64 x box_rows x 1) box and
 // the 128-byte swizzle; out-of-range rows read as zero / are clipped on store.
-int make_map(CUtensorMap* m, const void* base, int inner, int rows, int batch, int box_rows) {
+int make_map(CUtensorMap* m, const void* base, int inner, int rows, int batch, int box_rows,
+             bool bytes = false) {
+  // bf16 elements (box 64 wide) or one-byte FP8 elements (box 128 wide): one
+  // 128-byte swizzle row either way
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cuda_fail(cudaErrorNotSupported);
+  const cuuint64_t es = bytes ? 1 : 2;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(batch)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2,
-                                 static_cast<cuuint64_t>(inner) * 2 * static_cast<cuuint64_t>(rows)};
-  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * es,
+                                 static_cast<cuuint64_t>(inner) * es * static_cast<cuuint64_t>(rows)};
+  const cuuint32_t box[3] = {bytes ? 128u : 64u, static_cast<cuuint32_t>(box_rows), 1u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
   return FA_OK;
 }
@@ -302,6 +307,50 @@ int fa_merge_splits(const float* m_part, const float* l_part, const float* o_par
   mp.rows = static_cast<long long>(B) * H * Nq;
   mp.n_splits = n_splits;
   cudaError_t e = fa::launch_merge(d, mp, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Nq, int Nk, int d, float scale, float q_descale, float k_descale,
+               float v_descale, int causal, void* stream) {
+  int rc = check_sizes(B, H, Nq, Nk, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  for (float x : {q_descale, k_descale, v_descale})
+    if (!std::isfinite(x) || !(x > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_INVALID_ARG;
+  DevState* dev = nullptr;
+  if ((rc = device_state(&dev)) != FA_OK) return rc;
+  const int BH = B * H;
+  const int qt = Nq > 128 ? 2 : 1;
+  fa::FwdParams p{};
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.BH = BH;
+  p.n_splits = 1;
+  p.partial = 0;
+  p.kv_tiles = (Nk + 127) / 128;
+  p.tiles_per_split = p.kv_tiles;
+  p.wl = -1;
+  p.wr = causal ? 0 : -1;
+  p.causal = causal ? 1 : 0;
+  const double s_qk = static_cast<double>(scale) * q_descale * k_descale;
+  p.scale = static_cast<float>(s_qk);
+  p.scale_log2 = static_cast<float>(s_qk * 1.4426950408889634);
+  p.o_scale = v_descale / 256.f;  // final_scale
+  p.timeout_ns = kDefaultTimeoutNs;
+  p.test_skip_load = -1;
+  p.status = dev->status;
+  p.lse = lse;
+  CUtensorMap maps[4];
+  if ((rc = make_map(&maps[0], q, d, Nq, BH, 128, true)) != FA_OK) return rc;
+  if ((rc = make_map(&maps[1], k, d, Nk, BH, 128, true)) != FA_OK) return rc;
+  if ((rc = make_map(&maps[2], v, d, Nk, BH, 128, true)) != FA_OK) return rc;
+  if ((rc = make_map(&maps[3], o, d, Nq, BH, 128)) != FA_OK) return rc;
+  const dim3 grid((Nq + 128 * qt - 1) / (128 * qt), 1, static_cast<unsigned>(BH));
+  cudaError_t e = fa::launch_fwd_fp8_d128(qt, maps, p, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 

@@ -57,9 +57,16 @@
 
 namespace fa {
 
-template <int D, int BC, int QT>
+// F8: Q, K, V and P are FP8 E4M3 (one byte per element) and the products use
+// tcgen05.mma kind::f8f6f4; everything else -- roles, ring, recurrence -- is
+// shared with the bf16 kernel.
+template <int D, int BC, int QT, bool F8 = false>
 struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(!F8 || (D == 128 && BC == 128), "FP8: d = 128, 128-key tiles");
+  static constexpr int kEs = F8 ? 1 : 2;           // bytes per Q / K / V / P element
+  static constexpr int kChunkElems = 128 / kEs;    // elements per 128-byte swizzle row
+  static constexpr int kKStep = 32 / kEs;          // elements per MMA K-step (32 bytes)
   static_assert(BC == 64 || BC == 128, "K/V tile");
   static_assert(QT == 1 || QT == 2, "Q tiles per CTA");
   static constexpr int kBr = 128;  // query rows per tile (= TMEM lanes)
@@ -78,10 +85,10 @@ struct FwdCfg {
   static_assert(QT * kRegSoftmax + kRegCorr + kRegOther == (QT + 2) * kRegLaunch,
                 "setmaxnreg split must add up to the registers the block launches with");
   static_assert(kRegLaunch * kThreads <= 65536, "launch register budget");
-  static constexpr int kChunks = D / 64;          // 64-column (128-byte) swizzle chunks
+  static constexpr int kChunks = D / kChunkElems;  // 128-byte swizzle chunks per row
   static constexpr int kQChunkBytes = kBr * 128;  // 128 rows x 128 B
   static constexpr int kQTileBytes = kChunks * kQChunkBytes;
-  static constexpr int kPTileBytes = (BC / 64) * kQChunkBytes;  // 128 rows x BC keys, bf16
+  static constexpr int kPTileBytes = (BC / kChunkElems) * kQChunkBytes;  // 128 rows x BC keys
   static constexpr int kKVChunkBytes = BC * 128;
   static constexpr int kKVTileBytes = kChunks * kKVChunkBytes;
   static constexpr int kSCol = 0;
@@ -138,12 +145,12 @@ __device__ __forceinline__ void ring_decode(int p, int n, bool& is_v, int& step)
   }
 }
 
-template <int D, int BC, int QT>
-__global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
+template <int D, int BC, int QT, bool F8 = false>
+__global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const FwdParams p) {
-  using C = FwdCfg<D, BC, QT>;
+  using C = FwdCfg<D, BC, QT, F8>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment of the shared-space address (128-byte swizzle atoms).
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -260,7 +267,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem_u32(sQ + i * C::kQTileBytes + c * C::kQChunkBytes), &tm_q, bar_q,
-                        c * 64, row0 + C::kBr * i, bh);
+                        c * C::kChunkElems, row0 + C::kBr * i, bh);
         }
       }
       uint32_t issued_mask = 0, issued_par = 0;
@@ -291,7 +298,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem_u32(sKV + stage * C::kKVTileBytes + c * C::kKVChunkBytes), map, full,
-                      c * 64, (cta_b + step) * BC, bh);
+                      c * C::kChunkElems, (cta_b + step) * BC, bh);
         issued_mask |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (static_cast<uint32_t>(use & 1) << stage);
       }
@@ -304,8 +311,15 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
     } else if (warp >= C::kMmaWarp0 && warp < C::kMmaWarp0 + QT) {
       // ====================================================== MMA issuer, tile i
       const int i = warp - C::kMmaWarp0;
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BC, false);  // K-major A (Q), B (K)
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);    // A = P K-major, B = V MN-major
+      // K-major A (Q), B (K); PV: A = P K-major, B = V MN-major
+      constexpr uint32_t kIdescQK = F8 ? idesc_e4m3_f32(128, BC, false) : idesc_bf16_f32(128, BC, false);
+      constexpr uint32_t kIdescPV = F8 ? idesc_e4m3_f32(128, D, true) : idesc_bf16_f32(128, D, true);
+      auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+        if constexpr (F8)
+          mma_e4m3_ss_elect(d, a, b, idesc, acc);
+        else
+          mma_bf16_ss_elect(d, a, b, idesc, acc);
+      };
       // Descriptor templates; the start-address field (bits 0-13, address >> 4)
       // of a shared address below 256 KB never carries, so per-MMA offsets are
       // plain 32-bit adds to the low word.
@@ -327,10 +341,10 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
         const int stage = ring_pos_k(q) % C::kStages;
         const uint32_t k_lo = lo_k + ((stage * C::kKVTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / C::kKStep; ++kk) {  // 32 bytes of K per step
           const uint32_t off_q = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
           const uint32_t off_k = ((kk / 4) * C::kKVChunkBytes + (kk % 4) * 32) >> 4;
-          mma_bf16_ss_elect(tS, hi_q | (lo_q + off_q), hi_k | (k_lo + off_k), kIdescQK, kk > 0);
+          mma(tS, hi_q | (lo_q + off_q), hi_k | (k_lo + off_k), kIdescQK, kk > 0);
         }
         mma_commit_elect(bar_s + 8 * i);
         mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
@@ -339,12 +353,13 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
         const int stage = ring_pos_v(v, n_cta) % C::kStages;
         const uint32_t v_lo = lo_v + ((stage * C::kKVTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BC / 16; ++kk) {
-          // P: 16 keys of the K-major tile.  V: 16 keys = two 8-row groups
-          // (SBO 1024 B); D columns in 64-wide chunks BC*128 B apart (LBO).
+        for (int kk = 0; kk < BC / C::kKStep; ++kk) {
+          // P: one K-step (32 bytes) of the K-major tile.  V: kKStep keys =
+          // 8-row groups of 1024 B (SBO); D columns in 128-byte chunks BC*128 B
+          // apart (LBO).
           const uint32_t off_p = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
-          mma_bf16_ss_elect(tO, hi_p | (lo_p + off_p), hi_v | (v_lo + ((kk * 2048) >> 4)), kIdescPV,
-                            (v > 0 || kk > 0) ? 1u : 0u);
+          mma(tO, hi_p | (lo_p + off_p), hi_v | (v_lo + ((kk * C::kKStep * 128) >> 4)), kIdescPV,
+              (v > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit_elect(bar_o + 8 * i);
         mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
@@ -552,21 +567,34 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
       mbar_arrive(bar_alpha + 8 * i);
 
       // P = 2^(s*c - m_ref*c) (packed FFMA, then EX2); rowsum of the fp32 P
-      // (before the bf16 cast) in four packed partial sums.
+      // (before the cast to bf16 / E4M3) in four packed partial sums.  FP8:
+      // Max_offset = 8 ("Online Softmax 算法详解" section 6): P' = 2^8 P, in
+      // [0, 256], to use the E4M3 range; the sum of P' is scaled back by 2^-8
+      // at the end and O by final_scale.
       const uint64_t c2 = f2_pack(c, c);
-      const uint64_t neg2 = f2_pack(-m_ref * c, -m_ref * c);
+      const float neg = -m_ref * c + (F8 ? 8.f : 0.f);
+      const uint64_t neg2 = f2_pack(neg, neg);
       uint64_t ls[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) ls[u] = 0ull;
-      uint32_t pk[BC / 2];
+      uint32_t pk[BC / (4 / C::kEs)];  // bf16 pairs or E4M3 quads
 #pragma unroll
-      for (int cc = 0; cc < BC; cc += 2) {
-        float x0, x1;
+      for (int cc = 0; cc < BC; cc += 4) {
+        float x0, x1, x2, x3;
         f2_unpack(ffma2(f2_pack(s[cc], s[cc + 1]), c2, neg2), x0, x1);
+        f2_unpack(ffma2(f2_pack(s[cc + 2], s[cc + 3]), c2, neg2), x2, x3);
         const float p0 = ex2_approx(x0);
         const float p1 = ex2_approx(x1);
+        const float p2 = ex2_approx(x2);
+        const float p3 = ex2_approx(x3);
         ls[(cc >> 1) & 3] = fadd2(ls[(cc >> 1) & 3], f2_pack(p0, p1));
-        pk[cc >> 1] = pack_bf16x2(p0, p1);
+        ls[((cc >> 1) + 1) & 3] = fadd2(ls[((cc >> 1) + 1) & 3], f2_pack(p2, p3));
+        if constexpr (F8) {
+          pk[cc >> 2] = pack_e4m3x4(p0, p1, p2, p3);
+        } else {
+          pk[cc >> 1] = pack_bf16x2(p0, p1);
+          pk[(cc >> 1) + 1] = pack_bf16x2(p2, p3);
+        }
       }
       float lsum[4];
       f2_unpack(fadd2(ls[0], ls[1]), lsum[0], lsum[1]);
@@ -581,7 +609,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
       {
         const uint32_t sp = smem_u32(sP + i * C::kPTileBytes) + t * 128;
 #pragma unroll
-        for (int u = 0; u < BC / 8; ++u)  // 16-byte unit u holds keys 8u..8u+7
+        for (int u = 0; u < BC * C::kEs / 16; ++u)  // 16-byte unit u: 16 / kEs keys
           st_shared_v4(sp + (u >> 3) * C::kQChunkBytes + (((u & 7) ^ (t & 7)) << 4), pk[4 * u],
                        pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       }
@@ -597,13 +625,22 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
     if (!bad && row0 + C::kBr * i < p.Nq) {
       if (n > 0) tc_fence_after();
       const bool empty = !(l > 0.f);
-      const float inv = empty ? 0.f : 1.f / l;
+      // FP8: sum_scale l <- l 2^-8 undoes Max_offset in the row sum, and
+      // final_scale (p.o_scale = v_descale 2^-8) in O ("Online Softmax 算法详解"
+      // section 6.3); both are powers of two or exact scalings.
+      const float lc = F8 ? l * (1.f / 256.f) : l;
+      const float inv = empty ? 0.f : (F8 ? p.o_scale : 1.f) / lc;
       if (!p.partial) {
         // bf16 O, staged in this tile's (now unused) Q buffer with the 128-byte
-        // swizzle, then one TMA store (rows past Nq are clipped by the map).
+        // swizzle, then TMA stores (rows past Nq are clipped by the map).  The
+        // FP8 Q buffer holds one 64-column chunk of bf16 O at a time.
         const uint32_t stg = smem_u32(sQ + i * C::kQTileBytes);
+        constexpr int kOChunks = D / 64;
+        constexpr int kStageChunks = F8 ? 1 : kOChunks;  // O chunks staged per round
 #pragma unroll
-        for (int cc = 0; cc < D; cc += 32) {
+        for (int round = 0; round < kOChunks / kStageChunks; ++round) {
+#pragma unroll
+        for (int cc = round * 64 * kStageChunks; cc < (round + 1) * 64 * kStageChunks; cc += 32) {
           uint32_t o[32];
           if (n > 0) {
             tmem_ld32_sync(tO + cc, o);
@@ -615,7 +652,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 16; ++k)
             w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
-          const int chunk = cc / 64;
+          const int chunk = cc / 64 - round * kStageChunks;
           const int u0 = (cc % 64) / 8;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -628,13 +665,16 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
         named_bar_sync(1 + i, 128);
         if (t == 0) {
 #pragma unroll
-          for (int ch = 0; ch < C::kChunks; ++ch)
-            tma_store_3d(&tm_o, stg + ch * C::kQChunkBytes, ch * 64, row0 + C::kBr * i, bh);
+          for (int ch = 0; ch < kStageChunks; ++ch)
+            tma_store_3d(&tm_o, stg + ch * C::kQChunkBytes, (round * kStageChunks + ch) * 64,
+                         row0 + C::kBr * i, bh);
           tma_store_commit();
           tma_store_wait_read();
         }
+        if (kStageChunks < kOChunks) named_bar_sync(1 + i, 128);  // staging buffer free again
+        }
         if (row < p.Nq)
-          p.lse[static_cast<size_t>(bh) * p.Nq + row] = empty ? -INFINITY : m * p.scale + logf(l);
+          p.lse[static_cast<size_t>(bh) * p.Nq + row] = empty ? -INFINITY : m * p.scale + logf(lc);
       } else {
         // fp32 partial triple (m in natural-log units, l, O/l) for the merge.
         const size_t prow = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + row;
@@ -673,10 +713,10 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT>::kThreads, 1)
   }
 }
 
-template <int D, int BC, int QT>
+template <int D, int BC, int QT, bool F8 = false>
 cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, dim3 grid, cudaStream_t s) {
-  using C = FwdCfg<D, BC, QT>;
-  auto kern = fa_fwd_kernel<D, BC, QT>;
+  using C = FwdCfg<D, BC, QT, F8>;
+  auto kern = fa_fwd_kernel<D, BC, QT, F8>;
   // The setmaxnreg split assumes the block launches with exactly kRegLaunch
   // registers per thread; with fewer, setmaxnreg.inc could never be granted.
   static const bool regs_ok = [&] {

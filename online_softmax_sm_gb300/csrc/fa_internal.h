@@ -32,6 +32,7 @@ struct FwdParams {
   int wl, wr;        // visible keys [r + off - wl, r + off + wr]; -1 = open side
   float scale;       // natural-units logit scale
   float scale_log2;  // scale * log2(e)
+  float o_scale;     // FP8 forward: final_scale = v_descale 2^-8 applied to O
   unsigned long long timeout_ns;
   int test_skip_load;  // >= 0: the producer skips this K/V load (test hook)
   int* status;         // device status word
@@ -57,6 +58,8 @@ cudaError_t launch_fwd_d128_bc64(int qt, const CUtensorMap* maps, const FwdParam
                                  cudaStream_t s);
 cudaError_t launch_fwd_d128_bc128(int qt, const CUtensorMap* maps, const FwdParams& p, dim3 grid,
                                   cudaStream_t s);
+cudaError_t launch_fwd_fp8_d128(int qt, const CUtensorMap* maps, const FwdParams& p, dim3 grid,
+                                cudaStream_t s);
 cudaError_t launch_merge(int d, const MergeParams& p, cudaStream_t s);
 
 // Attention backward (fa_bwd_kernel.cuh).

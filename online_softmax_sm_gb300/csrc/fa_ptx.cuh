@@ -225,6 +225,19 @@ __device__ __forceinline__ void mma_bf16_ts_elect(uint32_t d_tmem, uint32_t a_tm
       : "memory");
 }
 
+// FP8 (E4M3 x E4M3 -> fp32), kind::f8f6f4: D[tmem] (+)= A[smem] * B[smem],
+// K = 32 elements (32 bytes) per instruction.
+__device__ __forceinline__ void mma_e4m3_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pe, pa;\n\t"
+      "elect.sync _|pe, 0xffffffff;\n\t"
+      "setp.ne.b32 pa, %4, 0;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, pa;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred pe;\n\t"
@@ -334,6 +347,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4: D fp32, A and B E4M3 (format code 0
+// in bits 7-9 and 10-12), dense; other fields as idesc_bf16_f32.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // ------------------------------------------------------------------ scalar
 
 // Three-input max (sm_100+): one instruction for two new elements.
@@ -440,6 +460,18 @@ __device__ __forceinline__ void st_async_f32x4(uint32_t caddr, float a, float b,
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
+}
+
+// Four fp32 -> four E4M3 bytes (round to nearest even, saturating), byte k = v_k.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float v0, float v1, float v2, float v3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
