@@ -38,6 +38,7 @@ from online_softmax_sm_gb300 import workloads  # noqa: E402
 
 METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and % of dense BF16 tensor peak"
 SOFTMAX_METRIC = "row softmax throughput (two-pass online normaliser), algorithmic GB/s"
+FP8_METRIC = "attention fwd TFLOPS (FP8 E4M3 inputs and P, 1×GB300) and % of dense FP8 tensor peak"
 BWD_METRIC = "attention bwd TFLOPS (bf16, 1×GB300; 2.5x the forward's FLOPs) and % of dense BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 WORKLOAD_ALIASES = {"c1": workloads.C1, "c2": workloads.C2, "c3": workloads.C3, "c4": workloads.C4,
@@ -686,6 +687,107 @@ def run_softmax(args, sw):
         dist.destroy_process_group()
 
 
+def run_fp8(args, w):
+    """The FP8 forward (fa_fwd_fp8) on the workload's shape: Q, K, V drawn as
+    for the bf16 workload and cast to E4M3 (descales 1).  Peak: the measured
+    bf16 peak x 2, the nominal FP8 / bf16 ratio of the tensor cores."""
+    import online_softmax_sm_gb300 as fa
+
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "metric": FP8_METRIC,
+                              "unavailable": "the FP8 reference arm is not timed; the oracle's FP8 "
+                                             "steps are the parity reference in the tests"}), flush=True)
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    fa.lib()
+    q, k, v = (t.to(torch.float8_e4m3fn) for t in workloads.generate(w, device=dev))
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step(qq=q, kk=k, vv=v):
+        fa.fwd_fp8(qq, kk, vv, w.scale, 1.0, 1.0, 1.0, w.causal, out=o, lse=lse)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.device_status(dev) != fa.FA_OK:
+        raise SystemExit("device status reports a timed-out wait")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_region0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_region1 = time.time()
+    barrier(world)
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_local = statistics.mean(step_ms)
+    ms, value = aggregate(world, w.flops, ms_local, dev)
+    peaks, peak_src = load_peaks()
+    peak = 2.0 * float(peaks["bf16_tflops"])
+    achieved = w.flops / (ms_local * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(w.name + ":fp8"),
+                "kernel": "fa_fwd_kernel<128,128,2,F8>", "kernel_ms": ms_local,
+                "algorithmic_flops_per_launch": w.flops,
+                "peak_source": peak_src + " bf16_tflops x 2 (nominal FP8 / bf16 dense ratio)"}
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        tt = []
+        for it in range(2 + max(5, min(args.steps, 20))):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            step(dq, dk, dv)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+            b.record(stream)
+            if it >= 2:
+                tt.append((a, b))
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in tt), world, dev)
+        e2e = {"value": world * w.flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv)),
+               "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
+               "ms_per_step": e_ms}
+    if rank == 0:
+        line = {"metric": FP8_METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+                "data": "synthetic",
+                "config": {"workload": w.name + ":fp8", "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk,
+                           "d": w.d, "causal": w.causal, "descales": [1.0, 1.0, 1.0],
+                           "l2": "flushed before every timed step (512 MB write); inputs > L2",
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
+                "gpu_launches": args.steps, "clocks": sampler.summary(t_region0, t_region1),
+                "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def run_bwd(args, w):
     """The attention backward: one fa_bwd call per step (row pass + dK/dV
     kernel + dQ kernel), O, LSE and dO resident.  Algorithmic FLOPs: the five
@@ -775,6 +877,9 @@ def main():
     args = parse()
     if args.workload.endswith(":bwd"):
         run_bwd(args, workload_of(args.workload[: -len(":bwd")]))
+        return
+    if args.workload.endswith(":fp8"):
+        run_fp8(args, workload_of(args.workload[: -len(":fp8")]))
         return
     sw = softmax_workload_of(args.workload)
     if sw is not None:
