@@ -23,27 +23,32 @@
 // tile, so the query tiles' ranges are prefixes of one stream.
 //   WG i < QT     tile i.  Thread t owns row t of the tile (TMEM lane t), so
 //                 row max and row sum are register-local (no shuffles).  Each
-//                 step: read S_i, publish alpha per row, write P_i (bf16) to
-//                 shared memory.  Also runs the epilogue of its tile.
+//                 step: read S_i, publish alpha per row, write P_i (bf16 pairs
+//                 or E4M3 quads) to TMEM.  Also runs the epilogue of its tile.
 //   WG QT         correction: O_i <- alpha O_i in TMEM once P_i(j-1).V_{j-1}
-//                 has landed, skipped for a warp whose 32 rows all kept their
-//                 max.  Runs beside the softmax, off its critical path.
+//                 has landed; a warp whose 32 rows all keep their reference
+//                 releases the step at once.  Runs beside the softmax.
 //   last WG       warp 0: TMA producer (one thread): Q once, then K and V
 //                 tiles through a ring of shared-memory stages, K one step
 //                 ahead of V (see ring_pos_k / ring_pos_v).
 //                 Warp 1 + i: MMA issuer of tile i (warp-uniform code, one
 //                 elected lane issues, blocking barrier waits):
-//                 S_i(j+1) = Q_i K_{j+1}^T as soon as every row of tile i has
-//                 read S_i(j) (so it overlaps that step's exponentials), then
-//                 O_i += P_i(j) V_j once P_i(j) and the O rescale are in place.
-//                 The two tiles' issuers run side by side and keep the tensor
-//                 queue fed.  Warp 3 allocates TMEM.
+//                 S_i(j+1) = Q_i K_{j+1}^T into the S buffer as soon as the
+//                 other tile has read its S (so it overlaps this tile's
+//                 exponentials), then O_i += P_i(j) V_j (A = P_i from TMEM)
+//                 once P_i(j) and the O rescale are in place.  Warp 3
+//                 allocates TMEM.
 // setmaxnreg moves registers from the producer and correction warpgroups to
 // the softmax warpgroups.
-// TMEM (fp32 columns): S_i at [i*BC, (i+1)*BC), O_i at [QT*BC + i*D, ..+D).
-// Shared memory: Q_i, P_i (both [128 rows][BC or D] bf16, 128-byte swizzle, the
-// layout the MMA reads K-major), then the K/V ring.  P_i(j+1) is written only
-// after O_i += P_i(j) V_j has completed.
+// TMEM (32-bit columns): one S buffer of BC columns that the tiles take in
+// turn (S_0(0), S_1(0), S_0(1), ...), P_i (BC/2 or BC/4 columns), O_i (D
+// columns each).  P_i(j+1) is written only after O_i += P_i(j) V_j has
+// completed.  Shared memory: the Q tiles ([128 rows][D], 128-byte swizzle, the
+// layout the MMA reads K-major), then the K/V ring: keeping P out of shared
+// memory leaves room for five 32 KB stages at d = 128.
+// Softmax reference: bf16 rows move their reference m only when the tile max
+// exceeds it by more than 8 in base-2 exponent units (P <= 2^8), so O is
+// rarely rescaled; the final O / l and LSE do not depend on the reference.
 //
 // Every mbarrier wait is bounded by a global-timer limit.  A wait that runs
 // out sets the CTA's abort flag and the device status word; every role then
@@ -88,12 +93,18 @@ struct FwdCfg {
   static constexpr int kChunks = D / kChunkElems;  // 128-byte swizzle chunks per row
   static constexpr int kQChunkBytes = kBr * 128;  // 128 rows x 128 B
   static constexpr int kQTileBytes = kChunks * kQChunkBytes;
-  static constexpr int kPTileBytes = (BC / kChunkElems) * kQChunkBytes;  // 128 rows x BC keys
+  static constexpr int kPCols = BC * kEs / 4;  // TMEM columns of P_i (packed pairs / quads)
+  // Growth of the row max (base-2 exponent units) absorbed without moving the
+  // softmax reference: bf16 P up to 2^8; E4M3 P' already spans its range.
+  static constexpr float kLazy = F8 ? 0.f : 8.f;
   static constexpr int kKVChunkBytes = BC * 128;
   static constexpr int kKVTileBytes = kChunks * kKVChunkBytes;
+  // TMEM (32-bit columns): one S buffer that the tiles take in turn, P_i, then
+  // O_i (starting on a multiple of D).
   static constexpr int kSCol = 0;
-  static constexpr int kOCol = QT * BC;
-  static constexpr int kTmemNeed = QT * (BC + D);
+  static constexpr int kPCol = BC;
+  static constexpr int kOCol = (BC + QT * kPCols + D - 1) / D * D;
+  static constexpr int kTmemNeed = kOCol + QT * D;
   static constexpr int kTmemCols = kTmemNeed <= 64    ? 64
                                    : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256
@@ -101,11 +112,11 @@ struct FwdCfg {
   static constexpr int kCtlBytes = 2048;
   static constexpr int kSmemLimit = 227 * 1024;
   static constexpr int kStagesFit =
-      (kSmemLimit - 1024 - kCtlBytes - QT * (kQTileBytes + kPTileBytes)) / kKVTileBytes;
+      (kSmemLimit - 1024 - kCtlBytes - QT * kQTileBytes) / kKVTileBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static_assert(kStages >= 2, "shared memory");
   static constexpr int kSmemBytes =
-      1024 + QT * (kQTileBytes + kPTileBytes) + kStages * kKVTileBytes + kCtlBytes;
+      1024 + QT * kQTileBytes + kStages * kKVTileBytes + kCtlBytes;
 };
 
 struct __align__(8) Ctl {
@@ -113,7 +124,7 @@ struct __align__(8) Ctl {
   uint64_t kv_full[8];
   uint64_t kv_empty[8][2];  // [stage][tile]: that tile's MMAs reading the stage completed
   uint64_t s_full[2];       // S_i(j) in TMEM (MMA commit)
-  uint64_t s_free[2];       // all 128 rows of S_i(j) read into registers
+  uint64_t s_free[2];       // all 128 rows of S_i(j) read into registers (128 arrivals)
   uint64_t alpha_full[2];   // alpha_i(j) published (128 softmax arrivals)
   uint64_t alpha_free[2];   // alpha_i(j) read by the correction (128 arrivals)
   uint64_t pv_ready[2];     // P_i(j) in shared memory and O_i rescaled (128 + 128 arrivals)
@@ -126,10 +137,8 @@ struct __align__(8) Ctl {
 static_assert(sizeof(Ctl) <= 2048, "control block");
 
 // Order of the K/V tiles through the shared-memory ring for a CTA with n steps:
-// K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}.  K runs one step
-// ahead of V, so K_{j+1} reuses the slot of V_{j-2} and V_j the slot of K_j:
-// both are free long before they are needed, and S_i(j+1) can start while
-// step j's softmax is still running.
+// K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}: K runs one step
+// ahead of V, as S_i(j+1) is computed while step j's softmax still runs.
 __device__ __forceinline__ int ring_pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int ring_pos_v(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
 // Inverse: position p -> (is_v, step).
@@ -156,8 +165,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint8_t* sQ = smem;
-  uint8_t* sP = sQ + QT * C::kQTileBytes;
-  uint8_t* sKV = sP + QT * C::kPTileBytes;
+  uint8_t* sKV = sQ + QT * C::kQTileBytes;
   Ctl* ctl = reinterpret_cast<Ctl*>(sKV + C::kStages * C::kKVTileBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -320,22 +328,48 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
         else
           mma_bf16_ss_elect(d, a, b, idesc, acc);
       };
+      auto mma_ts = [&](uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+        if constexpr (F8)
+          mma_e4m3_ts_elect(d, a_tmem, b, idesc, acc);
+        else
+          mma_bf16_ts_elect(d, a_tmem, b, idesc, acc);
+      };
       // Descriptor templates; the start-address field (bits 0-13, address >> 4)
       // of a shared address below 256 KB never carries, so per-MMA offsets are
       // plain 32-bit adds to the low word.
       const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ + i * C::kQTileBytes), 16, 1024);
-      const uint64_t dp0 = smem_desc_sw128(smem_u32(sP + i * C::kPTileBytes), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sKV), 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(sKV), C::kKVChunkBytes, 1024);
-      const uint64_t hi_q = dq0 & 0xFFFFFFFF00000000ull, hi_p = dp0 & 0xFFFFFFFF00000000ull,
-                     hi_k = dk0 & 0xFFFFFFFF00000000ull, hi_v = dv0 & 0xFFFFFFFF00000000ull;
-      const uint32_t lo_q = static_cast<uint32_t>(dq0), lo_p = static_cast<uint32_t>(dp0),
-                     lo_k = static_cast<uint32_t>(dk0), lo_v = static_cast<uint32_t>(dv0);
-      const uint32_t tS = tmem + C::kSCol + i * BC, tO = tmem + C::kOCol + i * D;
+      const uint64_t hi_q = dq0 & 0xFFFFFFFF00000000ull, hi_k = dk0 & 0xFFFFFFFF00000000ull,
+                     hi_v = dv0 & 0xFFFFFFFF00000000ull;
+      const uint32_t lo_q = static_cast<uint32_t>(dq0), lo_k = static_cast<uint32_t>(dk0),
+                     lo_v = static_cast<uint32_t>(dv0);
+      const uint32_t tS = tmem + C::kSCol, tP = tmem + C::kPCol + i * C::kPCols,
+                     tO = tmem + C::kOCol + i * D;
       const int n = n_i[i];
       const int n_cta = kv_end_cta - cta_b;
       auto kv_ready = [&](int pos) {
         return warp_wait(bar_kv_full + 8 * (pos % C::kStages), (pos / C::kStages) & 1, wc);
+      };
+      // The S buffer is taken in the order S_0(0), S_1(0), S_0(1), S_1(1), ...
+      // (a tile past its last step drops out); each use waits until the
+      // previous one has been read into registers.  Previous use before
+      // S_i(q): bar / parity of its s_free, false if none.
+      auto prev_use = [&](int q, uint32_t& bar, uint32_t& par) {
+        if constexpr (QT == 2) {
+          const int o = 1 - i, qo = i == 1 ? q : q - 1;
+          if (qo >= 0 && qo < n_i[o]) {
+            bar = bar_sfree + 8 * o, par = qo & 1;
+            return true;
+          }
+        }
+        if (q == 0) return false;
+        bar = bar_sfree + 8 * i, par = (q - 1) & 1;
+        return true;
+      };
+      auto s_ready = [&](int q) {  // S_i(q) may be written: the buffer's previous product was read
+        uint32_t bar, par;
+        return !prev_use(q, bar, par) || warp_wait(bar, par, wc);
       };
       auto issue_qk = [&](int q) {  // S_i(q) = Q_i K_q^T, then release K_q's slot for tile i
         const int stage = ring_pos_k(q) % C::kStages;
@@ -354,19 +388,20 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
         const uint32_t v_lo = lo_v + ((stage * C::kKVTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < BC / C::kKStep; ++kk) {
-          // P: one K-step (32 bytes) of the K-major tile.  V: kKStep keys =
-          // 8-row groups of 1024 B (SBO); D columns in 128-byte chunks BC*128 B
-          // apart (LBO).
-          const uint32_t off_p = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
-          mma(tO, hi_p | (lo_p + off_p), hi_v | (v_lo + ((kk * C::kKStep * 128) >> 4)), kIdescPV,
-              (v > 0 || kk > 0) ? 1u : 0u);
+          // P: one K-step (32 bytes = 8 TMEM columns of packed P).  V: kKStep
+          // keys = 8-row groups of 1024 B (SBO); D columns in 128-byte chunks
+          // BC*128 B apart (LBO).
+          mma_ts(tO, tP + 8 * kk, hi_v | (v_lo + ((kk * C::kKStep * 128) >> 4)), kIdescPV,
+                 (v > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit_elect(bar_o + 8 * i);
         mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
       };
+      // S_i(j+1) first: it waits only for the other tile to read its S, which
+      // comes before P_i(j) is ready.
       bool ok = n > 0;
       bool issued = false;
-      if (ok) ok = warp_wait(bar_q, 0, wc) && kv_ready(ring_pos_k(0));
+      if (ok) ok = warp_wait(bar_q, 0, wc) && s_ready(0) && kv_ready(ring_pos_k(0));
       if (ok) {
         tc_fence_after();
         issue_qk(0);
@@ -374,13 +409,12 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       }
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n) {
-          // S_i(j+1) once every row read S_i(j)
-          ok = warp_wait(bar_sfree + 8 * i, j & 1, wc) && kv_ready(ring_pos_k(j + 1));
+          ok = s_ready(j + 1) && kv_ready(ring_pos_k(j + 1));
           if (!ok) break;
           tc_fence_after();
           issue_qk(j + 1);
         }
-        // O_i += P_i(j) V_j once P_i(j) is in shared memory and O_i rescaled
+        // O_i += P_i(j) V_j once P_i(j) is in TMEM and O_i rescaled
         ok = warp_wait(bar_pv + 8 * i, j & 1, wc) && kv_ready(ring_pos_v(j, n_cta));
         if (!ok) break;
         tc_fence_after();
@@ -434,13 +468,15 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
           have[i] = true;
           progressed = true;
         }
-        if (j > 0) {
+        // A warp whose 32 rows all keep their reference (alpha = 1) has
+        // nothing to rescale and releases the product at once.
+        const float alpha = alpha_r[i];
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           if (!probe(bar_o + 8 * i, (j - 1) & 1)) {
             if (sleep_i < 0) sleep_i = i;
             continue;
           }
-          const float alpha = alpha_r[i];
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          {
             tc_fence_after();
             const uint32_t tO = tmem + lane_off + C::kOCol + i * D;
             const uint64_t a2 = f2_pack(alpha, alpha);
@@ -497,7 +533,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
     setmaxnreg_inc<C::kRegSoftmax>();
     const int i = wg;
     const int t = threadIdx.x & 127;
-    const uint32_t tS = tmem + lane_off + C::kSCol + i * BC;
+    const uint32_t tS = tmem + lane_off + C::kSCol;
+    const uint32_t tP = tmem + lane_off + C::kPCol + i * C::kPCols;
     const uint32_t tO = tmem + lane_off + C::kOCol + i * D;
     const int row = row0 + C::kBr * i + t;
     const int n = n_i[i];
@@ -523,6 +560,10 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
     bool ok = true;
     float m = -INFINITY;
     float l = 0.f;
+    // bf16: sum over the tiles of bf16(P) - P at each tile's max element,
+    // rescaled like l.  O is normalised by l + l_fix, so the largest weights
+    // of a row enter O and its normaliser with the same rounding; LSE uses l.
+    float l_fix = 0.f;
     for (int jj = 0; ok && jj < n; ++jj) {
       const int j = cta_b + jj;
       if (!warp_wait(bar_s + 8 * i, jj & 1, wc)) {
@@ -535,7 +576,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
 #pragma unroll
       for (int h = 0; h < BC / 64; ++h) tmem_ld64_sync(tS + h * 64, r + h * 64);
       tc_fence_before();
-      mbar_arrive(bar_sfree + 8 * i);  // S_i(j) may be overwritten by S_i(j+1)
+      mbar_arrive(bar_sfree + 8 * i);  // the S buffer may take the next product
       float s[BC];
 #pragma unroll
       for (int cc = 0; cc < BC; ++cc) s[cc] = __uint_as_float(r[cc]);
@@ -554,9 +595,15 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       for (int u = 0; u < 4; ++u) mx[u] = fmaxf(s[2 * u], s[2 * u + 1]);
 #pragma unroll
       for (int cc = 8; cc < BC; cc += 2) mx[(cc >> 1) & 3] = max3f(mx[(cc >> 1) & 3], s[cc], s[cc + 1]);
-      const float m_new = max3f(m, fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      // The reference m moves to the tile's max only when that lies more
+      // than C::kLazy (base-2 exponent units) above it, so P stays within
+      // [0, 2^kLazy] and most steps leave O alone (alpha = 1).  The final
+      // O / l and LSE = m scale + ln l are the same for any reference.
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const bool bump = mt > m && (m == -INFINITY || (mt - m) * c > C::kLazy);
+      const float m_new = bump ? mt : m;
       const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = (m_new == m) ? 1.f : ex2_approx((m - m_ref) * c);
+      const float alpha = bump ? ex2_approx((m - m_ref) * c) : 1.f;
       // The correction must have read alpha_i(j-1) before the slot is reused
       // (S_i(j) was issued before it ran, so this step can be ahead of it).
       if (jj > 0 && !warp_wait(bar_afree + 8 * i, (jj - 1) & 1, wc)) {
@@ -574,6 +621,13 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       const uint64_t c2 = f2_pack(c, c);
       const float neg = -m_ref * c + (F8 ? 8.f : 0.f);
       const uint64_t neg2 = f2_pack(neg, neg);
+      float dfix = 0.f;
+      if constexpr (!F8) {
+        // P at the tile's max element, as the loop below computes it, and its
+        // bf16 rounding (0 for a fully masked tile: 2^-inf).
+        const float pm = ex2_approx(fmaf(mt, c, neg));
+        dfix = __uint_as_float(pack_bf16x2(0.f, pm) & 0xFFFF0000u) - pm;
+      }
       uint64_t ls[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) ls[u] = 0ull;
@@ -600,23 +654,19 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       f2_unpack(fadd2(ls[0], ls[1]), lsum[0], lsum[1]);
       f2_unpack(fadd2(ls[2], ls[3]), lsum[2], lsum[3]);
       const float rowsum = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
-      // P_i(j) -> shared memory (128-byte swizzle, row t), once O_i += P_i(j-1) V
-      // has finished reading the buffer.
+      // P_i(j) -> TMEM, row t in lane t (the A operand of O_i += P_i(j) V_j),
+      // once O_i += P_i(j-1) V_{j-1} has finished reading the columns.
       if (jj > 0 && !warp_wait(bar_o + 8 * i, (jj - 1) & 1, wc)) {
         ok = false;
         break;
       }
-      {
-        const uint32_t sp = smem_u32(sP + i * C::kPTileBytes) + t * 128;
 #pragma unroll
-        for (int u = 0; u < BC * C::kEs / 16; ++u)  // 16-byte unit u: 16 / kEs keys
-          st_shared_v4(sp + (u >> 3) * C::kQChunkBytes + (((u & 7) ^ (t & 7)) << 4), pk[4 * u],
-                       pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      }
-      fence_proxy_async_smem();
+      for (int u = 0; u < C::kPCols; u += 32) tmem_st32(tP + u, pk + u);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_pv + 8 * i);
       l = alpha * l + rowsum;
+      l_fix = alpha * l_fix + dfix;
       m = m_new;
     }
     if (ok && n > 0) ok = warp_wait(bar_o + 8 * i, (n - 1) & 1, wc);
@@ -629,7 +679,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       // final_scale (p.o_scale = v_descale 2^-8) in O ("Online Softmax 算法详解"
       // section 6.3); both are powers of two or exact scalings.
       const float lc = F8 ? l * (1.f / 256.f) : l;
-      const float inv = empty ? 0.f : (F8 ? p.o_scale : 1.f) / lc;
+      const float inv = empty ? 0.f : (F8 ? p.o_scale / lc : 1.f / (l + l_fix));
       if (!p.partial) {
         // bf16 O, staged in this tile's (now unused) Q buffer with the 128-byte
         // swizzle, then TMA stores (rows past Nq are clipped by the map).  The

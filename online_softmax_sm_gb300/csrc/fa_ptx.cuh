@@ -238,6 +238,19 @@ __device__ __forceinline__ void mma_e4m3_ss_elect(uint32_t d_tmem, uint64_t a_de
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc], E4M3: A holds four elements per 32-bit
+// column, so a 32-element K-step is 8 columns.
+__device__ __forceinline__ void mma_e4m3_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pe, pa;\n\t"
+      "elect.sync _|pe, 0xffffffff;\n\t"
+      "setp.ne.b32 pa, %4, 0;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, pa;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred pe;\n\t"
