@@ -40,9 +40,9 @@
 //                 allocates TMEM.
 // setmaxnreg moves registers from the producer and correction warpgroups to
 // the softmax warpgroups.
-// TMEM (32-bit columns): one S buffer of BC columns that the tiles take in
-// turn (S_0(0), S_1(0), S_0(1), ...), P_i (BC/2 or BC/4 columns), O_i (D
-// columns each).  P_i(j+1) is written only after O_i += P_i(j) V_j has
+// TMEM (32-bit columns): S_i (BC columns per tile where 512 columns hold
+// everything, else one S buffer that the tiles take in turn: S_0(0), S_1(0),
+// S_0(1), ...), P_i (BC/2 or BC/4 columns), O_i (D columns each).  P_i(j+1) is written only after O_i += P_i(j) V_j has
 // completed.  Shared memory: the Q tiles ([128 rows][D], 128-byte swizzle, the
 // layout the MMA reads K-major), then the K/V ring: keeping P out of shared
 // memory leaves room for five 32 KB stages at d = 128.
@@ -100,11 +100,14 @@ struct FwdCfg {
   static constexpr float kLazy = F8 ? 0.f : 16.f;
   static constexpr int kKVChunkBytes = BC * 128;
   static constexpr int kKVTileBytes = kChunks * kKVChunkBytes;
-  // TMEM (32-bit columns): one S buffer that the tiles take in turn, P_i, then
-  // O_i (starting on a multiple of D).
+  // TMEM (32-bit columns): S, P_i, then O_i (starting on a multiple of D).
+  // Each tile has its own S buffer where that fits in 512 columns; otherwise
+  // one S buffer that the tiles take in turn.
+  static constexpr bool kSharedS = QT * (BC + kPCols + D) > 512;
+  static constexpr int kSBufs = kSharedS ? 1 : QT;
   static constexpr int kSCol = 0;
-  static constexpr int kPCol = BC;
-  static constexpr int kOCol = (BC + QT * kPCols + D - 1) / D * D;
+  static constexpr int kPCol = kSBufs * BC;
+  static constexpr int kOCol = (kPCol + QT * kPCols + D - 1) / D * D;
   static constexpr int kTmemNeed = kOCol + QT * D;
   static constexpr int kTmemCols = kTmemNeed <= 64    ? 64
                                    : kTmemNeed <= 128 ? 128
@@ -345,19 +348,21 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
                      hi_v = dv0 & 0xFFFFFFFF00000000ull;
       const uint32_t lo_q = static_cast<uint32_t>(dq0), lo_k = static_cast<uint32_t>(dk0),
                      lo_v = static_cast<uint32_t>(dv0);
-      const uint32_t tS = tmem + C::kSCol, tP = tmem + C::kPCol + i * C::kPCols,
+      const uint32_t tS = tmem + C::kSCol + (C::kSharedS ? 0 : i * BC),
+                     tP = tmem + C::kPCol + i * C::kPCols,
                      tO = tmem + C::kOCol + i * D;
       const int n = n_i[i];
       const int n_cta = kv_end_cta - cta_b;
       auto kv_ready = [&](int pos) {
         return warp_wait(bar_kv_full + 8 * (pos % C::kStages), (pos / C::kStages) & 1, wc);
       };
-      // The S buffer is taken in the order S_0(0), S_1(0), S_0(1), S_1(1), ...
-      // (a tile past its last step drops out); each use waits until the
-      // previous one has been read into registers.  Previous use before
-      // S_i(q): bar / parity of its s_free, false if none.
+      // A shared S buffer is taken in the order S_0(0), S_1(0), S_0(1), ...
+      // (a tile past its last step drops out); a tile's own buffer holds
+      // S_i(0), S_i(1), ...  Each use waits until the previous one has been
+      // read into registers.  Previous use before S_i(q): bar / parity of its
+      // s_free, false if none.
       auto prev_use = [&](int q, uint32_t& bar, uint32_t& par) {
-        if constexpr (QT == 2) {
+        if constexpr (QT == 2 && C::kSharedS) {
           const int o = 1 - i, qo = i == 1 ? q : q - 1;
           if (qo >= 0 && qo < n_i[o]) {
             bar = bar_sfree + 8 * o, par = qo & 1;
@@ -453,7 +458,6 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
     bool ok = true;
     while (ok) {
       bool done = true, progressed = false;
-      int sleep_i = -1;
 #pragma unroll
       for (int i = 0; i < QT; ++i) {
         const int j = jn[i];
@@ -461,7 +465,6 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
         done = false;
         if (!have[i]) {
           if (!probe(bar_alpha + 8 * i, j & 1)) {
-            if (sleep_i < 0) sleep_i = i;
             continue;
           }
           alpha_r[i] = ctl->alpha[i][t];
@@ -474,7 +477,6 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
         const float alpha = alpha_r[i];
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           if (!probe(bar_o + 8 * i, (j - 1) & 1)) {
-            if (sleep_i < 0) sleep_i = i;
             continue;
           }
           {
@@ -508,14 +510,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
         idle = 0;
         continue;
       }
-      // Nothing ready: sleep briefly on the first pending input.
-      {
-        const int i = sleep_i;
-        if (!have[i])
-          mbar_try_wait_hint(bar_alpha + 8 * i, jn[i] & 1, 100);
-        else
-          mbar_try_wait_hint(bar_o + 8 * i, (jn[i] - 1) & 1, 100);
-      }
+      // Nothing ready: poll again (a suspended wait on one tile's input
+      // reacts late to the other tile's).
       if ((idle++ & 63) == 0) {
         const uint64_t now = global_timer_ns();
         if (idle == 1) t_idle = now;
@@ -534,7 +530,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
     setmaxnreg_inc<C::kRegSoftmax>();
     const int i = wg;
     const int t = threadIdx.x & 127;
-    const uint32_t tS = tmem + lane_off + C::kSCol;
+    const uint32_t tS = tmem + lane_off + C::kSCol + (C::kSharedS ? 0 : i * BC);
     const uint32_t tP = tmem + lane_off + C::kPCol + i * C::kPCols;
     const uint32_t tO = tmem + lane_off + C::kOCol + i * D;
     const int row = row0 + C::kBr * i + t;
