@@ -25,9 +25,11 @@
 //                 row max and row sum are register-local (no shuffles).  Each
 //                 step: read S_i, publish alpha per row, write P_i (bf16 pairs
 //                 or E4M3 quads) to TMEM.  Also runs the epilogue of its tile.
-//   WG QT         correction: O_i <- alpha O_i in TMEM once P_i(j-1).V_{j-1}
-//                 has landed; a warp whose 32 rows all keep their reference
-//                 releases the step at once.  Runs beside the softmax.
+//   WG QT         E4M3 only -- correction: O_i <- alpha O_i in TMEM once
+//                 P_i(j-1).V_{j-1} has landed; a warp whose 32 rows all keep
+//                 their max releases the step at once.  Runs beside the
+//                 softmax.  bf16 rows seldom move their reference, and their
+//                 softmax warp rescales its own rows of O when one does.
 //   last WG       warp 0: TMA producer (one thread): Q once, then K and V
 //                 tiles through a ring of shared-memory stages, K one step
 //                 ahead of V (see ring_pos_k / ring_pos_v).
@@ -38,7 +40,7 @@
 //                 exponentials), then O_i += P_i(j) V_j (A = P_i from TMEM)
 //                 once P_i(j) and the O rescale are in place.  Warp 3
 //                 allocates TMEM.
-// setmaxnreg moves registers from the producer and correction warpgroups to
+// setmaxnreg moves registers from the producer (and correction) warpgroups to
 // the softmax warpgroups.
 // TMEM (32-bit columns): S_i (BC columns per tile where 512 columns hold
 // everything, else one S buffer that the tiles take in turn: S_0(0), S_1(0),
@@ -75,19 +77,26 @@ struct FwdCfg {
   static_assert(BC == 64 || BC == 128, "K/V tile");
   static_assert(QT == 1 || QT == 2, "Q tiles per CTA");
   static constexpr int kBr = 128;  // query rows per tile (= TMEM lanes)
-  static constexpr int kCorrWG = QT;             // correction warpgroup
-  static constexpr int kLoadWarp = 4 * (QT + 1);  // first warp of the last WG
+  // A separate correction warpgroup rescales O for E4M3, whose rows move
+  // their max (and so rescale) on most steps.  bf16 rows rarely rescale (see
+  // kLazy); their softmax warpgroup does it itself.
+  static constexpr bool kCorr = F8;
+  static constexpr int kWGs = QT + (kCorr ? 2 : 1);
+  static constexpr int kCorrWG = kCorr ? QT : -1;    // correction warpgroup
+  static constexpr int kLoadWarp = 4 * (kWGs - 1);  // first warp of the last WG
   static constexpr int kMmaWarp0 = kLoadWarp + 1;  // + i: issuer of tile i
   static constexpr int kAllocWarp = kLoadWarp + 3;
-  static constexpr int kThreads = 4 * (QT + 2) * 32;
+  static constexpr int kThreads = 128 * kWGs;
   // Registers per thread at launch (65536 / threads, multiple of 8) and the
   // setmaxnreg split that moves them to the softmax warpgroups.  The split must
   // add up to what the block launches with, or setmaxnreg.inc would wait forever.
-  static constexpr int kRegLaunch = QT == 2 ? 128 : 168;
-  static constexpr int kRegSoftmax = QT == 2 ? 192 : 216;
-  static constexpr int kRegCorr = QT == 2 ? 64 : 160;
-  static constexpr int kRegOther = QT == 2 ? 64 : 128;
-  static_assert(QT * kRegSoftmax + kRegCorr + kRegOther == (QT + 2) * kRegLaunch,
+  // 256 threads launch with the per-thread maximum and need no split.
+  static constexpr bool kSplitRegs = kThreads > 256;
+  static constexpr int kRegLaunch = kCorr ? (QT == 2 ? 128 : 168) : (QT == 2 ? 168 : 0);
+  static constexpr int kRegSoftmax = kCorr ? (QT == 2 ? 192 : 216) : (QT == 2 ? 216 : 0);
+  static constexpr int kRegCorr = kCorr ? (QT == 2 ? 64 : 160) : 0;
+  static constexpr int kRegOther = kCorr ? (QT == 2 ? 64 : 128) : (QT == 2 ? 72 : 0);
+  static_assert(!kSplitRegs || QT * kRegSoftmax + kRegCorr + kRegOther == kWGs * kRegLaunch,
                 "setmaxnreg split must add up to the registers the block launches with");
   static_assert(kRegLaunch * kThreads <= 65536, "launch register budget");
   static constexpr int kChunks = D / kChunkElems;  // 128-byte swizzle chunks per row
@@ -238,7 +247,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       mbar_init(bar_sfree + 8 * i, 128);
       mbar_init(bar_alpha + 8 * i, 128);
       mbar_init(bar_afree + 8 * i, 128);
-      mbar_init(bar_pv + 8 * i, 256);
+      mbar_init(bar_pv + 8 * i, C::kCorr ? 256 : 128);
       mbar_init(bar_o + 8 * i, 1);
       mbar_init(bar_drain + 8 * i, 1);
     }
@@ -262,8 +271,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
   const int wg = warp >> 2;
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
 
-  if (wg == QT + 1) {
-    setmaxnreg_dec<C::kRegOther>();
+  if (wg == C::kWGs - 1) {
+    if constexpr (C::kSplitRegs) setmaxnreg_dec<C::kRegOther>();
     if (warp == C::kLoadWarp) {
       if (lane == 0) {
       // ============================================================== producer
@@ -433,13 +442,13 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       }
       __syncwarp();
     }
-  } else if (wg == C::kCorrWG) {
+  } else if (C::kCorr && wg == C::kCorrWG) {
     // ========================================================= correction
     // Serves the tiles in whatever order their inputs arrive: per tile,
     // (1) read alpha_i(j) as soon as it is published and release the slot,
     // (2) once O_i += P_i(j-1) V_{j-1} has completed, O_i <- alpha O_i, then
     // let the MMA warp issue O_i += P_i(j) V_j.
-    if constexpr (C::kRegCorr < C::kRegLaunch) setmaxnreg_dec<C::kRegCorr>();
+    if constexpr (C::kSplitRegs && C::kRegCorr < C::kRegLaunch) setmaxnreg_dec<C::kRegCorr>();
     const int t = threadIdx.x & 127;
     int jn[QT];        // next step of tile i
     bool have[QT];     // alpha_i(jn) read, waiting for the previous P.V
@@ -527,7 +536,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
     }
   } else {
     // ========================================================== tile i
-    setmaxnreg_inc<C::kRegSoftmax>();
+    if constexpr (C::kSplitRegs) setmaxnreg_inc<C::kRegSoftmax>();
     const int i = wg;
     const int t = threadIdx.x & 127;
     const uint32_t tS = tmem + lane_off + C::kSCol + (C::kSharedS ? 0 : i * BC);
@@ -601,14 +610,16 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       const float m_new = bump ? mt : m;
       const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = bump ? ex2_approx((m - m_ref) * c) : 1.f;
-      // The correction must have read alpha_i(j-1) before the slot is reused
-      // (S_i(j) was issued before it ran, so this step can be ahead of it).
-      if (jj > 0 && !warp_wait(bar_afree + 8 * i, (jj - 1) & 1, wc)) {
-        ok = false;
-        break;
+      if constexpr (C::kCorr) {
+        // The correction must have read alpha_i(j-1) before the slot is reused
+        // (S_i(j) was issued before it ran, so this step can be ahead of it).
+        if (jj > 0 && !warp_wait(bar_afree + 8 * i, (jj - 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        ctl->alpha[i][t] = alpha;  // the correction warpgroup rescales O_i by it
+        mbar_arrive(bar_alpha + 8 * i);
       }
-      ctl->alpha[i][t] = alpha;  // the correction warpgroup rescales O_i by it
-      mbar_arrive(bar_alpha + 8 * i);
 
       // P = 2^(s*c - m_ref*c) (packed FFMA, then EX2); rowsum of the fp32 P
       // (before the cast to bf16 / E4M3) in four packed partial sums.  FP8:
@@ -656,6 +667,27 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       if (jj > 0 && !warp_wait(bar_o + 8 * i, (jj - 1) & 1, wc)) {
         ok = false;
         break;
+      }
+      if constexpr (!C::kCorr) {
+        // O_i <- alpha O_i for this warp's 32 rows, now that O_i += P_i(j-1)
+        // V_{j-1} has landed; rare, as the reference seldom moves.
+        if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          tc_fence_after();
+          const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t o[32];
+            tmem_ld32_sync(tO + cc, o);
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              float y0, y1;
+              f2_unpack(fmul2(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), a2), y0, y1);
+              o[k] = __float_as_uint(y0);
+              o[k + 1] = __float_as_uint(y1);
+            }
+            tmem_st32(tO + cc, o);
+          }
+        }
       }
 #pragma unroll
       for (int u = 0; u < C::kPCols; u += 32) tmem_st32(tP + u, pk + u);
@@ -768,7 +800,8 @@ cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, dim3 grid,
   // registers per thread; with fewer, setmaxnreg.inc could never be granted.
   static const bool regs_ok = [&] {
     cudaFuncAttributes attr{};
-    return cudaFuncGetAttributes(&attr, kern) == cudaSuccess && attr.numRegs == C::kRegLaunch;
+    return cudaFuncGetAttributes(&attr, kern) == cudaSuccess &&
+           (!C::kSplitRegs || attr.numRegs == C::kRegLaunch);
   }();
   if (!regs_ok) return cudaErrorInvalidKernelImage;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
