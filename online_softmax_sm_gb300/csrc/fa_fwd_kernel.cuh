@@ -21,25 +21,25 @@
 // (-1, 0)).  The CTA streams the K/V tiles from the first one any of its rows
 // can see; every query tile starts there and stops after its own last visible
 // tile, so the query tiles' ranges are prefixes of one stream.
-//   WG i < QT     tile i.  Thread t owns row t of the tile (TMEM lane t), so
-//                 row max and row sum are register-local (no shuffles).  Each
-//                 step: read S_i, publish alpha per row, write P_i (bf16 pairs
-//                 or E4M3 quads) to TMEM.  Also runs the epilogue of its tile.
-//   WG QT         E4M3 only -- correction: O_i <- alpha O_i in TMEM once
-//                 P_i(j-1).V_{j-1} has landed; a warp whose 32 rows all keep
-//                 their max releases the step at once.  Runs beside the
-//                 softmax.  bf16 rows seldom move their reference, and their
-//                 softmax warp rescales its own rows of O when one does.
-//   last WG       warp 0: TMA producer (one thread): Q once, then K and V
+//   WG 0          warp 0: TMA producer (one thread): Q once, then K and V
 //                 tiles through a ring of shared-memory stages, K one step
 //                 ahead of V (see ring_pos_k / ring_pos_v).
 //                 Warp 1 + i: MMA issuer of tile i (warp-uniform code, one
 //                 elected lane issues, blocking barrier waits):
-//                 S_i(j+1) = Q_i K_{j+1}^T into the S buffer as soon as the
-//                 other tile has read its S (so it overlaps this tile's
-//                 exponentials), then O_i += P_i(j) V_j (A = P_i from TMEM)
-//                 once P_i(j) and the O rescale are in place.  Warp 3
-//                 allocates TMEM.
+//                 S_i(j+1) = Q_i K_{j+1}^T into its S buffer as soon as that
+//                 is free (so it overlaps this tile's exponentials), then
+//                 O_i += P_i(j) V_j (A = P_i from TMEM) once P_i(j) and the O
+//                 rescale are in place.  Warp 3 allocates TMEM.
+//   WG 1 + i      tile i.  Thread t owns row t of the tile (TMEM lane t), so
+//                 row max and row sum are register-local (no shuffles).  Each
+//                 step: read S_i, write P_i (bf16 pairs or E4M3 quads) to
+//                 TMEM; bf16 rows seldom move their reference, and the warp
+//                 rescales its own rows of O when one does.  Also runs the
+//                 epilogue of its tile.
+//   WG 1 + QT     E4M3 only -- correction: rows follow the exact max and
+//                 rescale on most steps, so O_i <- alpha O_i runs here, beside
+//                 the softmax, once P_i(j-1).V_{j-1} has landed; a warp whose
+//                 32 rows all keep their max releases the step at once.
 // setmaxnreg moves registers from the producer (and correction) warpgroups to
 // the softmax warpgroups.
 // TMEM (32-bit columns): S_i (BC columns per tile where 512 columns hold
@@ -82,8 +82,10 @@ struct FwdCfg {
   // kLazy); their softmax warpgroup does it itself.
   static constexpr bool kCorr = F8;
   static constexpr int kWGs = QT + (kCorr ? 2 : 1);
-  static constexpr int kCorrWG = kCorr ? QT : -1;    // correction warpgroup
-  static constexpr int kLoadWarp = 4 * (kWGs - 1);  // first warp of the last WG
+  // Warpgroup 0 holds the producer, MMA and TMEM-allocation warps; softmax
+  // tile i is warpgroup 1 + i, the E4M3 correction warpgroup comes last.
+  static constexpr int kCorrWG = kCorr ? QT + 1 : -1;  // correction warpgroup
+  static constexpr int kLoadWarp = 0;
   static constexpr int kMmaWarp0 = kLoadWarp + 1;  // + i: issuer of tile i
   static constexpr int kAllocWarp = kLoadWarp + 3;
   static constexpr int kThreads = 128 * kWGs;
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
   const int wg = warp >> 2;
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;  // this warp's TMEM lanes
 
-  if (wg == C::kWGs - 1) {
+  if (wg == 0) {
     if constexpr (C::kSplitRegs) setmaxnreg_dec<C::kRegOther>();
     if (warp == C::kLoadWarp) {
       if (lane == 0) {
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
   } else {
     // ========================================================== tile i
     if constexpr (C::kSplitRegs) setmaxnreg_inc<C::kRegSoftmax>();
-    const int i = wg;
+    const int i = wg - 1;
     const int t = threadIdx.x & 127;
     const uint32_t tS = tmem + lane_off + C::kSCol + (C::kSharedS ? 0 : i * BC);
     const uint32_t tP = tmem + lane_off + C::kPCol + i * C::kPCols;
