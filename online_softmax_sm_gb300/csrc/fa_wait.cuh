@@ -34,29 +34,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
   return __all_sync(0xffffffffu, wait_bounded(bar, parity, w));
 }
 
-// Like wait_bounded, but polls with the non-blocking test instead of the
-// potentially suspending try_wait: it sees the phase complete within a few
-// cycles, at the cost of issue slots while it waits.
-__device__ __forceinline__ bool spin_bounded(uint32_t bar, uint32_t parity, const WaitCtx& w) {
-  if (mbar_test(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t k = 1;; ++k) {
-    if (mbar_test(bar, parity)) return true;
-    if ((k & 255u) == 0u) {
-      if (*w.abort) return false;
-      if (global_timer_ns() - t0 > w.timeout_ns) {
-        *w.abort = 1;
-        atomicExch(w.status, kDevTimeout);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ bool warp_spin(uint32_t bar, uint32_t parity, const WaitCtx& w) {
-  return __all_sync(0xffffffffu, spin_bounded(bar, parity, w));
-}
-
 // Bounded wait for this thread's own copies / MMAs in flight (ignores abort).
 __device__ __forceinline__ void wait_own(uint32_t bar, uint32_t parity,
                                          unsigned long long timeout_ns) {
