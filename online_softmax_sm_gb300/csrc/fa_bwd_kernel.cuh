@@ -18,7 +18,9 @@
 //     d = 128); compute warpgroup b owns buffer b (queries [64b, 64b + 64) of
 //     every tile): thread t owns key t (TMEM lane t) and writes P^T and dS^T
 //     (bf16 pairs) back into the columns it has just read; dV_j += P^T dO and
-//     dK_j += dS^T Q then take them as the TMEM A operand.  The MMA warp issues
+//     dK_j += dS^T Q then take them as the TMEM A operand.  P^T is released
+//     on its own, before dS^T is formed, so dV (and after it the next S^T of
+//     the buffer) overlaps the second half of the warpgroup's work.  The MMA warp issues
 //     dV, dK of half-step h, then S^T of h+2 once dV(h) is done and dP^T of h+2
 //     once dK(h) is done: each follows the previous MMA on the tensor pipe, and
 //     each warpgroup has two half-steps of MMA time for its exponentials.
@@ -92,7 +94,8 @@ struct __align__(8) BwdCtl {
   uint64_t s_full[2];   // S(^T) of this step in TMEM (dK/dV: per buffer)
   uint64_t s_free;      // dQ kernel: S read by all 256 compute threads
   uint64_t dp_full[2];  // dP(^T) in TMEM (buffer)
-  uint64_t ready[2];    // bf16 P^T / dS^T (or dS) written back to TMEM
+  uint64_t ready[2];    // bf16 P^T (dK/dV kernel) or dS (dQ kernel) written back to TMEM
+  uint64_t ds_ready[2]; // dK/dV kernel: bf16 dS^T written back to TMEM
   uint64_t done_a[2];   // dK/dV kernel: dV MMA of a buffer done (its S columns free)
   uint64_t done_b[2];   // dK MMA of a buffer done (dP columns free) / dQ MMA of a buffer done
   uint64_t drain;       // every MMA of the CTA completed
@@ -193,6 +196,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const uint32_t bar_s = smem_u32(&ctl->s_full[0]);
   const uint32_t bar_dp = smem_u32(&ctl->dp_full[0]);
   const uint32_t bar_ready = smem_u32(&ctl->ready[0]);
+  const uint32_t bar_dsr = smem_u32(&ctl->ds_ready[0]);
   const uint32_t bar_dv = smem_u32(&ctl->done_a[0]);
   const uint32_t bar_dk = smem_u32(&ctl->done_b[0]);
   const uint32_t bar_drain = smem_u32(&ctl->drain);
@@ -207,6 +211,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_init(bar_s + 8 * b, 1);
       mbar_init(bar_dp + 8 * b, 1);
       mbar_init(bar_ready + 8 * b, 128);
+      mbar_init(bar_dsr + 8 * b, 128);
       mbar_init(bar_dv + 8 * b, 1);
       mbar_init(bar_dk + 8 * b, 1);
     }
@@ -338,6 +343,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_bf16_ts_elect(tmem + C::kDV, pa + 8 * kk, dOmn + kslice_mnmajor(4 * b + kk), kIdescAcc,
                             (hs > 0 || kk > 0) ? 1u : 0u);
         mma_commit_elect(bar_dv + 8 * b);
+        ok = warp_wait(bar_dsr + 8 * b, static_cast<uint32_t>((hs >> 1) & 1), wc);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q_h
           mma_bf16_ts_elect(tmem + C::kDK, da + 8 * kk, dQmn + kslice_mnmajor(4 * b + kk), kIdescAcc,
@@ -370,54 +378,65 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const int q0 = (i_lo + s) * C::kRows + 64 * h;  // this half's first query
       const float* lse2v = reinterpret_cast<const float*>(sRing + st * C::kStageBytesA + 2 * C::kTileBytes) + 64 * h;
       const float* ddv = lse2v + C::kRows;
-      // S^T, dP^T of this half in TMEM; the stage's own barrier (complete by
-      // now) makes the bulk-copied lse2 / dd visible to these threads
-      ok = warp_wait(bar_s + 8 * h, s & 1, wc) && warp_wait(bar_dp + 8 * h, s & 1, wc) &&
-           warp_wait(bar_full + 8 * st, (s / C::kStages) & 1, wc);
+      // P^T first, from S^T alone, so dV += P^T dO (and S^T of half-step
+      // h + 2 after it) can start while dS^T is still being formed.  The
+      // stage's own barrier makes the bulk-copied lse2 / dd visible here.
+      ok = warp_wait(bar_full + 8 * st, (s / C::kStages) & 1, wc) && warp_wait(bar_s + 8 * h, s & 1, wc);
       if (!ok) break;
       tc_fence_after();
       const bool all_vis = bwd_tile_all_visible(q0, key0, p);  // (a superset test: 128 queries)
-      // the whole half-step's S^T and dP^T rows (64 + 64 columns) at once
-      uint32_t srow[64], drow[64];
-      tmem_ld64_sync(tS, srow);
-      tmem_ld64_sync(tDP, drow);
+      float pv[64];
+      {
+        uint32_t srow[64];
+        tmem_ld64_sync(tS, srow);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const uint32_t* sr = srow + 32 * cc;
-        const uint32_t* dr = drow + 32 * cc;
-        float lv[32], dv[32];
-#pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-          const float4 a4 = *reinterpret_cast<const float4*>(lse2v + 32 * cc + k);
-          const float4 d4 = *reinterpret_cast<const float4*>(ddv + 32 * cc + k);
-          lv[k] = a4.x, lv[k + 1] = a4.y, lv[k + 2] = a4.z, lv[k + 3] = a4.w;
-          dv[k] = d4.x, dv[k + 1] = d4.y, dv[k + 2] = d4.z, dv[k + 3] = d4.w;
+        for (int k = 0; k < 64; k += 4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(lse2v + k);
+          pv[k] = ex2_approx(fmaf(__uint_as_float(srow[k]), c, -a4.x));
+          pv[k + 1] = ex2_approx(fmaf(__uint_as_float(srow[k + 1]), c, -a4.y));
+          pv[k + 2] = ex2_approx(fmaf(__uint_as_float(srow[k + 2]), c, -a4.z));
+          pv[k + 3] = ex2_approx(fmaf(__uint_as_float(srow[k + 3]), c, -a4.w));
         }
-        float pv[32];
+      }
+      // edge tiles only: the mask in a block of its own, so fully visible
+      // tiles run the loop above with no per-element test
+      if (!all_vis) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pv[k] = ex2_approx(fmaf(__uint_as_float(sr[k]), c, -lv[k]));
-        // edge tiles only: the mask in a block of its own, so fully visible
-        // tiles run the loop above with no per-element test
-        if (!all_vis) {
+        for (int k = 0; k < 64; ++k)
+          if (!bwd_visible(q0 + k, key, p)) pv[k] = 0.f;
+      }
+      {
+        uint32_t pk[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (!bwd_visible(q0 + 32 * cc + k, key, p)) pv[k] = 0.f;
-        }
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float d0 = pv[k] * (__uint_as_float(dr[k]) - dv[k]);
-          const float d1 = pv[k + 1] * (__uint_as_float(dr[k + 1]) - dv[k + 1]);
-          pk[k >> 1] = pack_bf16x2(pv[k], pv[k + 1]);
-          dk[k >> 1] = pack_bf16x2(d0, d1);
-        }
-        // pairs into columns already read: chunk cc -> [16 cc, 16 cc + 16)
-        tmem_st16(tS + 16 * cc, pk);
-        tmem_st16(tDP + 16 * cc, dk);
+        for (int k = 0; k < 32; ++k) pk[k] = pack_bf16x2(pv[2 * k], pv[2 * k + 1]);
+        tmem_st32(tS, pk);  // pairs into columns already read: [0, 32)
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_ready + 8 * h);
+      // dS^T = P^T (dP^T - D) once dP^T has landed
+      if (!warp_wait(bar_dp + 8 * h, s & 1, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        uint32_t drow[64];
+        tmem_ld64_sync(tDP, drow);
+        uint32_t dk[32];
+#pragma unroll
+        for (int k = 0; k < 64; k += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(ddv + k);
+          dk[k >> 1] = pack_bf16x2(pv[k] * (__uint_as_float(drow[k]) - d4.x),
+                                   pv[k + 1] * (__uint_as_float(drow[k + 1]) - d4.y));
+          dk[(k >> 1) + 1] = pack_bf16x2(pv[k + 2] * (__uint_as_float(drow[k + 2]) - d4.z),
+                                         pv[k + 3] * (__uint_as_float(drow[k + 3]) - d4.w));
+        }
+        tmem_st32(tDP, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_dsr + 8 * h);
     }
     // ---- epilogue: dV, dK (x scale) -> bf16 -> the K / V buffers -> TMA store
     if (ok && n > 0) ok = warp_wait(bar_drain, 0, wc);
