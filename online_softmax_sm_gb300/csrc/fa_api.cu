@@ -393,8 +393,8 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
   pre.o = o;
   pre.dout = dout;
   pre.lse = lse;
-  pre.lse2 = static_cast<float*>(ws);
-  pre.dd = reinterpret_cast<float*>(static_cast<char*>(ws) + vec);
+  pre.nlse2 = static_cast<float*>(ws);
+  pre.nd = reinterpret_cast<float*>(static_cast<char*>(ws) + vec);
   pre.Nq = Nq;
   pre.nq_pad = nq_pad;
   pre.BH = BH;
@@ -408,8 +408,8 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
   p.causal = (wl < 0 && wr >= 0) ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.lse2 = pre.lse2;
-  p.dd = pre.dd;
+  p.nlse2 = pre.nlse2;
+  p.nd = pre.nd;
   p.timeout_ns = kDefaultTimeoutNs;
   p.status = dev->status;
   e = d == 64 ? fa::launch_bwd_d64(maps, p, pre, s) : fa::launch_bwd_d128(maps, p, pre, s);

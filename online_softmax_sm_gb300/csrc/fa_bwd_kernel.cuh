@@ -29,9 +29,10 @@
 //     dP = dO_i V_j^T (two dP buffers), dS (bf16) back into dP's columns, and
 //     dQ_i += dS K_j.  S of step j+1 is issued as soon as S of step j is read.
 //   S and dP are recomputed by both: 7 MMAs per tile pair instead of 5.
-// fa_bwd_pre_kernel  D_i and LSE * log2(e) per row (+inf for a row with no
-//   visible key or past Nq, so exp2(S c - lse2) is exactly 0 there), padded to
-//   whole 128-row tiles so the kernels copy them in 512-byte pieces.
+// fa_bwd_pre_kernel  -D_i and -LSE * log2(e) per row (-inf for a row with no
+//   visible key or past Nq, so exp2(S c + nlse2) is exactly 0 there), padded
+//   to whole 128-row tiles so the kernels copy them in 512-byte pieces; stored
+//   negated so P and dS take packed two-lane FMA / add / multiply directly.
 //
 // In the dQ kernel the two compute warpgroups split the 128 columns of S / dP:
 // warpgroup h takes columns [64h, 64h + 64) and writes its bf16 pairs into
@@ -56,9 +57,9 @@ struct BwdCfg {
   static constexpr int kChunks = D / 64;          // 64-column (128-byte) swizzle chunks
   static constexpr int kChunkBytes = kRows * 128;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kVecBytes = kRows * 4;     // lse2 or dd of one tile
+  static constexpr int kVecBytes = kRows * 4;     // nlse2 or nd of one tile
   static constexpr int kStages = D == 128 ? 2 : 4;
-  static constexpr int kStageBytesA = 2 * kTileBytes + 2 * kVecBytes;  // Q_i, dO_i, lse2, dd
+  static constexpr int kStageBytesA = 2 * kTileBytes + 2 * kVecBytes;  // Q_i, dO_i, nlse2, nd
   // dQ kernel: K_j and V_j in separate slots of a ring, K_j at position 2 j
   // and V_j at 2 j + 1; each slot is released by its own last reader.
   static constexpr int kSlotsFit = (227 * 1024 - 1024 - 2 * kTileBytes - 1024) / kTileBytes;
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint8_t* sK = smem;
   uint8_t* sV = sK + C::kTileBytes;
-  uint8_t* sRing = sV + C::kTileBytes;  // stage: Q_i, dO_i, lse2[128], dd[128]
+  uint8_t* sRing = sV + C::kTileBytes;  // stage: Q_i, dO_i, nlse2[128], nd[128]
   BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sRing + C::kStages * C::kStageBytesA);
 
   const int warp = threadIdx.x >> 5;
@@ -263,8 +264,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                       bh);
         }
         const size_t vrow = static_cast<size_t>(bh) * p.nq_pad + q0;
-        bulk_load(smem_u32(base + 2 * C::kTileBytes), p.lse2 + vrow, C::kVecBytes, full, pol);
-        bulk_load(smem_u32(base + 2 * C::kTileBytes + C::kVecBytes), p.dd + vrow, C::kVecBytes,
+        bulk_load(smem_u32(base + 2 * C::kTileBytes), p.nlse2 + vrow, C::kVecBytes, full, pol);
+        bulk_load(smem_u32(base + 2 * C::kTileBytes + C::kVecBytes), p.nd + vrow, C::kVecBytes,
                   full, pol);
         issued_mask |= 1u << st;
         issued_par = (issued_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
@@ -376,11 +377,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     for (int s = 0; ok && s < n; ++s) {
       const int st = s % C::kStages;
       const int q0 = (i_lo + s) * C::kRows + 64 * h;  // this half's first query
-      const float* lse2v = reinterpret_cast<const float*>(sRing + st * C::kStageBytesA + 2 * C::kTileBytes) + 64 * h;
-      const float* ddv = lse2v + C::kRows;
+      const float* nlv = reinterpret_cast<const float*>(sRing + st * C::kStageBytesA + 2 * C::kTileBytes) + 64 * h;
+      const float* ndv = nlv + C::kRows;
       // P^T first, from S^T alone, so dV += P^T dO (and S^T of half-step
       // h + 2 after it) can start while dS^T is still being formed.  The
-      // stage's own barrier makes the bulk-copied lse2 / dd visible here.
+      // stage's own barrier makes the bulk-copied nlse2 / nd visible here.
       ok = warp_wait(bar_full + 8 * st, (s / C::kStages) & 1, wc) && warp_wait(bar_s + 8 * h, s & 1, wc);
       if (!ok) break;
       tc_fence_after();
@@ -389,13 +390,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       {
         uint32_t srow[64];
         tmem_ld64_sync(tS, srow);
+        const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
-        for (int k = 0; k < 64; k += 4) {
-          const float4 a4 = *reinterpret_cast<const float4*>(lse2v + k);
-          pv[k] = ex2_approx(fmaf(__uint_as_float(srow[k]), c, -a4.x));
-          pv[k + 1] = ex2_approx(fmaf(__uint_as_float(srow[k + 1]), c, -a4.y));
-          pv[k + 2] = ex2_approx(fmaf(__uint_as_float(srow[k + 2]), c, -a4.z));
-          pv[k + 3] = ex2_approx(fmaf(__uint_as_float(srow[k + 3]), c, -a4.w));
+        for (int k = 0; k < 64; k += 4) {  // 2^(S c - LSE log2 e), two lanes per FMA
+          const float4 a4 = *reinterpret_cast<const float4*>(nlv + k);
+          float x0, x1, x2, x3;
+          f2_unpack(ffma2(f2_pack(__uint_as_float(srow[k]), __uint_as_float(srow[k + 1])), c2,
+                          f2_pack(a4.x, a4.y)), x0, x1);
+          f2_unpack(ffma2(f2_pack(__uint_as_float(srow[k + 2]), __uint_as_float(srow[k + 3])), c2,
+                          f2_pack(a4.z, a4.w)), x2, x3);
+          pv[k] = ex2_approx(x0);
+          pv[k + 1] = ex2_approx(x1);
+          pv[k + 2] = ex2_approx(x2);
+          pv[k + 3] = ex2_approx(x3);
         }
       }
       // edge tiles only: the mask in a block of its own, so fully visible
@@ -425,12 +432,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tmem_ld64_sync(tDP, drow);
         uint32_t dk[32];
 #pragma unroll
-        for (int k = 0; k < 64; k += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(ddv + k);
-          dk[k >> 1] = pack_bf16x2(pv[k] * (__uint_as_float(drow[k]) - d4.x),
-                                   pv[k + 1] * (__uint_as_float(drow[k + 1]) - d4.y));
-          dk[(k >> 1) + 1] = pack_bf16x2(pv[k + 2] * (__uint_as_float(drow[k + 2]) - d4.z),
-                                         pv[k + 3] * (__uint_as_float(drow[k + 3]) - d4.w));
+        for (int k = 0; k < 64; k += 4) {  // P (dP - D), two lanes per add / multiply
+          const float4 d4 = *reinterpret_cast<const float4*>(ndv + k);
+          float y0, y1, y2, y3;
+          f2_unpack(fmul2(f2_pack(pv[k], pv[k + 1]),
+                          fadd2(f2_pack(__uint_as_float(drow[k]), __uint_as_float(drow[k + 1])),
+                                f2_pack(d4.x, d4.y))), y0, y1);
+          f2_unpack(fmul2(f2_pack(pv[k + 2], pv[k + 3]),
+                          fadd2(f2_pack(__uint_as_float(drow[k + 2]), __uint_as_float(drow[k + 3])),
+                                f2_pack(d4.z, d4.w))), y2, y3);
+          dk[k >> 1] = pack_bf16x2(y0, y1);
+          dk[(k >> 1) + 1] = pack_bf16x2(y2, y3);
         }
         tmem_st32(tDP, dk);
       }
@@ -652,9 +664,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int row = q0 + t;
     const size_t vrow = static_cast<size_t>(bh) * p.nq_pad + row;
-    const float lse2 = p.lse2[vrow];
-    const float dd = p.dd[vrow];
     const float c = p.scale_log2;
+    const uint64_t nl2 = f2_pack(p.nlse2[vrow], p.nlse2[vrow]), nd2 = f2_pack(p.nd[vrow], p.nd[vrow]);
+    const uint64_t c2 = f2_pack(c, c);
     bool ok = true;
     for (int j = 0; ok && j < n; ++j) {
       const int key0 = (j_lo + j) * C::kRows;
@@ -678,7 +690,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tmem_ld32_sync(dpc + col, dr);
         float pv[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pv[k] = ex2_approx(fmaf(__uint_as_float(sr[32 * cc + k]), c, -lse2));
+        for (int k = 0; k < 32; k += 2) {  // 2^(S c - LSE log2 e), two lanes per FMA
+          float x0, x1;
+          f2_unpack(ffma2(f2_pack(__uint_as_float(sr[32 * cc + k]), __uint_as_float(sr[32 * cc + k + 1])),
+                          c2, nl2), x0, x1);
+          pv[k] = ex2_approx(x0);
+          pv[k + 1] = ex2_approx(x1);
+        }
         if (!all_vis) {  // edge tiles only
 #pragma unroll
           for (int k = 0; k < 32; ++k)
@@ -686,9 +704,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
         uint32_t dk[16];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2)
-          dk[k >> 1] = pack_bf16x2(pv[k] * (__uint_as_float(dr[k]) - dd),
-                                   pv[k + 1] * (__uint_as_float(dr[k + 1]) - dd));
+        for (int k = 0; k < 32; k += 2) {  // P (dP - D)
+          float y0, y1;
+          f2_unpack(fmul2(f2_pack(pv[k], pv[k + 1]),
+                          fadd2(f2_pack(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1])), nd2)), y0, y1);
+          dk[k >> 1] = pack_bf16x2(y0, y1);
+        }
         tmem_st16(dpc + 64 * h + 16 * cc, dk);
       }
       tmem_wait_st();
@@ -738,8 +759,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 }
 
 // ================================================================ preprocess
-// D_i = <dO_i, O_i> (fp32 over bf16 inputs) and lse2_i = LSE_i log2(e), or
-// +inf where LSE_i = -inf; rows in [Nq, nq_pad) get D = 0, lse2 = +inf.
+// nd_i = -<dO_i, O_i> (fp32 over bf16 inputs) and nlse2_i = -LSE_i log2(e),
+// or -inf where LSE_i = -inf; rows in [Nq, nq_pad) get nd = 0, nlse2 = -inf.
 // d/8 lanes per row, one 16-byte load of O and of dO each.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdPreParams p) {
@@ -766,15 +787,15 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdPreParams p) {
 #pragma unroll
   for (int o = kLanes / 2; o > 0; o >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, o, kLanes);
   if (live && part == 0) {
-    float l2 = INFINITY;
+    float nl2 = -INFINITY;
     if (r < p.Nq) {
       const float lse = p.lse[static_cast<size_t>(bh) * p.Nq + r];
-      l2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
+      nl2 = lse == -INFINITY ? -INFINITY : -(lse * 1.4426950408889634f);
     } else {
       acc = 0.f;
     }
-    p.lse2[row] = l2;
-    p.dd[row] = acc;
+    p.nlse2[row] = nl2;
+    p.nd[row] = -acc;
   }
 }
 

@@ -65,13 +65,13 @@ cudaError_t launch_merge(int d, const MergeParams& p, cudaStream_t s);
 // Attention backward (fa_bwd_kernel.cuh).
 struct BwdParams {
   int Nq, Nk, BH;
-  int nq_pad;         // rows of lse2 / dd per head (Nq rounded up to 128)
+  int nq_pad;         // rows of nlse2 / nd per head (Nq rounded up to 128)
   int wl, wr;         // mask window, as FwdParams (causal = (-1, 0))
   int causal;         // launch order only
   float scale;        // natural-units logit scale
   float scale_log2;   // scale * log2(e)
-  const float* lse2;  // [BH][nq_pad]: LSE * log2(e); +inf where P must be 0
-  const float* dd;    // [BH][nq_pad]: D_i = <dO_i, O_i>
+  const float* nlse2; // [BH][nq_pad]: -LSE * log2(e); -inf where P must be 0
+  const float* nd;    // [BH][nq_pad]: -D_i = -<dO_i, O_i>
   unsigned long long timeout_ns;
   int* status;
 };
@@ -80,8 +80,8 @@ struct BwdPreParams {
   const void* o;      // bf16 [BH][Nq][d]
   const void* dout;   // bf16 [BH][Nq][d]
   const float* lse;   // [BH][Nq]
-  float* lse2;        // [BH][nq_pad]
-  float* dd;          // [BH][nq_pad]
+  float* nlse2;       // [BH][nq_pad]
+  float* nd;          // [BH][nq_pad]
   int Nq, nq_pad, BH;
 };
 
