@@ -26,8 +26,8 @@
 //     each warpgroup has two half-steps of MMA time for its exponentials.
 //   fa_bwd_dq_kernel  one 128-row query tile per CTA, Q_i and dO_i in shared
 //     memory, looping over the key tiles it sees: S = Q_i K_j^T and
-//     dP = dO_i V_j^T (two dP buffers), dS (bf16) back into dP's columns, and
-//     dQ_i += dS K_j.  S of step j+1 is issued as soon as S of step j is read.
+//     dP = dO_i V_j^T, each released as soon as every row has read it, dS
+//     (bf16) into one of two TMEM buffers of its own, and dQ_i += dS K_j.
 //   S and dP are recomputed by both: 7 MMAs per tile pair instead of 5.
 // fa_bwd_pre_kernel  -D_i and -LSE * log2(e) per row (-inf for a row with no
 //   visible key or past Nq, so exp2(S c + nlse2) is exactly 0 there), padded
@@ -36,9 +36,8 @@
 //
 // In the dQ kernel the two compute warpgroups split the 128 columns of S / dP:
 // warpgroup h takes columns [64h, 64h + 64) and writes its bf16 pairs into
-// columns [64h, 64h + 32) of the same region, so no warpgroup overwrites
-// columns the other still has to read.  The A operand's K-slice kk (16
-// elements = 8 columns) is therefore at column 64 (kk / 4) + 8 (kk % 4).
+// columns [32h, 32h + 32) of the dS buffer, so the buffer holds keys in order
+// and the A operand's K-slice kk (16 keys) is at column 8 kk.
 //
 // Every wait is bounded (fa_wait.cuh); a wait that runs out stops the CTA
 // without writing its outputs.
@@ -84,8 +83,8 @@ struct BwdCfg {
   // dK/dV kernel: S^T / P^T buffers at 64 b, dP^T / dS^T at 128 + 64 b, then
   // the two accumulators.
   static constexpr int kS = 0, kDP = 128, kDV = 256, kDK = 256 + D;
-  // dQ kernel: S, two dP / dS buffers, dQ.
-  static constexpr int kDP0 = 128, kDP1 = 256, kDQ = 384;
+  // dQ kernel: S, dP, two bf16 dS buffers of 64 columns, dQ.
+  static constexpr int kDPq = 128, kDS0 = 256, kDQ = 384;
 };
 
 struct __align__(8) BwdCtl {
@@ -94,6 +93,7 @@ struct __align__(8) BwdCtl {
   uint64_t empty[8];    // every MMA reading the stage / slot completed
   uint64_t s_full[2];   // S(^T) of this step in TMEM (dK/dV: per buffer)
   uint64_t s_free;      // dQ kernel: S read by all 256 compute threads
+  uint64_t dp_free;     // dQ kernel: dP read by all 256 compute threads
   uint64_t dp_full[2];  // dP(^T) in TMEM (buffer)
   uint64_t ready[2];    // bf16 P^T (dK/dV kernel) or dS (dQ kernel) written back to TMEM
   uint64_t ds_ready[2]; // dK/dV kernel: bf16 dS^T written back to TMEM
@@ -140,11 +140,6 @@ __device__ __forceinline__ uint32_t kslice_kmajor(int kk) {
 __device__ __forceinline__ uint32_t kslice_mnmajor(int kk) {
   return static_cast<uint32_t>(kk * 2048) >> 4;
 }
-// TMEM column of K-slice kk of a bf16 A operand written by the two warpgroups.
-__device__ __forceinline__ uint32_t a_col(int kk) {
-  return static_cast<uint32_t>(64 * (kk / 4) + 8 * (kk % 4));
-}
-
 // Stage a [128][D] bf16 tile row for a TMA store: row t, columns
 // [c0, c0 + 32) (packed pairs w[16]) into the 128-byte-swizzled layout.
 template <int D>
@@ -534,7 +529,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const uint32_t bar_empty = smem_u32(&ctl->empty[0]);
   const uint32_t bar_s = smem_u32(&ctl->s_full[0]);
   const uint32_t bar_sfree = smem_u32(&ctl->s_free);
-  const uint32_t bar_dp = smem_u32(&ctl->dp_full[0]);     // + 8 b
+  const uint32_t bar_dp = smem_u32(&ctl->dp_full[0]);
+  const uint32_t bar_dpfree = smem_u32(&ctl->dp_free);
   const uint32_t bar_ready = smem_u32(&ctl->ready[0]);    // + 8 b
   const uint32_t bar_dq = smem_u32(&ctl->done_b[0]);      // + 8 b
   const uint32_t bar_drain = smem_u32(&ctl->drain);
@@ -547,8 +543,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_sfree, 256);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_dpfree, 256);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_dp + 8 * b, 1);
       mbar_init(bar_ready + 8 * b, 256);
       mbar_init(bar_dq + 8 * b, 1);
     }
@@ -600,8 +597,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   } else if (warp == C::kMmaWarp || warp == C::kMmaWarp2) {
     // --------------------------------------------------------- MMA issuers
     // Warp kMmaWarp: S(j) = Q_i K_j^T once every row has read S(j-1), and
-    // dP(j) = dO_i V_j^T into buffer j & 1 once dQ(j-2) has read that buffer.
-    // Warp kMmaWarp2: dQ += dS(j) K_j once dS(j) is written back.
+    // dP(j) = dO_i V_j^T once every row has read dP(j-1).
+    // Warp kMmaWarp2: dQ += dS(j) K_j once dS(j) is in its TMEM buffer j & 1.
     constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
     constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, true);  // B = K_j (MN-major)
     auto slot = [&](int pos) { return smem_u32(sRing + (pos % C::kSlotsB) * C::kStageBytesB); };
@@ -624,17 +621,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                               kIdescS, kk > 0);
           mma_commit_elect(bar_s);
         }
-        ok = slot_full(2 * j + 1) &&
-             (j < 2 || warp_wait(bar_dq + 8 * (j & 1), ((j - 2) >> 1) & 1, wc));
+        ok = slot_full(2 * j + 1) && (j == 0 || warp_wait(bar_dpfree, (j - 1) & 1, wc));
         if (!ok) break;
         tc_fence_after();
         {
           const uint64_t dVk = desc_kmajor<D>(slot(2 * j + 1));
-          const uint32_t dst = tmem + ((j & 1) ? C::kDP1 : C::kDP0);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_bf16_ss_elect(dst, dOk + kslice_kmajor<D>(kk), dVk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
-          mma_commit_elect(bar_dp + 8 * (j & 1));
+            mma_bf16_ss_elect(tmem + C::kDPq, dOk + kslice_kmajor<D>(kk), dVk + kslice_kmajor<D>(kk),
+                              kIdescS, kk > 0);
+          mma_commit_elect(bar_dp);
           mma_commit_elect(bar_empty + 8 * ((2 * j + 1) % C::kSlotsB));  // V_j read
         }
       }
@@ -644,10 +640,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint64_t dKmn = desc_mnmajor<D>(slot(2 * j));
-        const uint32_t src = tmem + ((j & 1) ? C::kDP1 : C::kDP0);
+        const uint32_t src = tmem + C::kDS0 + 64 * (j & 1);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j (K = 128 keys)
-          mma_bf16_ts_elect(tmem + C::kDQ, src + a_col(kk), dKmn + kslice_mnmajor(kk), kIdescDQ,
+        for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j (K = 128 keys, 8 columns per K-step)
+          mma_bf16_ts_elect(tmem + C::kDQ, src + 8 * kk, dKmn + kslice_mnmajor(kk), kIdescDQ,
                             (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit_elect(bar_dq + 8 * (j & 1));
         // K_j: S(j) (the other warp) completed before dS(j) could exist
@@ -673,45 +669,52 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ok = warp_wait(bar_s, j & 1, wc);
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32_sync(tmem + lane_off + C::kS + 64 * h, sr);
-      tmem_ld32_sync(tmem + lane_off + C::kS + 64 * h + 32, sr + 32);
-      tc_fence_before();
-      mbar_arrive(bar_sfree);  // S may be overwritten by S of step j+1
-      const uint32_t dpc = tmem + lane_off + ((j & 1) ? C::kDP1 : C::kDP0);
-      ok = warp_wait(bar_dp + 8 * (j & 1), (j >> 1) & 1, wc);
-      if (!ok) break;
-      tc_fence_after();
-      const bool all_vis = bwd_tile_all_visible(q0, key0, p);
+      // this warpgroup's 64 keys of S; the buffer is released right away
+      float pv[64];
+      {
+        uint32_t sr[64];
+        tmem_ld32_sync(tmem + lane_off + C::kS + 64 * h, sr);
+        tmem_ld32_sync(tmem + lane_off + C::kS + 64 * h + 32, sr + 32);
+        tc_fence_before();
+        mbar_arrive(bar_sfree);  // S may be overwritten by S of step j+1
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int col = 64 * h + 32 * cc;
-        uint32_t dr[32];
-        tmem_ld32_sync(dpc + col, dr);
-        float pv[32];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {  // 2^(S c - LSE log2 e), two lanes per FMA
+        for (int k = 0; k < 64; k += 2) {  // 2^(S c - LSE log2 e), two lanes per FMA
           float x0, x1;
-          f2_unpack(ffma2(f2_pack(__uint_as_float(sr[32 * cc + k]), __uint_as_float(sr[32 * cc + k + 1])),
-                          c2, nl2), x0, x1);
+          f2_unpack(ffma2(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nl2), x0, x1);
           pv[k] = ex2_approx(x0);
           pv[k + 1] = ex2_approx(x1);
         }
-        if (!all_vis) {  // edge tiles only
+      }
+      if (!bwd_tile_all_visible(q0, key0, p)) {  // edge tiles only
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (!bwd_visible(row, key0 + col + k, p)) pv[k] = 0.f;
-        }
-        uint32_t dk[16];
+        for (int k = 0; k < 64; ++k)
+          if (!bwd_visible(row, key0 + 64 * h + k, p)) pv[k] = 0.f;
+      }
+      ok = warp_wait(bar_dp, j & 1, wc);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dk[32];
+      {
+        uint32_t dr[64];
+        tmem_ld32_sync(tmem + lane_off + C::kDPq + 64 * h, dr);
+        tmem_ld32_sync(tmem + lane_off + C::kDPq + 64 * h + 32, dr + 32);
+        tc_fence_before();
+        mbar_arrive(bar_dpfree);  // dP may be overwritten by dP of step j+1
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {  // P (dP - D)
+        for (int k = 0; k < 64; k += 2) {  // P (dP - D)
           float y0, y1;
           f2_unpack(fmul2(f2_pack(pv[k], pv[k + 1]),
                           fadd2(f2_pack(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1])), nd2)), y0, y1);
           dk[k >> 1] = pack_bf16x2(y0, y1);
         }
-        tmem_st16(dpc + 64 * h + 16 * cc, dk);
       }
+      // dS buffer j & 1 is free once dQ += dS(j-2) K has completed
+      if (j >= 2 && !warp_wait(bar_dq + 8 * (j & 1), ((j - 2) >> 1) & 1, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st32(tmem + lane_off + C::kDS0 + 64 * (j & 1) + 32 * h, dk);  // keys 64 h .. 64 h + 63
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_ready + 8 * (j & 1));
