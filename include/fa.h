@@ -77,6 +77,28 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int Nk, int d, float scale, int causal, int n_splits, void* stream);
 
 /*
+ * fa_fwd on HOST buffers, the copies included: Q, K, V go to the device, the
+ * forward runs, O and LSE come back; returns once o and lse hold the result.
+ * The (b, h) heads are cut into n_chunks groups of consecutive heads that pass
+ * through three internal streams (host-to-device copies, kernels,
+ * device-to-host copies), so one group's copies overlap another's kernel.
+ * n_chunks <= 0 picks min(B*H, 8); larger values are clamped to min(B*H, 64).
+ *
+ * q, k, v : in,  host bf16 [B][H][Nq|Nk][d]
+ * o       : out, host bf16 [B][H][Nq][d]
+ * lse     : out, host fp32 [B][H][Nq]
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to run asynchronously and overlap; pageable buffers give the same
+ * results, staged by the driver.  Device memory: one buffer per device of the
+ * problem's size (Q, K, V, O, LSE), kept by the library for later calls and
+ * grown when a larger call comes (FA_ERR_NO_MEMORY if that fails).  Calls on
+ * the same device are serialised (they share that buffer and the streams).
+ * Errors: as fa_fwd; FA_ERR_DEVICE_TIMEOUT if a device-side wait ran out.
+ */
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Nq, int Nk, int d, float scale, int causal, int n_chunks);
+
+/*
  * Attention forward with a local (sliding-window) mask, "causal, local" masks
  * of "Online Softmax 算法详解" section 3.2 (which names the local mask without
  * defining it).  With off = Nk - Nq, key j is visible to query i iff

@@ -68,6 +68,8 @@ def _declare(L):
     L.fa_fwd_local.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i,
                                _i, _vp]
     L.fa_fwd_local.restype = _i
+    L.fa_fwd_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i]
+    L.fa_fwd_host.restype = _i
     L.fa_softmax_rows.argtypes = [_vp, _vp, _vp, ctypes.c_longlong, _i, _i, _vp]
     L.fa_softmax_rows.restype = _i
     L.fa_fwd_fp8.argtypes = [_vp] * 5 + [_i] * 5 + [ctypes.c_float] * 4 + [_i, _vp]
@@ -153,6 +155,37 @@ def fwd(q, k, v, scale: float | None = None, causal: bool = False, n_splits: int
         else:
             rc = L.fa_fwd(*args)
     _check(rc, "fa_fwd")
+    return out, lse
+
+
+def fwd_host(q, k, v, scale: float | None = None, causal: bool = False, out=None, lse=None,
+             n_chunks: int = 0, device=None):
+    """fa_fwd_host: q, k, v are CPU bf16 [B, H, N, d] tensors (page-locked for overlap); the
+    call copies them to the device, runs the forward there and copies O and LSE back into
+    CPU tensors.  Returns (o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq]) on the CPU."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+            raise ValueError(f"{name} must be a CPU tensor")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bfloat16 [B, H, N, d] tensor")
+    B, H, Nq, d = q.shape
+    if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError("k and v must be [B, H, Nk, d] matching q")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=q.is_pinned())
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=q.is_pinned())
+    if out.device.type != "cpu" or out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CPU bfloat16 tensor shaped like q")
+    if lse.device.type != "cpu" or lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous CPU float32 [B, H, Nq] tensor")
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        rc = lib().fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               B, H, Nq, Nk, d, float(scale), int(bool(causal)), int(n_chunks))
+    _check(rc, "fa_fwd_host")
     return out, lse
 
 

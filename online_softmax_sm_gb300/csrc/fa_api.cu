@@ -253,6 +253,32 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   return FA_OK;
 }
 
+// fa_fwd_host: per-device device buffer and streams, held across calls.
+constexpr int kMaxHostChunks = 64;
+struct HostPipe {
+  std::mutex mu;
+  bool init = false;
+  char* buf = nullptr;
+  size_t cap = 0;
+  cudaStream_t s_in = nullptr, s_run = nullptr, s_out = nullptr;
+  cudaEvent_t in_done[kMaxHostChunks], run_done[kMaxHostChunks];
+};
+HostPipe g_pipe[kMaxDevices];
+
+int host_pipe_init(HostPipe& hp) {
+  if (hp.init) return FA_OK;
+  cudaError_t e = cudaSuccess;
+  for (cudaStream_t* st : {&hp.s_in, &hp.s_run, &hp.s_out})
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
+  for (int c = 0; e == cudaSuccess && c < kMaxHostChunks; ++c) {
+    e = cudaEventCreateWithFlags(&hp.in_done[c], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.run_done[c], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  hp.init = true;
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -261,6 +287,91 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int Nk, int d, float scale, int causal, int n_splits, void* stream) {
   return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, -1, causal ? 0 : -1, n_splits, stream,
                   nullptr, nullptr, nullptr, nullptr);
+}
+
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Nq, int Nk, int d, float scale, int causal, int n_chunks) {
+  int rc = check_sizes(B, H, Nq, Nk, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  DevState* dev = nullptr;
+  if ((rc = device_state(&dev)) != FA_OK) return rc;
+  int dev_id = 0;
+  cudaError_t e = cudaGetDevice(&dev_id);
+  if (e != cudaSuccess) return cuda_fail(e);
+  HostPipe& hp = g_pipe[dev_id];
+  std::lock_guard<std::mutex> lock(hp.mu);
+  if ((rc = host_pipe_init(hp)) != FA_OK) return rc;
+
+  const int BH = B * H;
+  const size_t q_head = static_cast<size_t>(Nq) * d * 2, kv_head = static_cast<size_t>(Nk) * d * 2;
+  const size_t lse_head = static_cast<size_t>(Nq) * 4;
+  const size_t off_k = align256(BH * q_head), off_v = off_k + align256(BH * kv_head);
+  const size_t off_o = off_v + align256(BH * kv_head), off_l = off_o + align256(BH * q_head);
+  const size_t need = off_l + align256(BH * lse_head);
+  if (need > hp.cap) {
+    if (hp.buf && (e = cudaFree(hp.buf)) != cudaSuccess) return cuda_fail(e);
+    hp.buf = nullptr;
+    hp.cap = 0;
+    if ((e = cudaMalloc(&hp.buf, need)) != cudaSuccess) {
+      t_last_cuda = e;
+      return FA_ERR_NO_MEMORY;
+    }
+    hp.cap = need;
+  }
+  char* dq = hp.buf;
+  char* dk = hp.buf + off_k;
+  char* dv = hp.buf + off_v;
+  char* dout = hp.buf + off_o;
+  float* dl = reinterpret_cast<float*>(hp.buf + off_l);
+  const char* hq = static_cast<const char*>(q);
+  const char* hk = static_cast<const char*>(k);
+  const char* hv = static_cast<const char*>(v);
+  char* ho = static_cast<char*>(o);
+
+  int chunks = n_chunks <= 0 ? (BH < 8 ? BH : 8) : n_chunks;
+  if (chunks > BH) chunks = BH;
+  if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;
+  const int per = (BH + chunks - 1) / chunks;
+  // Group c: heads [c per, min(BH, (c + 1) per)): copies in on s_in, the
+  // kernel on s_run after them, copies out on s_out after the kernel.  (A
+  // second copy-in stream gained nothing: one stream already fills the
+  // host-to-device link, about 205 GB/s on GB300.)
+  for (int c = 0; c < chunks && rc == FA_OK && e == cudaSuccess; ++c) {
+    const int h0 = c * per, nh = (BH - h0 < per) ? BH - h0 : per;
+    if (nh <= 0) break;
+    cudaStream_t si = hp.s_in;
+    e = cudaMemcpyAsync(dq + h0 * q_head, hq + h0 * q_head, nh * q_head, cudaMemcpyHostToDevice, si);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dk + h0 * kv_head, hk + h0 * kv_head, nh * kv_head, cudaMemcpyHostToDevice, si);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dv + h0 * kv_head, hv + h0 * kv_head, nh * kv_head, cudaMemcpyHostToDevice, si);
+    if (e == cudaSuccess) e = cudaEventRecord(hp.in_done[c], si);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_run, hp.in_done[c], 0);
+    if (e != cudaSuccess) break;
+    rc = fwd_impl(dq + h0 * q_head, dk + h0 * kv_head, dv + h0 * kv_head, dout + h0 * q_head,
+                  dl + static_cast<size_t>(h0) * Nq, 1, nh, Nq, Nk, d, scale, -1, causal ? 0 : -1, 1,
+                  hp.s_run, nullptr, nullptr, nullptr, nullptr);
+    if (rc != FA_OK) break;
+    e = cudaEventRecord(hp.run_done[c], hp.s_run);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_out, hp.run_done[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(ho + h0 * q_head, dout + h0 * q_head, nh * q_head, cudaMemcpyDeviceToHost,
+                          hp.s_out);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(lse + static_cast<size_t>(h0) * Nq, dl + static_cast<size_t>(h0) * Nq,
+                          nh * lse_head, cudaMemcpyDeviceToHost, hp.s_out);
+  }
+  // drain all three streams whatever happened above
+  cudaError_t es = cudaStreamSynchronize(hp.s_in);
+  cudaError_t er = cudaStreamSynchronize(hp.s_run);
+  cudaError_t eo = cudaStreamSynchronize(hp.s_out);
+  if (rc != FA_OK) return rc;
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (es != cudaSuccess) return cuda_fail(es);
+  if (er != cudaSuccess) return cuda_fail(er);
+  if (eo != cudaSuccess) return cuda_fail(eo);
+  return fa_get_device_status(hp.s_out);
 }
 
 int fa_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

@@ -86,6 +86,11 @@ def test_invalid_options_and_partial_and_merge_args(L):
     assert L.fa_merge_splits(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 80, 2, None) == fa.FA_ERR_UNSUPPORTED
     assert L.fa_merge_splits(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 64, 0, None) == fa.FA_ERR_INVALID_ARG
     assert L.fa_merge_splits(0x1000, 0x1000, 0x1008, 0x1000, 0x1000, 1, 1, 8, 64, 2, None) == fa.FA_ERR_INVALID_ARG
+    # fa_fwd_host: sizes and null pointers checked before any device work
+    assert L.fa_fwd_host(None, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 64, 0.125, 0, 0) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_host(0x1000, 0x1000, 0x1000, 0x1000, None, 1, 1, 8, 8, 64, 0.125, 0, 0) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0, 1, 8, 8, 64, 0.125, 0, 0) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 96, 0.125, 0, 0) == fa.FA_ERR_UNSUPPORTED
 
 
 def test_product_path_fails_loudly_without_library(tmp_path, monkeypatch):
