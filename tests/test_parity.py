@@ -58,6 +58,27 @@ def test_large_logits_and_growing_max():
     print(P.run_workload(w).check(w.name))
 
 
+@pytest.mark.parametrize("bc", [64, 128])
+def test_reference_moves_and_stays(bc):
+    """Row maxima that grow by a set amount per K/V tile: with key j of tile t
+    carrying g*t in dimension 0 and query row r carrying a_r there, row r's
+    max grows by about a_r*g*log2(e) base-2 units per tile.  a_r spans 0.25..2
+    with g*log2(e) = 12, so some rows grow by less than 16 units per tile (the
+    kernel keeps its softmax reference for several tiles, P up to 2^16) and
+    others by more (it moves the reference and rescales O on every tile)."""
+    B, H, Nq, Nk, d = 1, 2, 256, 8 * 128, 64
+    g = torch.Generator().manual_seed(11)
+    q = 0.05 * torch.randn((B, H, Nq, d), generator=g)
+    k = 0.05 * torch.randn((B, H, Nk, d), generator=g)
+    v = torch.randn((B, H, Nk, d), generator=g)
+    q[..., 0] = torch.linspace(0.25, 2.0, Nq)
+    k[..., 0] = (torch.arange(Nk) // 128).float() * (12.0 / math.log2(math.e))
+    q, k, v = (t.to(torch.bfloat16).cuda() for t in (q, k, v))
+    o, lse = fa.fwd(q, k, v, 1.0, False, bc=bc)
+    torch.cuda.synchronize()
+    print(P.compare(q, k, v, o, lse, 1.0, False).check(f"reference moves/stays bc={bc}"))
+
+
 # --------------------------------------------------- the pages' worked examples
 
 def _example_case(scores_blocks, values, bc=64, n_splits=1):
