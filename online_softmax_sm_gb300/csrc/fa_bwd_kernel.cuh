@@ -673,8 +673,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       float pv[64];
       {
         uint32_t sr[64];
-        tmem_ld32_sync(tmem + lane_off + C::kS + 64 * h, sr);
-        tmem_ld32_sync(tmem + lane_off + C::kS + 64 * h + 32, sr + 32);
+        tmem_ld64_sync(tmem + lane_off + C::kS + 64 * h, sr);
         tc_fence_before();
         mbar_arrive(bar_sfree);  // S may be overwritten by S of step j+1
 #pragma unroll
@@ -696,8 +695,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       uint32_t dk[32];
       {
         uint32_t dr[64];
-        tmem_ld32_sync(tmem + lane_off + C::kDPq + 64 * h, dr);
-        tmem_ld32_sync(tmem + lane_off + C::kDPq + 64 * h + 32, dr + 32);
+        tmem_ld64_sync(tmem + lane_off + C::kDPq + 64 * h, dr);
         tc_fence_before();
         mbar_arrive(bar_dpfree);  // dP may be overwritten by dP of step j+1
 #pragma unroll

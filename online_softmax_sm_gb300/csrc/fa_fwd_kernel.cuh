@@ -581,8 +581,10 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       tc_fence_after();
 
       uint32_t r[BC];
-#pragma unroll
-      for (int h = 0; h < BC / 64; ++h) tmem_ld64_sync(tS + h * 64, r + h * 64);
+      if constexpr (BC == 128)
+        tmem_ld64x2_sync(tS, tS + 64, r);
+      else
+        tmem_ld64_sync(tS, r);
       tc_fence_before();
       mbar_arrive(bar_sfree + 8 * i);  // the S buffer may take the next product
       float s[BC];
