@@ -276,13 +276,15 @@ def forward(fa, w: workloads.Workload, q, k, v, o, lse):
     return fa.fwd(q, k, v, w.scale, w.causal, w.n_splits, out=o, lse=lse, bc=w.bc)
 
 
-def cpu_oracle_sample(w: workloads.Workload, q, k, v, target_s: float, seed: int = 0):
-    """Time the oracle on a bounded row sample of the workload; returns a dict."""
+def cpu_oracle_sample(w: workloads.Workload, q, k, v, target_s: float, seed: int = 0,
+                      threads: int = 0):
+    """Time the oracle on a bounded row sample of the workload (all host
+    cores unless `threads` is given); returns a dict."""
     import numpy as np
 
     import oracle
 
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     rng = np.random.default_rng(seed)
     B, H = w.B, w.H
     # per-row cost: 4*Nk_visible*d; calibrate on a small sample first
@@ -522,6 +524,12 @@ def run_ours(args, w):
         cpu = {"value": s["tflops"], "unit": "TFLOPS", "cores": s["threads"], "kind": "oracle",
                "sample": f"{s['rows']} seeded query rows over {s['heads']} heads of this workload "
                          f"({s['flops']:.3g} FLOP, {s['seconds']:.1f} s), fp64 three-pass oracle"}
+        if w.name in (workloads.C1.name, workloads.C2.name):
+            # the two small workloads also get the oracle's single-thread rate
+            s1 = cpu_oracle_sample(w, q, k, v, min(args.cpu_seconds, 5.0), threads=1)
+            cpu["one_core"] = {"value": s1["tflops"], "unit": "TFLOPS", "cores": 1,
+                               "sample": f"{s1['rows']} seeded query rows over {s1['heads']} heads "
+                                         f"({s1['flops']:.3g} FLOP, {s1['seconds']:.1f} s)"}
 
     if rank == 0:
         line = {
