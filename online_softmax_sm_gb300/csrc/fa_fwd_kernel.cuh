@@ -44,10 +44,11 @@
 // the softmax warpgroups.
 // TMEM (32-bit columns): S_i (BC columns per tile where 512 columns hold
 // everything, else one S buffer that the tiles take in turn: S_0(0), S_1(0),
-// S_0(1), ...), P_i (BC/2 or BC/4 columns), O_i (D columns each).  P_i(j+1) is written only after O_i += P_i(j) V_j has
-// completed.  Shared memory: the Q tiles ([128 rows][D], 128-byte swizzle, the
-// layout the MMA reads K-major), then the K/V ring: keeping P out of shared
-// memory leaves room for five 32 KB stages at d = 128.
+// S_0(1), ...), P_i (BC/2 or BC/4 columns), O_i (D columns each).  P_i(j+1)
+// is written only after O_i += P_i(j) V_j has completed.  Shared memory: the
+// Q tiles ([128 rows][D], 128-byte swizzle, the layout the MMA reads K-major),
+// then the K/V ring: keeping P out of shared memory leaves room for five 32 KB
+// stages at d = 128.
 // Softmax reference: bf16 rows move their reference m only when the tile max
 // exceeds it by more than 16 in base-2 exponent units (P <= 2^16), so O is
 // rarely rescaled; the final O / l and LSE do not depend on the reference.
@@ -142,7 +143,7 @@ struct __align__(8) Ctl {
   uint64_t s_free[2];       // all 128 rows of S_i(j) read into registers (128 arrivals)
   uint64_t alpha_full[2];   // alpha_i(j) published (128 softmax arrivals)
   uint64_t alpha_free[2];   // alpha_i(j) read by the correction (128 arrivals)
-  uint64_t pv_ready[2];     // P_i(j) in shared memory and O_i rescaled (128 + 128 arrivals)
+  uint64_t pv_ready[2];     // P_i(j) in TMEM and O_i rescaled (128 softmax [+ 128 correction] arrivals)
   uint64_t o_done[2];       // O_i += P_i(j) V_j completed (MMA commit)
   uint64_t drain[2];        // every MMA of tile i's issuer has completed
   uint32_t tmem_base;
