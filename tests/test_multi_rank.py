@@ -43,7 +43,7 @@ def _worker(rank, world, port, out):
 @pytest.mark.timeout(120)
 def test_two_rank_replicas_take_max_time_and_sum_work():
     if torch.cuda.is_available():
-        pytest.skip("gloo-on-CPU test; the GPU box runs the single-GPU tests")
+        pytest.skip("gloo ranks on CPU; a machine with a GPU runs the single-GPU tests instead")
     ctx = mp.get_context("spawn")
     mgr = ctx.Manager()
     out = mgr.dict()
