@@ -717,19 +717,100 @@ def run_softmax(args, sw):
         dist.destroy_process_group()
 
 
+def oracle_fp8_rows(w: workloads.Workload, q8, k8, v8, b: int, h: int, rows) -> float:
+    """The oracle's FP8 forward (Max_offset = 8, descales 1; one host thread)
+    on the listed rows of head (b, h).  Returns its wall time in seconds."""
+    import oracle
+
+    qh, kh, vh = (x[b, h].float().cpu().double().numpy() for x in (q8, k8, v8))
+    t0 = time.perf_counter()
+    oracle.attention_fp8(qh, kh, vh, w.scale, 1.0, 1.0, 1.0, w.causal, rows=rows)
+    return time.perf_counter() - t0
+
+
+def fp8_oracle_sample(w: workloads.Workload, q8, k8, v8, target_s: float, seed: int = 0):
+    """Time the FP8 oracle on seeded rows of seeded heads for about target_s
+    seconds; returns a dict."""
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    calib = sorted(rng.choice(w.Nq, size=min(w.Nq, 16), replace=False).tolist())
+    oracle_fp8_rows(w, q8, k8, v8, 0, 0, calib[:1])  # loads the library
+    rate = row_flops(w, calib) / max(oracle_fp8_rows(w, q8, k8, v8, 0, 0, calib), 1e-9)
+    avg_row = w.flops / (w.B * w.H * w.Nq)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    rng.shuffle(heads)
+    flops = elapsed = 0.0
+    n_rows = n_heads = 0
+    for b, h in heads:
+        if elapsed >= target_s:
+            break
+        take = int(max(8, min(w.Nq, rate * (target_s - elapsed) / avg_row)))
+        rows = sorted(rng.choice(w.Nq, size=take, replace=False).tolist())
+        elapsed += oracle_fp8_rows(w, q8, k8, v8, b, h, rows)
+        flops += row_flops(w, rows)
+        n_rows += take
+        n_heads += 1
+    return {"tflops": flops / elapsed / 1e12, "seconds": elapsed, "rows": n_rows, "heads": n_heads,
+            "threads": 1, "flops": flops}
+
+
+def run_fp8_reference(args, w):
+    """--impl reference for the FP8 forward: the oracle's FP8 steps (fp64
+    arithmetic, E4M3 rounding of P') on one host thread, each step seeded rows
+    of one head (bounded so the whole run takes about a minute)."""
+    world, rank, local = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    import numpy as np
+
+    q8, k8, v8 = (t.to(torch.float8_e4m3fn) for t in workloads.generate(w, device="cpu"))
+    rng = np.random.default_rng(1)
+    per_step_s = min(3.0, 60.0 / max(1, args.steps + args.warmup))
+    calib = sorted(rng.choice(w.Nq, size=min(w.Nq, 16), replace=False).tolist())
+    oracle_fp8_rows(w, q8, k8, v8, 0, 0, calib[:1])  # loads the library
+    rate = row_flops(w, calib) / max(oracle_fp8_rows(w, q8, k8, v8, 0, 0, calib), 1e-9)
+    avg_row = w.flops / (w.B * w.H * w.Nq)
+    rows_per_step = int(max(8, min(w.Nq, rate * per_step_s / avg_row)))
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+
+    def step(i):
+        b, h = heads[i % len(heads)]
+        rows = sorted(rng.choice(w.Nq, size=rows_per_step, replace=False).tolist())
+        return oracle_fp8_rows(w, q8, k8, v8, b, h, rows), row_flops(w, rows)
+
+    for i in range(args.warmup):
+        step(i)
+    total = flops = 0.0
+    for i in range(args.steps):
+        t, f = step(args.warmup + i)
+        total += t
+        flops += f
+    value = flops / total / 1e12
+    line = {
+        "impl": "reference", "metric": FP8_METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name + ":fp8", "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": w.causal, "descales": [1.0, 1.0, 1.0]},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows_per_step} seeded query rows of one head per step, "
+                                   f"FP8 oracle (Max_offset = 8) on one thread"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_fp8(args, w):
     """The FP8 forward (fa_fwd_fp8) on the workload's shape: Q, K, V drawn as
     for the bf16 workload and cast to E4M3 (descales 1).  Peak: the measured
     bf16 peak x 2, the nominal FP8 / bf16 ratio of the tensor cores."""
     import online_softmax_sm_gb300 as fa
 
-    world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
-        if rank == 0:
-            print(json.dumps({"impl": "reference", "metric": FP8_METRIC,
-                              "unavailable": "the FP8 reference arm is not timed; the oracle's FP8 "
-                                             "steps are the parity reference in the tests"}), flush=True)
-        return
+        return run_fp8_reference(args, w)
+    world, rank, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
@@ -800,6 +881,13 @@ def run_fp8(args, w):
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv)),
                "d2h_bytes_per_step": ho.numel() * ho.element_size() + hl.numel() * hl.element_size(),
                "ms_per_step": e_ms}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s8 = fp8_oracle_sample(w, q, k, v, args.cpu_seconds)
+        cpu = {"value": s8["tflops"], "unit": "TFLOPS", "cores": s8["threads"], "kind": "oracle",
+               "sample": f"{s8['rows']} seeded query rows over {s8['heads']} heads ({s8['flops']:.3g} "
+                         f"FLOP, {s8['seconds']:.1f} s), FP8 oracle (Max_offset = 8) on one thread"}
+
     if rank == 0:
         line = {"metric": FP8_METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -809,7 +897,7 @@ def run_fp8(args, w):
                            "d": w.d, "causal": w.causal, "descales": [1.0, 1.0, 1.0],
                            "l2": "flushed before every timed step (512 MB write); inputs > L2",
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-                "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps, "clocks": sampler.summary(t_region0, t_region1),
                 "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms)}
         print(json.dumps(line), flush=True)
@@ -818,20 +906,118 @@ def run_fp8(args, w):
         dist.destroy_process_group()
 
 
+def oracle_bwd_tail(w: workloads.Workload, q, k, v, do, b: int, h: int, nq: int, threads: int) -> float:
+    """The oracle's backward for the last nq query rows of head (b, h) with
+    every key: under the bottom-right alignment those rows see the same keys
+    as in the whole problem.  Returns the oracle's wall time in seconds."""
+    import oracle
+
+    tail = slice(w.Nq - nq, w.Nq)
+    qh, dh = (x[b, h, tail].detach().cpu().double().numpy() for x in (q, do))
+    kh, vh = (x[b, h].detach().cpu().double().numpy() for x in (k, v))
+    t0 = time.perf_counter()
+    oracle.attention_bwd(qh, kh, vh, dh, w.scale, w.causal, window=w.window, threads=threads)
+    return time.perf_counter() - t0
+
+
+def bwd_tail_flops(w: workloads.Workload, nq: int) -> float:
+    """Algorithmic backward FLOPs of the last nq rows: 2.5 x the forward's."""
+    return 2.5 * row_flops(w, range(w.Nq - nq, w.Nq))
+
+
+def bwd_tail_rows(w: workloads.Workload, rate: float, seconds: float) -> int:
+    """Rows (from the end) whose backward the oracle runs in about `seconds`
+    at `rate` FLOP/s."""
+    lo, hi = 16, w.Nq
+    while lo < hi:  # the largest tail within the budget (FLOPs grow with the tail)
+        mid = (lo + hi + 1) // 2
+        if bwd_tail_flops(w, mid) <= rate * seconds:
+            lo = mid
+        else:
+            hi = mid - 1
+    return max(16, min(w.Nq, lo))
+
+
+def bwd_oracle_sample(w: workloads.Workload, q, k, v, do, target_s: float, seed: int = 0):
+    """Time the oracle's backward on a bounded sample: the last rows of seeded
+    heads, about target_s seconds on all host cores; returns a dict."""
+    import numpy as np
+
+    import oracle
+
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(seed)
+    calib = min(w.Nq, 64)
+    oracle_bwd_tail(w, q, k, v, do, 0, 0, 16, threads)  # loads the library
+    rate = bwd_tail_flops(w, calib) / max(oracle_bwd_tail(w, q, k, v, do, 0, 0, calib, threads), 1e-9)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    rng.shuffle(heads)
+    flops = elapsed = 0.0
+    rows = n_heads = 0
+    for b, h in heads:
+        if elapsed >= target_s:
+            break
+        nq = bwd_tail_rows(w, rate, target_s - elapsed)
+        elapsed += oracle_bwd_tail(w, q, k, v, do, b, h, nq, threads)
+        flops += bwd_tail_flops(w, nq)
+        rows += nq
+        n_heads += 1
+    return {"tflops": flops / elapsed / 1e12, "seconds": elapsed, "rows": rows, "heads": n_heads,
+            "threads": threads, "flops": flops}
+
+
+def run_bwd_reference(args, w):
+    """--impl reference for the backward: the fp64 oracle's gradients on the
+    host cores, each step the last rows of one seeded head (bounded so the
+    whole run takes about a minute)."""
+    world, rank, local = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    import oracle
+
+    threads = oracle.default_threads()
+    q, k, v = workloads.generate(w, device="cpu")
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    do = torch.randn(q.shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    per_step_s = min(3.0, 60.0 / max(1, args.steps + args.warmup))
+    calib = min(w.Nq, 64)
+    oracle_bwd_tail(w, q, k, v, do, 0, 0, 16, threads)  # loads the library
+    rate = bwd_tail_flops(w, calib) / max(oracle_bwd_tail(w, q, k, v, do, 0, 0, calib, threads), 1e-9)
+    nq = bwd_tail_rows(w, rate, per_step_s)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    for i in range(args.warmup):
+        b, h = heads[i % len(heads)]
+        oracle_bwd_tail(w, q, k, v, do, b, h, nq, threads)
+    total = 0.0
+    for i in range(args.steps):
+        b, h = heads[(args.warmup + i) % len(heads)]
+        total += oracle_bwd_tail(w, q, k, v, do, b, h, nq, threads)
+    flops = bwd_tail_flops(w, nq) * args.steps
+    value = flops / total / 1e12
+    line = {
+        "impl": "reference", "metric": BWD_METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name + ":bwd", "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": w.causal, "window": list(w.window) if w.window is not None else None},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": f"the last {nq} query rows of one head per step with every key "
+                                   f"({bwd_tail_flops(w, nq):.3g} FLOP), fp64 oracle gradients"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_bwd(args, w):
     """The attention backward: one fa_bwd call per step (row pass + dK/dV
     kernel + dQ kernel), O, LSE and dO resident.  Algorithmic FLOPs: the five
     products S, dP, dV, dK, dQ = 2.5 x the forward's."""
     import online_softmax_sm_gb300 as fa
 
-    world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
-        if rank == 0:
-            print(json.dumps({"impl": "reference", "metric": BWD_METRIC,
-                              "unavailable": "the backward reference arm is not timed; the oracle's "
-                                             "gradients are the parity reference in the tests"}),
-                  flush=True)
-        return
+        return run_bwd_reference(args, w)
+    world, rank, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
@@ -884,6 +1070,50 @@ def run_bwd(args, w):
                 "kernel": "fa_bwd_pre + fa_bwd_dkdv_kernel + fa_bwd_dq_kernel", "kernel_ms": ms_local,
                 "algorithmic_flops_per_launch": flops,
                 "peak_source": peak_src + " bf16_tflops (burst: one step timed alone)"}
+    # ---- end to end: Q, K, V, O, LSE, dO in from page-locked host memory,
+    # fa_bwd, dQ, dK, dV out, on one stream
+    e2e = None
+    if not args.no_e2e:
+        ins = (q, k, v, o, lse, do)
+        h_in = [x.cpu().pin_memory() for x in ins]
+        d_in = [torch.empty_like(x) for x in ins]
+        h_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dq, dk, dv)]
+        n_e2e = max(5, min(args.steps, 30))
+
+        def e2e_step():
+            for dst, src in zip(d_in, h_in):
+                dst.copy_(src, non_blocking=True)
+            fa.bwd(*d_in, w.scale, causal=w.causal, window=window, dq=dq, dk=dk, dv=dv)
+            for dst, src in zip(h_out, (dq, dk, dv)):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        tt = []
+        for _ in range(n_e2e):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            tt.append((a, b))
+        torch.cuda.synchronize(dev)
+        if fa.device_status(dev) != fa.FA_OK:
+            raise SystemExit("device status reports a timed-out wait")
+        e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in tt), world, dev)
+        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in h_in),
+               "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in h_out),
+               "ms_per_step": e_ms, "api": "pinned torch copies + fa_bwd, one stream, CUDA events"}
+        del d_in
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sb = bwd_oracle_sample(w, q, k, v, do, args.cpu_seconds)
+        cpu = {"value": sb["tflops"], "unit": "TFLOPS", "cores": sb["threads"], "kind": "oracle",
+               "sample": f"the last rows of {sb['heads']} seeded heads with every key ({sb['rows']} "
+                         f"rows, {sb['flops']:.3g} FLOP, {sb['seconds']:.1f} s), fp64 oracle gradients"}
+
     if rank == 0:
         line = {"metric": BWD_METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -894,7 +1124,7 @@ def run_bwd(args, w):
                            "window": list(w.window) if w.window is not None else None,
                            "l2": "flushed before every timed step (512 MB write); inputs > L2",
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-                "roofline": roofline, "cpu_baseline": None, "e2e": None,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": 3 * args.steps, "clocks": sampler.summary(t_region0, t_region1),
                 "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms)}
         print(json.dumps(line), flush=True)

@@ -57,3 +57,17 @@ def test_reference_arm_softmax_line(name):
     assert line["unit"] == "GB/s"
     _common(line, line["metric"], "GB/s", sw.name)
     assert "softmax" in line["metric"]
+
+
+def test_reference_arm_backward_line():
+    w = bench.workload_of("c1")
+    line = _run("--impl", "reference", "--workload", "c1:bwd", "--steps", "2", "--warmup", "1")
+    _common(line, bench.BWD_METRIC, "TFLOPS", w.name + ":bwd")
+
+
+def test_reference_arm_fp8_line():
+    name = "custom:1,2,256,256,128"
+    w = bench.workload_of(name)
+    line = _run("--impl", "reference", "--workload", name + ":fp8", "--steps", "2", "--warmup", "1")
+    _common(line, bench.FP8_METRIC, "TFLOPS", w.name + ":fp8")
+    assert line["cpu_baseline"]["cores"] == 1
