@@ -57,3 +57,43 @@ def test_backward_at_the_head_limit(qkv):
         f = lambda t: t[b, h].detach().cpu().double().numpy()
         _check_head(f(q), f(k), f(v), f(o), f(do), f(dq), f(dk), f(dv), w.scale, (-1, 0),
                     f"bwd B*H = 65535 head ({b}, {h})")
+
+
+def test_keys_past_4_gib_in_one_head():
+    """One head with Nk = 2^25 keys at d = 64: K and V hold 4 GiB each, so
+    every byte offset past the first 2^32 must be formed in 64 bits.  The
+    reference for sampled rows comes from the oracle over key chunks of 2^22,
+    combined with the oracle's merge rule (the rows see every key)."""
+    import numpy as np
+
+    import oracle
+
+    Nq, Nk, d = 128, 1 << 25, 64
+    w = workloads.custom(1, 1, Nq, Nk, d, seed=33)
+    q, k, v = workloads.generate(w, device="cuda")
+    rows = [0, 1, 31, 64, 100, 127]
+    qh = q[0, 0].cpu().double().numpy()
+    parts_o, parts_lse = [], []
+    chunk = 1 << 22
+    for c0 in range(0, Nk, chunk):
+        kc = k[0, 0, c0:c0 + chunk].cpu().double().numpy()
+        vc = v[0, 0, c0:c0 + chunk].cpu().double().numpy()
+        o_c, lse_c = oracle.attention(qh, kc, vc, w.scale, False, rows=rows)
+        parts_o.append(o_c)
+        parts_lse.append(lse_c)
+        del kc, vc
+    o_ref = np.empty((len(rows), d))
+    lse_ref = np.empty(len(rows))
+    for r in range(len(rows)):
+        # a chunk's (O, LSE) is the partial (m = LSE, l = 1, O) of the merge rule
+        m = np.array([p[r] for p in parts_lse])
+        _, _, o_r, lse_r = oracle.merge(m, np.ones_like(m), np.stack([p[r] for p in parts_o]))
+        o_ref[r], lse_ref[r] = o_r, lse_r
+    for n_splits in (1, 296):
+        o, lse = fa.fwd(q, k, v, w.scale, False, n_splits)
+        torch.cuda.synchronize()
+        assert fa.device_status() == fa.FA_OK
+        diff = P.Diff()
+        diff.add(o[0, 0, rows].float().cpu().double().numpy(), lse[0, 0, rows].cpu().double().numpy(),
+                 o_ref, lse_ref, bf16_output=True)
+        print(diff.check(f"Nk = 2^25, d = 64, {n_splits} split(s)"))
