@@ -97,3 +97,18 @@ def test_keys_past_4_gib_in_one_head():
         diff.add(o[0, 0, rows].float().cpu().double().numpy(), lse[0, 0, rows].cpu().double().numpy(),
                  o_ref, lse_ref, bf16_output=True)
         print(diff.check(f"Nk = 2^25, d = 64, {n_splits} split(s)"))
+
+
+def test_softmax_past_2_31_elements():
+    """2049 rows of 2^20 bf16 logits: 2^31 + 2^20 elements (4.3 GB); rows at
+    both ends and in the middle against the oracle's two-pass normaliser."""
+    from tests.test_softmax import _check
+
+    sw = workloads.SoftmaxWorkload("limit", 2049, 1 << 20, "bf16", seed=34)
+    x = workloads.generate_logits(sw, device="cuda")
+    y, lse = fa.softmax_rows(x)
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FA_OK
+    rows = torch.tensor([0, 1, 1024, 2047, 2048], device="cuda")
+    # only the sampled rows go to the host (the whole matrix in fp64 would be 17 GB)
+    _check(x[rows], y[rows], lse[rows], what="2049 x 2^20 bf16")
