@@ -35,16 +35,17 @@ def _e4m3_step(x):
     return np.where(x < 2.0 ** -6, 2.0 ** -9, np.exp2(e - 3))
 
 
-def _ambiguity(q, k, v, s_qk, vd, causal, block=128):
-    """Per row and column: sum over keys whose P' sits near a rounding
-    midpoint of (E4M3 step) |v| v_descale / (2^8 l)."""
+def _ambiguity(q, k, v, s_qk, vd, causal, block=128, rows=None):
+    """Per row (all, or the listed query rows) and column: sum over keys whose
+    P' sits near a rounding midpoint of (E4M3 step) |v| v_descale / (2^8 l)."""
     nq, nk = q.shape[0], k.shape[0]
-    s = s_qk * (q @ k.T)
+    r = np.arange(nq) if rows is None else np.asarray(rows)
+    s = s_qk * (q[r] @ k.T)
     if causal:
-        i = np.arange(nq)[:, None] + (nk - nq)
+        i = r[:, None] + (nk - nq)
         s = np.where(np.arange(nk)[None, :] <= i, s, -np.inf)
-    m_run = np.full((nq, nk), -np.inf)
-    m = np.full(nq, -np.inf)
+    m_run = np.full((len(r), nk), -np.inf)
+    m = np.full(len(r), -np.inf)
     for j0 in range(0, nk, block):
         m = np.maximum(m, s[:, j0:j0 + block].max(axis=1))
         m_run[:, j0:j0 + block] = m[:, None]
@@ -59,7 +60,8 @@ def _ambiguity(q, k, v, s_qk, vd, causal, block=128):
     with np.errstate(invalid="ignore"):
         l = np.where(np.isfinite(s), np.exp(s - m_fin), 0.0).sum(axis=1)
     # a P' against a running max m_r enters O with weight exp(m_r - m_fin) after rescaling
-    w = np.where(near, step * np.exp(np.where(np.isfinite(m_run), m_run - m_fin, 0.0)), 0.0)
+    with np.errstate(invalid="ignore"):  # rows with no visible key: -inf - (-inf), discarded
+        w = np.where(near, step * np.exp(np.where(np.isfinite(m_run), m_run - m_fin, 0.0)), 0.0)
     amb = (w @ np.abs(v)) * vd / (256.0 * np.where(l > 0, l, 1.0))[:, None]
     return amb
 
@@ -68,24 +70,27 @@ def _fp8(rng, shape, sd):
     return torch.tensor(rng.standard_normal(shape) * sd, dtype=torch.float32).to(torch.float8_e4m3fn)
 
 
-def _check(q8, k8, v8, o, lse, scale, qd, kd, vd, causal, what):
+def _check(q8, k8, v8, o, lse, scale, qd, kd, vd, causal, what, heads=None, rows=None):
+    """Every head and row, or the listed (b, h) heads and query rows."""
     B, H = q8.shape[:2]
-    for b in range(B):
-        for h in range(H):
-            q, k, v = (t[b, h].float().double().numpy() for t in (q8.cpu(), k8.cpu(), v8.cpu()))
-            o_ref, l_ref = oracle.attention_fp8(q, k, v, scale, qd, kd, vd, causal=causal)
-            og = o[b, h].cpu().double().numpy()
-            lg = lse[b, h].cpu().double().numpy()
-            empty = np.isneginf(l_ref)
-            assert np.all(og[empty] == 0) and np.all(np.isneginf(lg[empty])), what
-            amb = _ambiguity(q, k, v, scale * qd * kd, vd, causal)
-            tol = amb + P.half_ulp_bf16(o_ref) + 1e-4 * np.abs(o_ref).max(initial=0.0)
-            err = np.abs(og - o_ref)
-            bad = err > tol
-            assert not bad.any(), (f"{what} (b={b},h={h}): {bad.sum()} of {bad.size} out of bound, worst "
-                                   f"excess {(err - tol).max():.3e}, max|dO| {err.max():.3e}")
-            d = np.abs(lg[~empty] - l_ref[~empty])
-            assert d.max(initial=0.0) <= 1e-4, f"{what}: max|dLSE| {d.max():.3e}"
+    heads = heads or [(b, h) for b in range(B) for h in range(H)]
+    for b, h in heads:
+        q, k, v = (t[b, h].float().cpu().double().numpy() for t in (q8, k8, v8))
+        o_ref, l_ref = oracle.attention_fp8(q, k, v, scale, qd, kd, vd, causal=causal, rows=rows)
+        og = o[b, h].cpu().double().numpy()
+        lg = lse[b, h].cpu().double().numpy()
+        if rows is not None:
+            og, lg = og[rows], lg[rows]
+        empty = np.isneginf(l_ref)
+        assert np.all(og[empty] == 0) and np.all(np.isneginf(lg[empty])), what
+        amb = _ambiguity(q, k, v, scale * qd * kd, vd, causal, rows=rows)
+        tol = amb + P.half_ulp_bf16(o_ref) + 1e-4 * np.abs(o_ref).max(initial=0.0)
+        err = np.abs(og - o_ref)
+        bad = err > tol
+        assert not bad.any(), (f"{what} (b={b},h={h}): {bad.sum()} of {bad.size} out of bound, worst "
+                               f"excess {(err - tol).max():.3e}, max|dO| {err.max():.3e}")
+        d = np.abs(lg[~empty] - l_ref[~empty])
+        assert d.max(initial=0.0) <= 1e-4, f"{what}: max|dLSE| {d.max():.3e}"
 
 
 # B, H, Nq, Nk, causal, sd (value spread)
@@ -141,3 +146,20 @@ def test_fp8_rejects_other_head_dims():
     with pytest.raises(fa.FAError) as e:
         fa.fwd_fp8(q8, q8, q8, 0.125)
     assert e.value.code == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("name", ["c3", "c4"])
+def test_fp8_workload_sampled(name):
+    """The benchmark's FP8 launches: the bf16 workload cast to E4M3, descales
+    1, at full size; every tile's first and last row plus seeded extras of the
+    first and last head."""
+    from online_softmax_sm_gb300 import workloads
+
+    w = workloads.C3 if name == "c3" else workloads.C4
+    q8, k8, v8 = (t.to(torch.float8_e4m3fn) for t in workloads.generate(w, device="cuda"))
+    o, lse = fa.fwd_fp8(q8, k8, v8, w.scale, 1.0, 1.0, 1.0, w.causal)
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FA_OK
+    rows = P.sample_rows(w.Nq, extra=64, seed=5)
+    _check(q8, k8, v8, o, lse, w.scale, 1.0, 1.0, 1.0, w.causal, f"{w.name} fp8",
+           heads=[(0, 0), (w.B - 1, w.H - 1)], rows=rows)
