@@ -27,11 +27,13 @@ pytestmark = pytest.mark.gpu
 U = 2.0 ** -9
 
 
-def _masks(nq, nk, window):
+def _masks(nq, nk, window, r0=0, r1=None):
+    """Visible (query, key) pairs of query rows [r0, r1) (all by default)."""
     wl, wr = window
-    i = np.arange(nq)[:, None] + (nk - nq)
+    r1 = nq if r1 is None else r1
+    i = np.arange(r0, r1)[:, None] + (nk - nq)
     j = np.arange(nk)[None, :]
-    vis = np.ones((nq, nk), dtype=bool)
+    vis = np.ones((r1 - r0, nk), dtype=bool)
     if wl >= 0:
         vis &= j >= i - wl
     if wr >= 0:
@@ -39,23 +41,25 @@ def _masks(nq, nk, window):
     return vis
 
 
-def _check_head(q, k, v, o, do, dq, dk, dv, scale, window, what):
-    """One head, all elements; q, k, v, o, do, dq, dk, dv: CPU float64 numpy."""
+def _check_head(q, k, v, o, do, dq, dk, dv, scale, window, what, block=1024):
+    """One head, all elements; q, k, v, o, do, dq, dk, dv: CPU float64 numpy.
+    The bounds are summed over blocks of query rows, so the nq x nk
+    matrices never exist whole."""
     ref = oracle.attention_bwd(q, k, v, do, scale, window=window)
     nq, nk = q.shape[0], k.shape[0]
-    vis = _masks(nq, nk, window)
-    lse = ref["lse"][:, None]
-    live = np.isfinite(lse)
-    s = scale * (q @ k.T)
-    pm = np.where(vis & live, np.exp(np.where(vis & live, s - np.where(live, lse, 0.0), -np.inf)), 0.0)
-    dp = do @ v.T
-    ds = pm * (dp - ref["dd"][:, None])
     e = np.sum(np.abs(do) * np.abs(o), axis=1)
-    bounds = {
-        "dv": 2 * U * (pm.T @ np.abs(do)),
-        "dk": scale * 2 * U * (np.abs(ds).T @ np.abs(q) + (pm * e[:, None]).T @ np.abs(q)),
-        "dq": scale * 2 * U * (np.abs(ds) @ np.abs(k) + e[:, None] * (pm @ np.abs(k))),
-    }
+    bounds = {"dv": np.zeros_like(v), "dk": np.zeros_like(k), "dq": np.zeros_like(q)}
+    for r0 in range(0, nq, block):
+        r = slice(r0, min(nq, r0 + block))
+        vis = _masks(nq, nk, window, r.start, r.stop)
+        lse = ref["lse"][r, None]
+        live = np.isfinite(lse)
+        s = scale * (q[r] @ k.T)
+        pm = np.where(vis & live, np.exp(np.where(vis & live, s - np.where(live, lse, 0.0), -np.inf)), 0.0)
+        ds = pm * (do[r] @ v.T - ref["dd"][r, None])
+        bounds["dv"] += 2 * U * (pm.T @ np.abs(do[r]))
+        bounds["dk"] += scale * 2 * U * (np.abs(ds).T @ np.abs(q[r]) + (pm * e[r, None]).T @ np.abs(q[r]))
+        bounds["dq"][r] = scale * 2 * U * (np.abs(ds) @ np.abs(k) + e[r, None] * (pm @ np.abs(k)))
     for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
         r = ref[name]
         tol = bounds[name] + P.half_ulp_bf16(r) + 1e-6 * np.abs(r).max(initial=0.0)
@@ -134,6 +138,28 @@ def test_bwd_full_size_head():
     b, h = 1, 17
     _check_head(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), _np(o[b, h]), _np(do[b, h]), _np(dq[b, h]),
                 _np(dk[b, h]), _np(dv[b, h]), w.scale, (-1, -1), w.name)
+
+
+@pytest.mark.parametrize("name", ["c4", "local"])
+def test_bwd_full_size_head_causal_and_window(name):
+    """The causal N = 16384 shape and the 4096-key window on it, as the
+    benchmark runs them: one head of the full call, element by element."""
+    w = workloads.C4 if name == "c4" else workloads.LOCAL
+    window = w.window if w.window is not None else (-1, 0)
+    q, k, v = workloads.generate(w, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(78)
+    do = torch.randn(q.shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    if w.window is not None:
+        o, lse = fa.fwd_local(q, k, v, window[0], window[1], w.scale)
+    else:
+        o, lse = fa.fwd(q, k, v, w.scale, True)
+    dq, dk, dv = fa.bwd(q, k, v, o, lse, do, w.scale, causal=w.causal, window=w.window)
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FA_OK
+    b, h = 0, 21
+    _check_head(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), _np(o[b, h]), _np(do[b, h]), _np(dq[b, h]),
+                _np(dk[b, h]), _np(dv[b, h]), w.scale, window, w.name)
 
 
 @pytest.mark.parametrize("d", [64, 128])
