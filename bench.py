@@ -52,7 +52,7 @@ SOFTMAX_ALIASES = {"softmax_f32": workloads.SOFTMAX_F32,
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c3")
@@ -336,7 +336,7 @@ def run_reference(args, w):
     threads = oracle.default_threads()
     q, k, v = workloads.generate(w, device="cpu")
     rng = np.random.default_rng(1)
-    per_step_s = 3.0
+    per_step_s = min(3.0, 60.0 / max(1, args.steps + args.warmup))  # about a minute in all
     # calibrate rows per step
     qh, kh, vh = (x[0, 0].double().numpy() for x in (q, k, v))
     rows = sorted(rng.choice(w.Nq, size=min(w.Nq, 128), replace=False).tolist())
