@@ -463,27 +463,29 @@ def run_ours(args, w):
 
     # ---- end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e and w.window is None and w.n_splits == 1 and not w.bc:
-        # fa_fwd_host: the library's host-buffer call (page-locked in/out buffers,
-        # copies in, kernels and copies out pipelined over groups of heads); it
-        # returns when O and LSE are on the host, so the wall clock times it.
+    if not args.no_e2e and w.n_splits == 1 and not w.bc:
+        # fa_fwd_host (fa_fwd_local_host with a window): the library's host-buffer
+        # call (page-locked in/out buffers, copies in, kernels and copies out
+        # pipelined over groups of heads); it returns when O and LSE are on the
+        # host, so the wall clock times it.
         hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
         ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         n_e2e = max(5, min(args.steps, 30))
         for _ in range(2):
-            fa.fwd_host(hq, hk, hv, w.scale, w.causal, out=ho, lse=hl)
+            fa.fwd_host(hq, hk, hv, w.scale, w.causal, out=ho, lse=hl, window=w.window)
         tt = []
         for _ in range(n_e2e):
             t0 = time.perf_counter()
-            fa.fwd_host(hq, hk, hv, w.scale, w.causal, out=ho, lse=hl)
+            fa.fwd_host(hq, hk, hv, w.scale, w.causal, out=ho, lse=hl, window=w.window)
             tt.append((time.perf_counter() - t0) * 1e3)
         e_ms = max_over_ranks(statistics.mean(tt), world, dev)
         h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
         d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
         e2e = {"value": world * w.flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-               "api": "fa_fwd_host (C ABI, host buffers, wall clock)"}
+               "api": ("fa_fwd_host" if w.window is None else "fa_fwd_local_host")
+                      + " (C ABI, host buffers, wall clock)"}
     elif not args.no_e2e:
         hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
         ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()

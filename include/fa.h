@@ -114,6 +114,15 @@ int fa_fwd_local(const void* q, const void* k, const void* v, void* o, float* ls
                  void* stream);
 
 /*
+ * fa_fwd_local on HOST buffers: the mask of fa_fwd_local (window_left,
+ * window_right in [-1, 2^30]), the copies and head groups of fa_fwd_host, whose
+ * buffer, stream, blocking and error rules apply unchanged.
+ */
+int fa_fwd_local_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, float scale, int window_left, int window_right,
+                      int n_chunks);
+
+/*
  * Attention backward from the saved LSE ("Online Softmax 算法详解" section 8.3:
  * recompute S = Q K^T, restore P = exp(scale S - LSE) without a second online
  * softmax, then form the gradients).  With D_i = <dO_i, O_i>:

@@ -5,6 +5,7 @@ package is its Python binding plus the seeded workload generators:
 
   fwd(q, k, v, scale, causal, n_splits)   -> (o, lse)       fa_fwd / fa_fwd_ex
   fwd_host(q, k, v, scale, causal)        -> (o, lse)       fa_fwd_host (CPU tensors, copies included)
+  fwd_host(..., window=(wl, wr))          -> (o, lse)       fa_fwd_local_host
   fwd_local(q, k, v, wl, wr, ...)         -> (o, lse)       fa_fwd_local (sliding window)
   fwd_fp8(q8, k8, v8, ...)                -> (o, lse)       fa_fwd_fp8 (E4M3, Max_offset 8)
   fwd_partial(q, k, v, n_splits, ...)     -> (m, l, o) parts fa_fwd_partial

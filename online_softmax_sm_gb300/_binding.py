@@ -70,6 +70,8 @@ def _declare(L):
     L.fa_fwd_local.restype = _i
     L.fa_fwd_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i]
     L.fa_fwd_host.restype = _i
+    L.fa_fwd_local_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _i]
+    L.fa_fwd_local_host.restype = _i
     L.fa_softmax_rows.argtypes = [_vp, _vp, _vp, ctypes.c_longlong, _i, _i, _vp]
     L.fa_softmax_rows.restype = _i
     L.fa_fwd_fp8.argtypes = [_vp] * 5 + [_i] * 5 + [ctypes.c_float] * 4 + [_i, _vp]
@@ -159,10 +161,11 @@ def fwd(q, k, v, scale: float | None = None, causal: bool = False, n_splits: int
 
 
 def fwd_host(q, k, v, scale: float | None = None, causal: bool = False, out=None, lse=None,
-             n_chunks: int = 0, device=None):
+             n_chunks: int = 0, device=None, window=None):
     """fa_fwd_host: q, k, v are CPU bf16 [B, H, N, d] tensors (page-locked for overlap); the
     call copies them to the device, runs the forward there and copies O and LSE back into
-    CPU tensors.  Returns (o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq]) on the CPU."""
+    CPU tensors.  Returns (o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq]) on the CPU.
+    window=(window_left, window_right) selects fa_fwd_local_host (the mask of fwd_local)."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
             raise ValueError(f"{name} must be a CPU tensor")
@@ -183,9 +186,14 @@ def fwd_host(q, k, v, scale: float | None = None, causal: bool = False, out=None
     if lse.device.type != "cpu" or lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous CPU float32 [B, H, Nq] tensor")
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
-        rc = lib().fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                               B, H, Nq, Nk, d, float(scale), int(bool(causal)), int(n_chunks))
-    _check(rc, "fa_fwd_host")
+        if window is None:
+            rc = lib().fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                   B, H, Nq, Nk, d, float(scale), int(bool(causal)), int(n_chunks))
+        else:
+            rc = lib().fa_fwd_local_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                         lse.data_ptr(), B, H, Nq, Nk, d, float(scale), int(window[0]),
+                                         int(window[1]), int(n_chunks))
+    _check(rc, "fa_fwd_host" if window is None else "fa_fwd_local_host")
     return out, lse
 
 

@@ -289,11 +289,13 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
                   nullptr, nullptr, nullptr, nullptr);
 }
 
-int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                int Nq, int Nk, int d, float scale, int causal, int n_chunks) {
+// fa_fwd_host / fa_fwd_local_host: the forward with mask (wl, wr) on host buffers.
+static int fwd_host_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                         int Nq, int Nk, int d, float scale, int wl, int wr, int n_chunks) {
   int rc = check_sizes(B, H, Nq, Nk, d, scale);
   if (rc != FA_OK) return rc;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (wl < -1 || wr < -1 || wl > kMaxSeq || wr > kMaxSeq) return FA_ERR_INVALID_ARG;
   DevState* dev = nullptr;
   if ((rc = device_state(&dev)) != FA_OK) return rc;
   int dev_id = 0;
@@ -350,7 +352,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_run, hp.in_done[c], 0);
     if (e != cudaSuccess) break;
     rc = fwd_impl(dq + h0 * q_head, dk + h0 * kv_head, dv + h0 * kv_head, dout + h0 * q_head,
-                  dl + static_cast<size_t>(h0) * Nq, 1, nh, Nq, Nk, d, scale, -1, causal ? 0 : -1, 1,
+                  dl + static_cast<size_t>(h0) * Nq, 1, nh, Nq, Nk, d, scale, wl, wr, 1,
                   hp.s_run, nullptr, nullptr, nullptr, nullptr);
     if (rc != FA_OK) break;
     e = cudaEventRecord(hp.run_done[c], hp.s_run);
@@ -372,6 +374,17 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
   if (er != cudaSuccess) return cuda_fail(er);
   if (eo != cudaSuccess) return cuda_fail(eo);
   return fa_get_device_status(hp.s_out);
+}
+
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Nq, int Nk, int d, float scale, int causal, int n_chunks) {
+  return fwd_host_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, -1, causal ? 0 : -1, n_chunks);
+}
+
+int fa_fwd_local_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, float scale, int window_left, int window_right,
+                      int n_chunks) {
+  return fwd_host_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, window_left, window_right, n_chunks);
 }
 
 int fa_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

@@ -91,6 +91,10 @@ def test_invalid_options_and_partial_and_merge_args(L):
     assert L.fa_fwd_host(0x1000, 0x1000, 0x1000, 0x1000, None, 1, 1, 8, 8, 64, 0.125, 0, 0) == fa.FA_ERR_INVALID_ARG
     assert L.fa_fwd_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0, 1, 8, 8, 64, 0.125, 0, 0) == fa.FA_ERR_INVALID_ARG
     assert L.fa_fwd_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 96, 0.125, 0, 0) == fa.FA_ERR_UNSUPPORTED
+    # fa_fwd_local_host: also the window bounds
+    assert L.fa_fwd_local_host(None, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 64, 0.125, 4, 0, 0) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_local_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 64, 0.125, -2, 0, 0) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_local_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 64, 0.125, 4, (1 << 30) + 1, 0) == fa.FA_ERR_INVALID_ARG
 
 
 def test_product_path_fails_loudly_without_library(tmp_path, monkeypatch):

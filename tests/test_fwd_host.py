@@ -66,3 +66,15 @@ def test_fwd_host_rejects_bad_arguments():
     rc = fa.lib().fa_fwd_host(None, q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(),
                               1, 1, 128, 128, 128, 0.1, 0, 0)
     assert rc == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("window,n_chunks", [((64, 0), 3), ((200, 50), 0), ((-1, 0), 2)])
+def test_fwd_local_host_matches_device_call(window, n_chunks):
+    """fa_fwd_local_host against fa_fwd_local: the same kernel per head group."""
+    w = workloads.custom(1, 4, 300, 500, 128, seed=7, q_mult=2.0)
+    q, k, v = workloads.generate(w, device="cuda")
+    o_ref, lse_ref = fa.fwd_local(q, k, v, window[0], window[1], w.scale)
+    torch.cuda.synchronize()
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    o, lse = fa.fwd_host(hq, hk, hv, w.scale, n_chunks=n_chunks, window=window)
+    assert torch.equal(o, o_ref.cpu()) and torch.equal(lse, lse_ref.cpu())
