@@ -168,6 +168,16 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                int Nq, int Nk, int d, float scale, float q_descale, float k_descale,
                float v_descale, int causal, void* stream);
 
+/*
+ * fa_fwd_fp8 on HOST buffers: E4M3 Q, K, V (one byte per element) in, bf16 O
+ * and fp32 LSE out, with the copies and head groups of fa_fwd_host, whose
+ * buffer, stream, blocking and error rules apply unchanged.  Arguments as
+ * fa_fwd_fp8 (d = 128; descales finite and > 0, checked before any copy).
+ */
+int fa_fwd_fp8_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                    int Nq, int Nk, int d, float scale, float q_descale, float k_descale,
+                    float v_descale, int causal, int n_chunks);
+
 /* Options for fa_fwd_ex.  Zero-initialise, then set what you need. */
 typedef struct fa_opts {
   int bc;                     /* K/V tile rows: 0 = default (128), or 64 or 128 */

@@ -72,6 +72,8 @@ def _declare(L):
     L.fa_fwd_host.restype = _i
     L.fa_fwd_local_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _i]
     L.fa_fwd_local_host.restype = _i
+    L.fa_fwd_fp8_host.argtypes = [_vp] * 5 + [_i] * 5 + [ctypes.c_float] * 4 + [_i, _i]
+    L.fa_fwd_fp8_host.restype = _i
     L.fa_softmax_rows.argtypes = [_vp, _vp, _vp, ctypes.c_longlong, _i, _i, _vp]
     L.fa_softmax_rows.restype = _i
     L.fa_fwd_fp8.argtypes = [_vp] * 5 + [_i] * 5 + [ctypes.c_float] * 4 + [_i, _vp]
@@ -235,6 +237,38 @@ def fwd_fp8(q8, k8, v8, scale: float | None = None, q_descale: float = 1.0, k_de
                               B, H, Nq, Nk, d, float(scale), float(q_descale), float(k_descale),
                               float(v_descale), int(bool(causal)), _stream_handle(q8.device, stream))
     _check(rc, "fa_fwd_fp8")
+    return out, lse
+
+
+def fwd_fp8_host(q8, k8, v8, scale: float | None = None, q_descale: float = 1.0, k_descale: float = 1.0,
+                 v_descale: float = 1.0, causal: bool = False, out=None, lse=None, n_chunks: int = 0,
+                 device=None):
+    """fa_fwd_fp8_host: q8, k8, v8 CPU float8_e4m3fn [B, H, N, 128] tensors (page-locked for
+    overlap); copies in, the FP8 forward, O (bf16) and LSE (fp32) back into CPU tensors."""
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+        if t.dtype != torch.float8_e4m3fn or t.dim() != 4:
+            raise ValueError(f"{name} must be a float8_e4m3fn [B, H, N, d] tensor")
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    if k8.shape != (B, H, Nk, d) or v8.shape != k8.shape:
+        raise ValueError("k8 and v8 must be [B, H, Nk, d] matching q8")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, pin_memory=q8.is_pinned())
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=q8.is_pinned())
+    if out.device.type != "cpu" or out.shape != (B, H, Nq, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CPU bfloat16 [B, H, Nq, d] tensor")
+    if lse.device.type != "cpu" or lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous CPU float32 [B, H, Nq] tensor")
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        rc = lib().fa_fwd_fp8_host(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(),
+                                   lse.data_ptr(), B, H, Nq, Nk, d, float(scale), float(q_descale),
+                                   float(k_descale), float(v_descale), int(bool(causal)), int(n_chunks))
+    _check(rc, "fa_fwd_fp8_host")
     return out, lse
 
 

@@ -289,13 +289,21 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
                   nullptr, nullptr, nullptr, nullptr);
 }
 
-// fa_fwd_host / fa_fwd_local_host: the forward with mask (wl, wr) on host buffers.
+// fa_fwd_host / fa_fwd_local_host / fa_fwd_fp8_host: the forward with mask
+// (wl, wr) on host buffers; fp8 = the three descales of the E4M3 forward (one
+// byte per Q, K, V element; O stays bf16), or nullptr for bf16.
 static int fwd_host_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                         int Nq, int Nk, int d, float scale, int wl, int wr, int n_chunks) {
+                         int Nq, int Nk, int d, float scale, int wl, int wr, int n_chunks,
+                         const float* fp8) {
   int rc = check_sizes(B, H, Nq, Nk, d, scale);
   if (rc != FA_OK) return rc;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (wl < -1 || wr < -1 || wl > kMaxSeq || wr > kMaxSeq) return FA_ERR_INVALID_ARG;
+  if (fp8) {
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    for (int i = 0; i < 3; ++i)
+      if (!std::isfinite(fp8[i]) || !(fp8[i] > 0.f)) return FA_ERR_INVALID_ARG;
+  }
   DevState* dev = nullptr;
   if ((rc = device_state(&dev)) != FA_OK) return rc;
   int dev_id = 0;
@@ -306,10 +314,11 @@ static int fwd_host_impl(const void* q, const void* k, const void* v, void* o, f
   if ((rc = host_pipe_init(hp)) != FA_OK) return rc;
 
   const int BH = B * H;
-  const size_t q_head = static_cast<size_t>(Nq) * d * 2, kv_head = static_cast<size_t>(Nk) * d * 2;
-  const size_t lse_head = static_cast<size_t>(Nq) * 4;
+  const size_t in_es = fp8 ? 1 : 2;  // bytes per Q, K, V element
+  const size_t q_head = static_cast<size_t>(Nq) * d * in_es, kv_head = static_cast<size_t>(Nk) * d * in_es;
+  const size_t o_head = static_cast<size_t>(Nq) * d * 2, lse_head = static_cast<size_t>(Nq) * 4;
   const size_t off_k = align256(BH * q_head), off_v = off_k + align256(BH * kv_head);
-  const size_t off_o = off_v + align256(BH * kv_head), off_l = off_o + align256(BH * q_head);
+  const size_t off_o = off_v + align256(BH * kv_head), off_l = off_o + align256(BH * o_head);
   const size_t need = off_l + align256(BH * lse_head);
   if (need > hp.cap) {
     if (hp.buf && (e = cudaFree(hp.buf)) != cudaSuccess) return cuda_fail(e);
@@ -351,14 +360,19 @@ static int fwd_host_impl(const void* q, const void* k, const void* v, void* o, f
     if (e == cudaSuccess) e = cudaEventRecord(hp.in_done[c], si);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_run, hp.in_done[c], 0);
     if (e != cudaSuccess) break;
-    rc = fwd_impl(dq + h0 * q_head, dk + h0 * kv_head, dv + h0 * kv_head, dout + h0 * q_head,
-                  dl + static_cast<size_t>(h0) * Nq, 1, nh, Nq, Nk, d, scale, wl, wr, 1,
-                  hp.s_run, nullptr, nullptr, nullptr, nullptr);
+    if (fp8)
+      rc = fa_fwd_fp8(dq + h0 * q_head, dk + h0 * kv_head, dv + h0 * kv_head, dout + h0 * o_head,
+                      dl + static_cast<size_t>(h0) * Nq, 1, nh, Nq, Nk, d, scale, fp8[0], fp8[1], fp8[2],
+                      wr == 0 ? 1 : 0, hp.s_run);
+    else
+      rc = fwd_impl(dq + h0 * q_head, dk + h0 * kv_head, dv + h0 * kv_head, dout + h0 * o_head,
+                    dl + static_cast<size_t>(h0) * Nq, 1, nh, Nq, Nk, d, scale, wl, wr, 1,
+                    hp.s_run, nullptr, nullptr, nullptr, nullptr);
     if (rc != FA_OK) break;
     e = cudaEventRecord(hp.run_done[c], hp.s_run);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_out, hp.run_done[c], 0);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(ho + h0 * q_head, dout + h0 * q_head, nh * q_head, cudaMemcpyDeviceToHost,
+      e = cudaMemcpyAsync(ho + h0 * o_head, dout + h0 * o_head, nh * o_head, cudaMemcpyDeviceToHost,
                           hp.s_out);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(lse + static_cast<size_t>(h0) * Nq, dl + static_cast<size_t>(h0) * Nq,
@@ -378,13 +392,21 @@ static int fwd_host_impl(const void* q, const void* k, const void* v, void* o, f
 
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int Nq, int Nk, int d, float scale, int causal, int n_chunks) {
-  return fwd_host_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, -1, causal ? 0 : -1, n_chunks);
+  return fwd_host_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, -1, causal ? 0 : -1, n_chunks, nullptr);
 }
 
 int fa_fwd_local_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                       int H, int Nq, int Nk, int d, float scale, int window_left, int window_right,
                       int n_chunks) {
-  return fwd_host_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, window_left, window_right, n_chunks);
+  return fwd_host_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, window_left, window_right, n_chunks,
+                       nullptr);
+}
+
+int fa_fwd_fp8_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                    int Nq, int Nk, int d, float scale, float q_descale, float k_descale,
+                    float v_descale, int causal, int n_chunks) {
+  const float ds[3] = {q_descale, k_descale, v_descale};
+  return fwd_host_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, -1, causal ? 0 : -1, n_chunks, ds);
 }
 
 int fa_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

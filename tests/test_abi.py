@@ -95,6 +95,10 @@ def test_invalid_options_and_partial_and_merge_args(L):
     assert L.fa_fwd_local_host(None, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 64, 0.125, 4, 0, 0) == fa.FA_ERR_INVALID_ARG
     assert L.fa_fwd_local_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 64, 0.125, -2, 0, 0) == fa.FA_ERR_INVALID_ARG
     assert L.fa_fwd_local_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 64, 0.125, 4, (1 << 30) + 1, 0) == fa.FA_ERR_INVALID_ARG
+    # fa_fwd_fp8_host: d = 128 only, descales finite and > 0
+    assert L.fa_fwd_fp8_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 64, 0.125, 1.0, 1.0, 1.0, 0, 0) == fa.FA_ERR_UNSUPPORTED
+    assert L.fa_fwd_fp8_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 128, 0.125, 0.0, 1.0, 1.0, 0, 0) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_fp8_host(None, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 128, 0.125, 1.0, 1.0, 1.0, 0, 0) == fa.FA_ERR_INVALID_ARG
 
 
 def test_product_path_fails_loudly_without_library(tmp_path, monkeypatch):

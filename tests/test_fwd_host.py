@@ -78,3 +78,15 @@ def test_fwd_local_host_matches_device_call(window, n_chunks):
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     o, lse = fa.fwd_host(hq, hk, hv, w.scale, n_chunks=n_chunks, window=window)
     assert torch.equal(o, o_ref.cpu()) and torch.equal(lse, lse_ref.cpu())
+
+
+@pytest.mark.parametrize("causal,n_chunks", [(False, 3), (True, 0)])
+def test_fwd_fp8_host_matches_device_call(causal, n_chunks):
+    """fa_fwd_fp8_host against fa_fwd_fp8 (one-byte inputs, bf16 O)."""
+    w = workloads.custom(2, 3, 384, 300, 128, seed=8)
+    q8, k8, v8 = (t.to(torch.float8_e4m3fn) for t in workloads.generate(w, device="cuda"))
+    o_ref, lse_ref = fa.fwd_fp8(q8, k8, v8, w.scale, 0.5, 1.0, 2.0, causal)
+    torch.cuda.synchronize()
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q8, k8, v8))
+    o, lse = fa.fwd_fp8_host(hq, hk, hv, w.scale, 0.5, 1.0, 2.0, causal, n_chunks=n_chunks)
+    assert torch.equal(o, o_ref.cpu()) and torch.equal(lse, lse_ref.cpu())
