@@ -152,6 +152,19 @@ int fa_bwd_local(const void* q, const void* k, const void* v, const void* o, con
                  int d, float scale, int window_left, int window_right, void* stream);
 
 /*
+ * fa_bwd / fa_bwd_local on HOST buffers: q, k, v, o, lse, dout in and dq, dk,
+ * dv out are host arrays (layouts as fa_bwd), copied through the head-group
+ * pipeline of fa_fwd_host, whose buffer, stream, blocking and error rules apply
+ * unchanged.  fa_bwd_local_host takes the window of fa_fwd_local.
+ */
+int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                float scale, int causal, int n_chunks);
+int fa_bwd_local_host(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
+                      int d, float scale, int window_left, int window_right, int n_chunks);
+
+/*
  * FP8 (E4M3) attention forward with Max_offset = 8 ("Online Softmax 算法详解"
  * section 6).  q, k, v hold E4M3 bytes (bf16 layout, one byte per element);
  * their real values are q * q_descale, k * k_descale, v * v_descale.  The

@@ -82,6 +82,10 @@ def _declare(L):
     L.fa_bwd.restype = _i
     L.fa_bwd_local.argtypes = [_vp] * 9 + [_i] * 5 + [ctypes.c_float, _i, _i, _vp]
     L.fa_bwd_local.restype = _i
+    L.fa_bwd_host.argtypes = [_vp] * 9 + [_i] * 5 + [ctypes.c_float, _i, _i]
+    L.fa_bwd_host.restype = _i
+    L.fa_bwd_local_host.argtypes = [_vp] * 9 + [_i] * 5 + [ctypes.c_float, _i, _i, _i]
+    L.fa_bwd_local_host.restype = _i
 
 
 def lib():
@@ -296,6 +300,42 @@ def bwd(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False,
         else:
             rc = lib().fa_bwd_local(*args, int(window[0]), int(window[1]), sh)
     _check(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def bwd_host(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False, window=None,
+             dq=None, dk=None, dv=None, n_chunks: int = 0, device=None):
+    """fa_bwd_host / fa_bwd_local_host: every tensor on the CPU (page-locked for overlap); the
+    call copies the inputs to the device, runs the backward and copies dq, dk, dv back."""
+    ts = {"q": q, "k": k, "v": v, "o": o, "dout": dout}
+    for name, t in ts.items():
+        if not isinstance(t, torch.Tensor) or t.device.type != "cpu" or t.dtype != torch.bfloat16 \
+                or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU bfloat16 [B, H, N, d] tensor")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("shapes: q, o, dout [B, H, Nq, d]; k, v [B, H, Nk, d]")
+    if (not isinstance(lse, torch.Tensor) or lse.device.type != "cpu" or lse.shape != (B, H, Nq)
+            or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous CPU float32 [B, H, Nq] tensor")
+    if scale is None:
+        scale = d ** -0.5
+    pin = q.is_pinned()
+    dq = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=torch.bfloat16, pin_memory=pin) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=torch.bfloat16, pin_memory=pin) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t.device.type != "cpu" or t.shape != ref.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU bfloat16 tensor shaped like its input")
+    args = [q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, float(scale)]
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        if window is None:
+            rc = lib().fa_bwd_host(*args, int(bool(causal)), int(n_chunks))
+        else:
+            rc = lib().fa_bwd_local_host(*args, int(window[0]), int(window[1]), int(n_chunks))
+    _check(rc, "fa_bwd_host")
     return dq, dk, dv
 
 

@@ -579,6 +579,100 @@ int fa_bwd_local(const void* q, const void* k, const void* v, const void* o, con
                   window_right, stream);
 }
 
+// fa_bwd_host / fa_bwd_local_host: the backward on host buffers, through the
+// head-group pipeline of fa_fwd_host (six copies in, the backward, three out).
+static int bwd_host_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
+                         int d, float scale, int wl, int wr, int n_chunks) {
+  int rc = check_sizes(B, H, Nq, Nk, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (wl < -1 || wr < -1 || wl > kMaxSeq || wr > kMaxSeq) return FA_ERR_INVALID_ARG;
+  DevState* dev = nullptr;
+  if ((rc = device_state(&dev)) != FA_OK) return rc;
+  int dev_id = 0;
+  cudaError_t e = cudaGetDevice(&dev_id);
+  if (e != cudaSuccess) return cuda_fail(e);
+  HostPipe& hp = g_pipe[dev_id];
+  std::lock_guard<std::mutex> lock(hp.mu);
+  if ((rc = host_pipe_init(hp)) != FA_OK) return rc;
+
+  const int BH = B * H;
+  // per head: bytes of each array, in the order in[] / out[] list them
+  const size_t q_head = static_cast<size_t>(Nq) * d * 2, kv_head = static_cast<size_t>(Nk) * d * 2;
+  const size_t lse_head = static_cast<size_t>(Nq) * 4;
+  const size_t in_head[6] = {q_head, kv_head, kv_head, q_head, q_head, lse_head};  // q k v o dout lse
+  const size_t out_head[3] = {q_head, kv_head, kv_head};                            // dq dk dv
+  size_t off_in[6], off_out[3], need = 0;
+  for (int a = 0; a < 6; ++a) off_in[a] = need, need += align256(BH * in_head[a]);
+  for (int a = 0; a < 3; ++a) off_out[a] = need, need += align256(BH * out_head[a]);
+  if (need > hp.cap) {
+    if (hp.buf && (e = cudaFree(hp.buf)) != cudaSuccess) return cuda_fail(e);
+    hp.buf = nullptr;
+    hp.cap = 0;
+    if ((e = cudaMalloc(&hp.buf, need)) != cudaSuccess) {
+      t_last_cuda = e;
+      return FA_ERR_NO_MEMORY;
+    }
+    hp.cap = need;
+  }
+  const char* h_in[6] = {static_cast<const char*>(q), static_cast<const char*>(k),
+                         static_cast<const char*>(v), static_cast<const char*>(o),
+                         static_cast<const char*>(dout), reinterpret_cast<const char*>(lse)};
+  char* h_out[3] = {static_cast<char*>(dq), static_cast<char*>(dk), static_cast<char*>(dv)};
+
+  int chunks = n_chunks <= 0 ? (BH < 8 ? BH : 8) : n_chunks;
+  if (chunks > BH) chunks = BH;
+  if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;
+  const int per = (BH + chunks - 1) / chunks;
+  for (int c = 0; c < chunks && rc == FA_OK && e == cudaSuccess; ++c) {
+    const int h0 = c * per, nh = (BH - h0 < per) ? BH - h0 : per;
+    if (nh <= 0) break;
+    char* d_in[6];
+    char* d_out[3];
+    for (int a = 0; a < 6; ++a) d_in[a] = hp.buf + off_in[a] + h0 * in_head[a];
+    for (int a = 0; a < 3; ++a) d_out[a] = hp.buf + off_out[a] + h0 * out_head[a];
+    for (int a = 0; a < 6 && e == cudaSuccess; ++a)
+      e = cudaMemcpyAsync(d_in[a], h_in[a] + h0 * in_head[a], nh * in_head[a], cudaMemcpyHostToDevice,
+                          hp.s_in);
+    if (e == cudaSuccess) e = cudaEventRecord(hp.in_done[c], hp.s_in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_run, hp.in_done[c], 0);
+    if (e != cudaSuccess) break;
+    rc = bwd_impl(d_in[0], d_in[1], d_in[2], d_in[3], reinterpret_cast<const float*>(d_in[5]), d_in[4],
+                  d_out[0], d_out[1], d_out[2], 1, nh, Nq, Nk, d, scale, wl, wr, hp.s_run);
+    if (rc != FA_OK) break;
+    e = cudaEventRecord(hp.run_done[c], hp.s_run);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_out, hp.run_done[c], 0);
+    for (int a = 0; a < 3 && e == cudaSuccess; ++a)
+      e = cudaMemcpyAsync(h_out[a] + h0 * out_head[a], d_out[a], nh * out_head[a], cudaMemcpyDeviceToHost,
+                          hp.s_out);
+  }
+  // drain all three streams whatever happened above
+  cudaError_t es = cudaStreamSynchronize(hp.s_in);
+  cudaError_t er = cudaStreamSynchronize(hp.s_run);
+  cudaError_t eo = cudaStreamSynchronize(hp.s_out);
+  if (rc != FA_OK) return rc;
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (es != cudaSuccess) return cuda_fail(es);
+  if (er != cudaSuccess) return cuda_fail(er);
+  if (eo != cudaSuccess) return cuda_fail(eo);
+  return fa_get_device_status(hp.s_out);
+}
+
+int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                float scale, int causal, int n_chunks) {
+  return bwd_host_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, -1, causal ? 0 : -1,
+                       n_chunks);
+}
+
+int fa_bwd_local_host(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
+                      int d, float scale, int window_left, int window_right, int n_chunks) {
+  return bwd_host_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, window_left,
+                       window_right, n_chunks);
+}
+
 int fa_softmax_rows(const void* x, void* y, float* lse, long long rows, int cols, int dtype,
                     void* stream) {
   if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;

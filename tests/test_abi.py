@@ -99,6 +99,11 @@ def test_invalid_options_and_partial_and_merge_args(L):
     assert L.fa_fwd_fp8_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 64, 0.125, 1.0, 1.0, 1.0, 0, 0) == fa.FA_ERR_UNSUPPORTED
     assert L.fa_fwd_fp8_host(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 128, 0.125, 0.0, 1.0, 1.0, 0, 0) == fa.FA_ERR_INVALID_ARG
     assert L.fa_fwd_fp8_host(None, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 8, 8, 128, 0.125, 1.0, 1.0, 1.0, 0, 0) == fa.FA_ERR_INVALID_ARG
+    # fa_bwd_host / fa_bwd_local_host: null pointers, sizes, window bounds
+    P9 = [0x1000] * 9
+    assert L.fa_bwd_host(*([None] + P9[1:]), 1, 1, 8, 8, 64, 0.125, 0, 0) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_bwd_host(*P9, 1, 1, 8, 8, 96, 0.125, 0, 0) == fa.FA_ERR_UNSUPPORTED
+    assert L.fa_bwd_local_host(*P9, 1, 1, 8, 8, 64, 0.125, -3, 0, 0) == fa.FA_ERR_INVALID_ARG
 
 
 def test_product_path_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -90,3 +90,24 @@ def test_fwd_fp8_host_matches_device_call(causal, n_chunks):
     hq, hk, hv = (t.cpu().pin_memory() for t in (q8, k8, v8))
     o, lse = fa.fwd_fp8_host(hq, hk, hv, w.scale, 0.5, 1.0, 2.0, causal, n_chunks=n_chunks)
     assert torch.equal(o, o_ref.cpu()) and torch.equal(lse, lse_ref.cpu())
+
+
+@pytest.mark.parametrize("window,n_chunks", [(None, 3), ((-1, 0), 0), ((100, 0), 4)])
+def test_bwd_host_matches_device_call(window, n_chunks):
+    """fa_bwd_host / fa_bwd_local_host against fa_bwd on the device (no atomics,
+    heads independent: equal bit for bit for any grouping)."""
+    w = workloads.custom(1, 5, 300, 260, 128, seed=9)
+    q, k, v = workloads.generate(w, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(10)
+    do = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    if window is None:
+        o, lse = fa.fwd(q, k, v, w.scale)
+    else:
+        o, lse = fa.fwd_local(q, k, v, window[0], window[1], w.scale)
+    ref = fa.bwd(q, k, v, o, lse, do, w.scale, window=window)
+    torch.cuda.synchronize()
+    h = [t.cpu().pin_memory() for t in (q, k, v, o, lse, do)]
+    got = fa.bwd_host(*h, w.scale, window=window, n_chunks=n_chunks)
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b.cpu())
