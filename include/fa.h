@@ -200,6 +200,9 @@ typedef struct fa_opts {
                                  of every CTA skip its n-th K/V tile load, so
                                  the consumer's wait runs out and the call
                                  reports FA_ERR_DEVICE_TIMEOUT */
+  int max_ctas;               /* 0 = one CTA per SM; n > 0: n CTAs (at most
+                                 one per work item; beyond one per SM they run
+                                 in waves).  Same results for every n */
 } fa_opts;
 
 /* fa_fwd with options; opts may be NULL (same as fa_fwd). */

@@ -30,7 +30,8 @@ NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 class FaOpts(ctypes.Structure):
     _fields_ = [("bc", ctypes.c_int), ("q_tiles_per_cta", ctypes.c_int),
-                ("timeout_ns", ctypes.c_ulonglong), ("test_skip_kv_load", ctypes.c_int)]
+                ("timeout_ns", ctypes.c_ulonglong), ("test_skip_kv_load", ctypes.c_int),
+                ("max_ctas", ctypes.c_int)]
 
 
 class FAError(RuntimeError):
@@ -141,7 +142,7 @@ def _check_qkv(q, k, v):
 
 def fwd(q, k, v, scale: float | None = None, causal: bool = False, n_splits: int = 1,
         out=None, lse=None, bc: int = 0, q_tiles_per_cta: int = 0, timeout_ns: int = 0,
-        test_skip_kv_load: int = 0, stream=None):
+        test_skip_kv_load: int = 0, max_ctas: int = 0, stream=None):
     """fa_fwd / fa_fwd_ex.  Returns (o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq])."""
     B, H, Nq, Nk, d = _check_qkv(q, k, v)
     if scale is None:
@@ -157,8 +158,9 @@ def fwd(q, k, v, scale: float | None = None, causal: bool = False, n_splits: int
         sh = _stream_handle(q.device, stream)
         args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                 B, H, Nq, Nk, d, float(scale), int(bool(causal)), int(n_splits), sh)
-        if bc or q_tiles_per_cta or timeout_ns or test_skip_kv_load:
-            opts = FaOpts(int(bc), int(q_tiles_per_cta), int(timeout_ns), int(test_skip_kv_load))
+        if bc or q_tiles_per_cta or timeout_ns or test_skip_kv_load or max_ctas:
+            opts = FaOpts(int(bc), int(q_tiles_per_cta), int(timeout_ns), int(test_skip_kv_load),
+                          int(max_ctas))
             rc = L.fa_fwd_ex(*args, ctypes.byref(opts))
         else:
             rc = L.fa_fwd(*args)

@@ -1,5 +1,6 @@
 // fa_api.cu -- the C ABI (include/fa.h): argument validation, TMA tensor
 // maps, launch configuration, the split-KV workspace and error reporting.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -10,7 +11,7 @@
 
 namespace {
 
-constexpr int kVersion = 100;
+constexpr int kVersion = 101;
 constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSeq = 1 << 30;
@@ -128,6 +129,45 @@ cudaError_t launch_fwd(int d, int bc, int qt, const CUtensorMap* maps, const fa:
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Work items of the persistent forward grid: (query-tile group, split, head).
+// A mask makes the query-tile groups' work unequal, so the items then go out
+// group by group, heaviest groups first (with the snake order of the CTAs the
+// totals even out); without one, head by head, so the query tiles of a head
+// run side by side and share its K/V tiles in L2.  Each launch covers fewer
+// than 2^31 items (32-bit index arithmetic in the kernel); a larger problem is
+// cut into launches over ranges of heads (or of splits, if one head alone has
+// that many items).  The grid has one CTA per SM (max_ctas CTAs if > 0), never
+// more than the launch's items.  launch(p, grid) issues one launch.
+template <class Launch>
+cudaError_t launch_items(fa::FwdParams p, int qt, int num_sms, int max_ctas, Launch&& launch) {
+  constexpr long long kMaxItems = 0x7fffffffLL;
+  p.n_qg = (p.Nq + 128 * qt - 1) / (128 * qt);
+  p.qg_major = (p.wl >= 0 || p.wr >= 0) ? 1 : 0;
+  p.qg_desc = p.wr >= 0 ? 1 : 0;  // a right bound: later query rows see more keys
+  const long long per_head = static_cast<long long>(p.n_qg) * p.n_splits;
+  const int heads_per = per_head > kMaxItems ? 1 : static_cast<int>(std::min<long long>(p.BH, kMaxItems / per_head));
+  const int splits_per = per_head > kMaxItems ? static_cast<int>(kMaxItems / p.n_qg) : p.n_splits;
+  for (int bh0 = 0; bh0 < p.BH; bh0 += heads_per) {
+    for (int s0 = 0; s0 < p.n_splits; s0 += splits_per) {
+      p.bh0 = bh0;
+      p.n_bh = std::min(heads_per, p.BH - bh0);
+      p.split0 = s0;
+      p.n_split = std::min(splits_per, p.n_splits - s0);
+      const long long items = static_cast<long long>(p.n_qg) * p.n_split * p.n_bh;
+      p.n_items = static_cast<int>(items);
+      p.div_qg = fa::make_fastdiv(p.n_qg);
+      p.div_split = fa::make_fastdiv(p.n_split);
+      p.div_per = fa::make_fastdiv(p.n_split * p.n_bh);
+      long long g = max_ctas > 0 ? max_ctas : (num_sms > 0 ? num_sms : 1);
+      if (g > items) g = items;
+      p.rounds = static_cast<int>((items + g - 1) / g);
+      const cudaError_t e = launch(p, dim3(static_cast<unsigned>(g)));
+      if (e != cudaSuccess) return e;
+    }
+  }
+  return cudaSuccess;
+}
+
 struct SplitLayout {
   size_t m_off, l_off, o_off, total;
 };
@@ -159,16 +199,17 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   }
   if (n_splits < 1 || n_splits > 65535) return FA_ERR_INVALID_ARG;
   if (wl < -1 || wr < -1 || wl > kMaxSeq || wr > kMaxSeq) return FA_ERR_INVALID_ARG;
-  int bc = 128, qt_opt = 0, skip = -1;
+  int bc = fa::kDefaultBc, qt_opt = 0, skip = -1, max_ctas = 0;
   unsigned long long timeout = kDefaultTimeoutNs;
   if (opts) {
     if (opts->bc != 0 && opts->bc != 64 && opts->bc != 128) return FA_ERR_INVALID_ARG;
     if (opts->q_tiles_per_cta < 0 || opts->q_tiles_per_cta > 2) return FA_ERR_INVALID_ARG;
-    if (opts->test_skip_kv_load < 0) return FA_ERR_INVALID_ARG;
+    if (opts->test_skip_kv_load < 0 || opts->max_ctas < 0) return FA_ERR_INVALID_ARG;
     if (opts->bc) bc = opts->bc;
     qt_opt = opts->q_tiles_per_cta;
     if (opts->timeout_ns) timeout = opts->timeout_ns;
     skip = opts->test_skip_kv_load - 1;
+    max_ctas = opts->max_ctas;
   }
   DevState* dev = nullptr;
   if ((rc = device_state(&dev)) != FA_OK) return rc;
@@ -188,7 +229,6 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.partial = (partial || splits > 1) ? 1 : 0;
   p.kv_tiles = kv_tiles;
   p.tiles_per_split = (kv_tiles + splits - 1) / splits;
-  p.causal = (wl < 0 && wr >= 0) ? 1 : 0;  // longest rows first
   p.wl = wl;
   p.wr = wr;
   p.scale = scale;
@@ -196,6 +236,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.timeout_ns = timeout;
   p.test_skip_load = skip;
   p.status = dev->status;
+  p.o = o;
   p.lse = lse;
 
   CUtensorMap maps[4];
@@ -207,19 +248,22 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   } else {
     maps[3] = maps[0];  // unused by the partial epilogue
   }
-  const dim3 grid((Nq + 128 * qt - 1) / (128 * qt), static_cast<unsigned>(p.n_splits),
-                  static_cast<unsigned>(BH));
   const long long rows = static_cast<long long>(BH) * Nq;
+  auto run = [&](const fa::FwdParams& pp) {
+    return launch_items(pp, qt, dev->num_sms, max_ctas, [&](const fa::FwdParams& pl, dim3 grid) {
+      return launch_fwd(d, bc, qt, maps, pl, grid, s);
+    });
+  };
 
   if (partial) {
     p.m_part = m_part;
     p.l_part = l_part;
     p.o_part = o_part;
-    cudaError_t e = launch_fwd(d, bc, qt, maps, p, grid, s);
+    cudaError_t e = run(p);
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
   }
   if (splits == 1) {
-    cudaError_t e = launch_fwd(d, bc, qt, maps, p, grid, s);
+    cudaError_t e = run(p);
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
   }
 
@@ -235,7 +279,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.m_part = reinterpret_cast<float*>(base + L.m_off);
   p.l_part = reinterpret_cast<float*>(base + L.l_off);
   p.o_part = reinterpret_cast<float*>(base + L.o_off);
-  e = launch_fwd(d, bc, qt, maps, p, grid, s);
+  e = run(p);
   if (e == cudaSuccess) {
     fa::MergeParams mp{};
     mp.m_part = p.m_part;
@@ -481,7 +525,6 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
   p.tiles_per_split = p.kv_tiles;
   p.wl = -1;
   p.wr = causal ? 0 : -1;
-  p.causal = causal ? 1 : 0;
   const double s_qk = static_cast<double>(scale) * q_descale * k_descale;
   p.scale = static_cast<float>(s_qk);
   p.scale_log2 = static_cast<float>(s_qk * 1.4426950408889634);
@@ -489,14 +532,16 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
   p.timeout_ns = kDefaultTimeoutNs;
   p.test_skip_load = -1;
   p.status = dev->status;
+  p.o = o;
   p.lse = lse;
   CUtensorMap maps[4];
   if ((rc = make_map(&maps[0], q, d, Nq, BH, 128, true)) != FA_OK) return rc;
   if ((rc = make_map(&maps[1], k, d, Nk, BH, 128, true)) != FA_OK) return rc;
   if ((rc = make_map(&maps[2], v, d, Nk, BH, 128, true)) != FA_OK) return rc;
   if ((rc = make_map(&maps[3], o, d, Nq, BH, 128)) != FA_OK) return rc;
-  const dim3 grid((Nq + 128 * qt - 1) / (128 * qt), 1, static_cast<unsigned>(BH));
-  cudaError_t e = fa::launch_fwd_fp8_d128(qt, maps, p, grid, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_items(p, qt, dev->num_sms, 0, [&](const fa::FwdParams& pl, dim3 grid) {
+    return fa::launch_fwd_fp8_d128(qt, maps, pl, grid, static_cast<cudaStream_t>(stream));
+  });
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 

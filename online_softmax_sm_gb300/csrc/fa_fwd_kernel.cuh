@@ -15,14 +15,24 @@
 // uses 0 as its reference point, so no (-inf) - (-inf) appears (section 7.1);
 // a row with l = 0 gets O = 0 and LSE = -inf (sections 7.2-7.3).
 //
-// CTA = QT query tiles of 128 rows of one (b, h), over one range of K/V tiles
-// (the whole key axis, or one split of it).  The mask keeps, for query row r,
-// keys [r + off - wl, r + off + wr] (off = Nk - Nq, -1 = open side; causal is
-// (-1, 0)).  The CTA streams the K/V tiles from the first one any of its rows
-// can see; every query tile starts there and stops after its own last visible
-// tile, so the query tiles' ranges are prefixes of one stream.
-//   WG 0          warp 0: TMA producer (one thread): Q once, then K and V
-//                 tiles through a ring of shared-memory stages, K one step
+// Persistent: the grid holds at most one CTA per SM, and each CTA walks a
+// static list of work items.  An item is QT query tiles of 128 rows of one
+// (b, h) over one range of K/V tiles (the whole key axis, or one split of
+// it).  Items are dealt out in snake order (round r gives item r*G + c to CTA
+// c on even rounds, r*G + G-1-c on odd ones), heaviest query tiles first when
+// a mask makes their work unequal, so the CTAs' totals even out.  Everything
+// that lives across items -- TMEM, the mbarriers and their phases, the K/V
+// ring -- carries over: the next item's Q and first K/V tiles load while the
+// current item finishes, and its first S product runs while the current
+// epilogue drains.
+//
+// The mask keeps, for query row r, keys [r + off - wl, r + off + wr]
+// (off = Nk - Nq, -1 = open side; causal is (-1, 0)).  An item streams the
+// K/V tiles from the first one any of its rows can see; every query tile
+// starts there and stops after its own last visible tile, so the query tiles'
+// ranges are prefixes of one stream.
+//   WG 0          warp 0: TMA producer (one thread): per item, Q_i, then K and
+//                 V tiles through a ring of shared-memory stages, K one step
 //                 ahead of V (see ring_pos_k / ring_pos_v).
 //                 Warp 1 + i: MMA issuer of tile i (warp-uniform code, one
 //                 elected lane issues, blocking barrier waits):
@@ -47,16 +57,17 @@
 // S_0(1), ...), P_i (BC/2 or BC/4 columns), O_i (D columns each).  P_i(j+1)
 // is written only after O_i += P_i(j) V_j has completed.  Shared memory: the
 // Q tiles ([128 rows][D], 128-byte swizzle, the layout the MMA reads K-major),
-// then the K/V ring: keeping P out of shared memory leaves room for five 32 KB
-// stages at d = 128.
+// a 16 KB O staging buffer per tile where it fits without dropping the K/V
+// ring below five stages (else each tile's epilogue borrows a K/V ring slot
+// for its O), then the K/V ring.
 // Softmax reference: bf16 rows move their reference m only when the tile max
 // exceeds it by more than 16 in base-2 exponent units (P <= 2^16), so O is
 // rarely rescaled; the final O / l and LSE do not depend on the reference.
 //
 // Every mbarrier wait is bounded by a global-timer limit.  A wait that runs
 // out sets the CTA's abort flag and the device status word; every role then
-// leaves its loop, lets its own copies / MMAs in flight finish, and the CTA
-// frees TMEM and exits without writing outputs.
+// leaves its loops, lets its own copies / MMAs in flight finish, and the CTA
+// frees TMEM and exits without writing further outputs.
 #pragma once
 
 #include "fa_internal.h"
@@ -96,8 +107,8 @@ struct FwdCfg {
   // 256 threads launch with the per-thread maximum and need no split.
   static constexpr bool kSplitRegs = kThreads > 256;
   static constexpr int kRegLaunch = kCorr ? (QT == 2 ? 128 : 168) : (QT == 2 ? 168 : 0);
-  static constexpr int kRegSoftmax = kCorr ? (QT == 2 ? 192 : 216) : (QT == 2 ? 216 : 0);
-  static constexpr int kRegCorr = kCorr ? (QT == 2 ? 64 : 160) : 0;
+  static constexpr int kRegSoftmax = kCorr ? (QT == 2 ? 184 : 216) : (QT == 2 ? 216 : 0);
+  static constexpr int kRegCorr = kCorr ? (QT == 2 ? 80 : 160) : 0;
   static constexpr int kRegOther = kCorr ? (QT == 2 ? 64 : 128) : (QT == 2 ? 72 : 0);
   static_assert(!kSplitRegs || QT * kRegSoftmax + kRegCorr + kRegOther == kWGs * kRegLaunch,
                 "setmaxnreg split must add up to the registers the block launches with");
@@ -127,16 +138,32 @@ struct FwdCfg {
                                                       : 512;
   static constexpr int kCtlBytes = 2048;
   static constexpr int kSmemLimit = 227 * 1024;
-  static constexpr int kStagesFit =
-      (kSmemLimit - 1024 - kCtlBytes - QT * kQTileBytes) / kKVTileBytes;
-  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  // bf16 O is staged for the TMA store 64 columns (one 128-byte swizzle row)
+  // at a time: 16 KB per tile.
+  static constexpr int kStgBytes = kBr * 128;
+  static constexpr int kRingRoom = kSmemLimit - 1024 - kCtlBytes - QT * kQTileBytes;
+  static constexpr int kStagesNoStg = kRingRoom / kKVTileBytes > 8 ? 8 : kRingRoom / kKVTileBytes;
+  static constexpr int kStagesStg = (kRingRoom - QT * kStgBytes) / kKVTileBytes > 8
+                                        ? 8
+                                        : (kRingRoom - QT * kStgBytes) / kKVTileBytes;
+  // O gets staging buffers of its own unless that costs a ring stage below
+  // five; otherwise each item's epilogue borrows K/V ring slots (kSlotStg):
+  // the producer hands out one slot per tile after the item's last K/V tile,
+  // tile i stages all of its O in slot i, and the slot returns to the ring
+  // once the store has read it.
+  static constexpr bool kOwnStg = kStagesStg >= 5 || kStagesStg == kStagesNoStg;
+  static constexpr bool kSlotStg = !kOwnStg;
+  static constexpr int kStages = kOwnStg ? kStagesStg : kStagesNoStg;
   static_assert(kStages >= 2, "shared memory");
+  static_assert(!kSlotStg || (kKVTileBytes >= D * 256 && kStages > QT), "O staging in ring slots");
   static constexpr int kSmemBytes =
-      1024 + QT * kQTileBytes + kStages * kKVTileBytes + kCtlBytes;
+      1024 + QT * kQTileBytes + (kOwnStg ? QT * kStgBytes : 0) + kStages * kKVTileBytes + kCtlBytes;
 };
 
 struct __align__(8) Ctl {
-  uint64_t q_full;
+  uint64_t q_full[2];       // Q_i landed (TMA bytes)
+  uint64_t q_free[2];       // Q_i buffer no longer read (last S_i product done; with O
+                            // staged in it, the store has read it too)
   uint64_t kv_full[8];
   uint64_t kv_empty[8][2];  // [stage][tile]: that tile's MMAs reading the stage completed
   uint64_t s_full[2];       // S_i(j) in TMEM (MMA commit)
@@ -148,13 +175,14 @@ struct __align__(8) Ctl {
   uint64_t drain[2];        // every MMA of tile i's issuer has completed
   uint32_t tmem_base;
   int abort;
+  int corr_stop[2];         // tile i has no more steps (E4M3 correction)
   float alpha[2][128];      // per-row rescale factor, softmax -> correction
 };
 static_assert(sizeof(Ctl) <= 2048, "control block");
 
-// Order of the K/V tiles through the shared-memory ring for a CTA with n steps:
-// K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}: K runs one step
-// ahead of V, as S_i(j+1) is computed while step j's softmax still runs.
+// Order of the K/V tiles through the shared-memory ring for an item with n
+// steps: K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}: K runs one
+// step ahead of V, as S_i(j+1) is computed while step j's softmax still runs.
 __device__ __forceinline__ int ring_pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int ring_pos_v(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
 // Inverse: position p -> (is_v, step).
@@ -170,6 +198,131 @@ __device__ __forceinline__ void ring_decode(int p, int n, bool& is_v, int& step)
   }
 }
 
+// Ring position -> (stage, phase parity): positions are counted from the
+// start of the CTA; (base_stage, base_par) is the item's first position.
+struct RingPos {
+  int stage;
+  uint32_t par;
+};
+template <int S>
+__device__ __forceinline__ RingPos ring_at(int base_stage, uint32_t base_par, int p) {
+  const int t = base_stage + p;
+  return RingPos{t % S, base_par ^ (static_cast<uint32_t>(t / S) & 1u)};
+}
+template <int S>
+__device__ __forceinline__ void ring_advance(int& base_stage, uint32_t& base_par, int n_pos) {
+  const int t = base_stage + n_pos;
+  base_stage = t % S;
+  base_par ^= static_cast<uint32_t>(t / S) & 1u;
+}
+
+// One work item: query tiles [row0, row0 + 128 QT) of head bh over the K/V
+// tiles of one split.  Tile i takes steps [0, n[i]) of the item's stream of
+// n_cta K/V tiles starting at tile cta_b (n[i] = 0: no visible key).
+template <int QT>
+struct Item {
+  int bh, split, row0;
+  int cta_b, n_cta;
+  int n[QT];
+};
+
+// Head, split and first query row of item `idx` (idx < n_items), in the
+// order the host chose.
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+  const unsigned int u = static_cast<unsigned int>(n);
+  return static_cast<int>((__umulhi(u, f.mul) + u) >> f.shift);
+}
+
+template <int QT>
+__device__ __forceinline__ void item_coords(int idx, const FwdParams& p, int& bh, int& split,
+                                            int& row0) {
+  int x;
+  if (p.qg_major) {  // query-tile group outermost: heaviest first across heads
+    x = fdiv(idx, p.div_per);
+    const int r = idx - x * p.div_per.d;
+    bh = fdiv(r, p.div_split);
+    split = r - bh * p.n_split;
+  } else {  // head outermost: the query tiles of one head are neighbours (L2 reuse of K/V)
+    const int r = fdiv(idx, p.div_qg);
+    x = idx - r * p.n_qg;
+    bh = fdiv(r, p.div_split);
+    split = r - bh * p.n_split;
+  }
+  bh += p.bh0;
+  split += p.split0;
+  const int qg = p.qg_desc ? p.n_qg - 1 - x : x;
+  row0 = qg * (128 * QT);
+}
+
+// a[i] for a tile index i known only at run time, as a select between
+// registers (indexing the array would put it in local memory).
+template <int QT>
+__device__ __forceinline__ int pick(const int (&a)[QT], int i) {
+  if constexpr (QT == 1) return a[0];
+  else return i == 0 ? a[0] : a[1];
+}
+
+// Item `idx` of the launch (idx < n_items): coordinates and the steps of each
+// query tile.
+template <int BC, int QT>
+__device__ __forceinline__ void make_item(int idx, const FwdParams& p, Item<QT>& it) {
+  item_coords<QT>(idx, p, it.bh, it.split, it.row0);
+  const int kv_begin = it.split * p.tiles_per_split;
+  const int kv_end = min(p.kv_tiles, kv_begin + p.tiles_per_split);
+  // K/V tiles [b_i, e_i) of this split hold keys visible to rows of query
+  // tile i (empty: e_i = b_i).  The item streams from cta_b = min b_i; tile i
+  // takes steps [0, n_i), n_i = e_i - cta_b (its leading tiles before b_i are
+  // fully masked for it and cost one MMA pair each).
+  const int off = p.Nk - p.Nq;
+  int cta_b = kv_end, kv_end_cta = kv_begin;
+  bool any_tile = false;  // a split past the last K/V tile has kv_begin >= kv_end
+#pragma unroll
+  for (int i = 0; i < QT; ++i) {
+    const int r_first = it.row0 + 128 * i;
+    it.n[i] = -1;  // end tile, -1 = none
+    if (r_first < p.Nq) {
+      const int r_last = min(r_first + 128, p.Nq) - 1;
+      // |r + off| < 2^30 and wl, wr <= 2^30: these sums stay within int
+      const int klo = p.wl < 0 ? 0 : max(0, r_first + off - p.wl);
+      const int khi = p.wr < 0 ? p.Nk - 1 : min(p.Nk - 1, r_last + off + p.wr);
+      if (khi >= klo) {
+        const int b = max(kv_begin, static_cast<int>(klo / BC));
+        const int e = min(kv_end, static_cast<int>(khi / BC) + 1);
+        if (e > b) {
+          it.n[i] = e;
+          any_tile = true;
+          cta_b = min(cta_b, b);
+          kv_end_cta = max(kv_end_cta, e);
+        }
+      }
+    }
+  }
+  if (!any_tile) cta_b = kv_end_cta = kv_begin;  // nothing to stream
+#pragma unroll
+  for (int i = 0; i < QT; ++i) it.n[i] = it.n[i] < 0 ? 0 : it.n[i] - cta_b;
+  it.cta_b = cta_b;
+  it.n_cta = kv_end_cta - cta_b;
+}
+
+// Ring positions an item takes: its K and V tiles, plus (with O staged in
+// ring slots) one slot per tile for the epilogue when it writes bf16 O of any
+// tile; tile i's slot is position 2 n_cta + i.
+template <bool kSlotStg, int QT>
+__device__ __forceinline__ int item_positions(const Item<QT>& it, const FwdParams& p, bool& oslot) {
+  oslot = false;
+  if (kSlotStg && !p.partial)
+#pragma unroll
+    for (int i = 0; i < QT; ++i) oslot = oslot || it.n[i] > 0;
+  return 2 * it.n_cta + (oslot ? QT : 0);
+}
+
+// Item of this CTA in round r (snake order), or -1 past the end.
+__device__ __forceinline__ int item_of_round(int r, const FwdParams& p) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const long long idx = static_cast<long long>(r) * G + ((r & 1) ? G - 1 - c : c);
+  return idx < p.n_items ? static_cast<int>(idx) : -1;
+}
+
 template <int D, int BC, int QT, bool F8 = false>
 __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -181,53 +334,16 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint8_t* sQ = smem;
-  uint8_t* sKV = sQ + QT * C::kQTileBytes;
+  uint8_t* sStg = sQ + QT * C::kQTileBytes;  // own O staging (kOwnStg)
+  uint8_t* sKV = sStg + (C::kOwnStg ? QT * C::kStgBytes : 0);
   Ctl* ctl = reinterpret_cast<Ctl*>(sKV + C::kStages * C::kKVTileBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rounds = p.rounds;
 
-  // ---- work coordinates (identical in every thread)
-  const int qg = p.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int split = blockIdx.y;
-  const int bh = blockIdx.z;
-  const int row0 = qg * (C::kBr * QT);
-  const int kv_begin = split * p.tiles_per_split;
-  const int kv_end = min(p.kv_tiles, kv_begin + p.tiles_per_split);
-  // K/V tiles [b_i, e_i) of this split hold keys visible to rows of query
-  // tile i (empty: e_i = b_i).  The CTA streams from cta_b = min b_i; tile i
-  // takes steps [0, n_i) of that stream, n_i = e_i - cta_b (its leading tiles
-  // before b_i are fully masked for it and cost one MMA pair each).
-  const int off = p.Nk - p.Nq;
-  int n_i[QT];
-  int cta_b = kv_end, kv_end_cta = kv_begin;
-  bool any_tile = false;  // a split past the last K/V tile has kv_begin >= kv_end
-#pragma unroll
-  for (int i = 0; i < QT; ++i) {
-    const int r_first = row0 + C::kBr * i;
-    n_i[i] = -1;  // end tile, -1 = none
-    if (r_first < p.Nq) {
-      const int r_last = min(r_first + C::kBr, p.Nq) - 1;
-      // |r + off| < 2^30 and wl, wr <= 2^30: these sums stay within int
-      const int klo = p.wl < 0 ? 0 : max(0, r_first + off - p.wl);
-      const int khi = p.wr < 0 ? p.Nk - 1 : min(p.Nk - 1, r_last + off + p.wr);
-      if (khi >= klo) {
-        const int b = max(kv_begin, static_cast<int>(klo / BC));
-        const int e = min(kv_end, static_cast<int>(khi / BC) + 1);
-        if (e > b) {
-          n_i[i] = e;
-          any_tile = true;
-          cta_b = min(cta_b, b);
-          kv_end_cta = max(kv_end_cta, e);
-        }
-      }
-    }
-  }
-  if (!any_tile) cta_b = kv_end_cta = kv_begin;  // nothing to stream
-#pragma unroll
-  for (int i = 0; i < QT; ++i) n_i[i] = n_i[i] < 0 ? 0 : n_i[i] - cta_b;
-
-  const uint32_t bar_q = smem_u32(&ctl->q_full);
+  const uint32_t bar_qf = smem_u32(&ctl->q_full[0]);
+  const uint32_t bar_qe = smem_u32(&ctl->q_free[0]);
   const uint32_t bar_kv_full = smem_u32(&ctl->kv_full[0]);
   const uint32_t bar_kv_empty = smem_u32(&ctl->kv_empty[0][0]);  // + 16*stage + 8*tile
   const uint32_t bar_s = smem_u32(&ctl->s_full[0]);
@@ -240,7 +356,10 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
 
   // ---- setup
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
+    for (int i = 0; i < QT; ++i) {
+      mbar_init(bar_qf + 8 * i, 1);
+      mbar_init(bar_qe + 8 * i, 1);
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar_kv_full + 8 * s, 1);
       for (int i = 0; i < QT; ++i) mbar_init(bar_kv_empty + 16 * s + 8 * i, 1);
@@ -255,12 +374,14 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       mbar_init(bar_drain + 8 * i, 1);
     }
     ctl->abort = 0;
+    ctl->corr_stop[0] = ctl->corr_stop[1] = 0;
     fence_mbar_init();
   }
   if (warp == C::kLoadWarp && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   if (warp == C::kAllocWarp) {
     tmem_alloc(smem_u32(&ctl->tmem_base), C::kTmemCols);
@@ -279,57 +400,112 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
     if (warp == C::kLoadWarp) {
       if (lane == 0) {
       // ============================================================== producer
-      uint32_t qbytes = 0;
+      // Per stage s, bits 2s + i: tile i reads the stage's current content
+      // (rd), and the parity of the next kv_empty[s][i] phase to wait for (pe).
+      uint32_t rd = 0, pe = 0;
+      uint32_t filled = 0, fill_par = 0;  // per stage: ever filled; parity of its last fill
+      int q_loads[QT];                    // Q_i loads so far
 #pragma unroll
-      for (int i = 0; i < QT; ++i)
-        if (n_i[i] > 0) qbytes += C::kQTileBytes;
-      if (qbytes) {
-        mbar_arrive_expect_tx(bar_q, qbytes);
-#pragma unroll
-        for (int i = 0; i < QT; ++i) {
-          if (n_i[i] <= 0) continue;
-#pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(smem_u32(sQ + i * C::kQTileBytes + c * C::kQChunkBytes), &tm_q, bar_q,
-                        c * C::kChunkElems, row0 + C::kBr * i, bh);
-        }
-      }
-      uint32_t issued_mask = 0, issued_par = 0;
-      const int n_cta = kv_end_cta - cta_b;
+      for (int i = 0; i < QT; ++i) q_loads[i] = 0;
+      int g_stage = 0;
+      uint32_t g_par = 0;
+      int g = 0;  // ring positions so far (the test hook counts these; stops at 2^31 - 1)
       bool ok = true;
-      for (int it = 0; ok && it < 2 * n_cta; ++it) {
-        const int stage = it % C::kStages;
-        const int use = it / C::kStages;
-        if (use > 0) {
-          // the slot's previous content (ring position it - kStages) must be
-          // released by every tile that read it
-          bool pv_;
-          int prev_step;
-          ring_decode(it - C::kStages, n_cta, pv_, prev_step);
+      for (int r = 0; ok && r < rounds; ++r) {
+        const int idx = item_of_round(r, p);
+        if (idx < 0) continue;
+        Item<QT> it;
+        make_item<BC, QT>(idx, p, it);
+        // Warm L2 with the next item's Q tiles, once this item's first loads
+        // are under way (a prefetch occupies the TMA unit like a load).
+        auto prefetch_next_q = [&]() {
+          int nidx = -1;
+          for (int r2 = r + 1; nidx < 0 && r2 < rounds; ++r2) nidx = item_of_round(r2, p);
+          if (nidx >= 0) {
+            int nbh, nsplit, nrow0;
+            item_coords<QT>(nidx, p, nbh, nsplit, nrow0);
+#pragma unroll
+            for (int i = 0; i < QT; ++i)
+              if (nrow0 + C::kBr * i < p.Nq)
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+                  tma_prefetch_l2_3d(&tm_q, c * C::kChunkElems, nrow0 + C::kBr * i, nbh);
+          }
+        };
+        // Q_i of this item, once the previous item's last S_i product is done.
+        auto load_q = [&]() {
+#pragma unroll
+          for (int i = 0; i < QT; ++i) {
+            if (it.n[i] <= 0) continue;
+            if (q_loads[i] > 0 && !wait_bounded(bar_qe + 8 * i, (q_loads[i] - 1) & 1, wc)) return false;
+            const uint32_t full = bar_qf + 8 * i;
+            mbar_arrive_expect_tx(full, C::kQTileBytes);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(smem_u32(sQ + i * C::kQTileBytes + c * C::kQChunkBytes), &tm_q, full,
+                          c * C::kChunkElems, it.row0 + C::kBr * i, it.bh);
+            ++q_loads[i];
+          }
+          return true;
+        };
+        bool oslot;
+        const int n_pos = item_positions<C::kSlotStg, QT>(it, p, oslot);
+        const int n_kv = 2 * it.n_cta;
+        const int pf_at = min(n_kv, C::kStages + 1);
+        if (!(ok = load_q())) break;
+        for (int pos = 0; ok && pos < n_pos; ++pos) {
+          if (pos == pf_at) prefetch_next_q();
+          const RingPos rp = ring_at<C::kStages>(g_stage, g_par, pos);
+          const int s2 = 2 * rp.stage;
+          // the slot's previous content must be released by every tile that read it
 #pragma unroll
           for (int i = 0; i < QT; ++i)
-            if (ok && prev_step < n_i[i])
-              ok = wait_bounded(bar_kv_empty + 16 * stage + 8 * i, (use - 1) & 1, wc);
+            if (ok && ((rd >> (s2 + i)) & 1u)) {
+              ok = wait_bounded(bar_kv_empty + 16 * rp.stage + 8 * i, (pe >> (s2 + i)) & 1u, wc);
+              pe ^= 1u << (s2 + i);
+            }
           if (!ok) break;
-        }
-        if (it == p.test_skip_load) continue;  // test hook: this slot never fills
-        bool is_v;
-        int step;
-        ring_decode(it, n_cta, is_v, step);
-        const uint32_t full = bar_kv_full + 8 * stage;
-        mbar_arrive_expect_tx(full, C::kKVTileBytes);
-        const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+          if (pos >= n_kv) {
+            // O staging slot of tile pos - n_kv: no copy; that tile releases
+            // it if it stages O
+            const int ti = pos - n_kv;
+            uint32_t stager = 0;
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem_u32(sKV + stage * C::kKVTileBytes + c * C::kKVChunkBytes), map, full,
-                      c * C::kChunkElems, (cta_b + step) * BC, bh);
-        issued_mask |= 1u << stage;
-        issued_par = (issued_par & ~(1u << stage)) | (static_cast<uint32_t>(use & 1) << stage);
+            for (int i = 0; i < QT; ++i) stager |= (i == ti && it.n[i] > 0 ? 1u : 0u) << i;
+            rd = (rd & ~(3u << s2)) | (stager << s2);
+            mbar_arrive(bar_kv_full + 8 * rp.stage);
+            filled |= 1u << rp.stage;
+            fill_par = (fill_par & ~(1u << rp.stage)) | (rp.par << rp.stage);
+            continue;
+          }
+          bool is_v;
+          int step;
+          ring_decode(pos, it.n_cta, is_v, step);
+          uint32_t readers = 0;
+#pragma unroll
+          for (int i = 0; i < QT; ++i) readers |= (step < it.n[i] ? 1u : 0u) << i;
+          rd = (rd & ~(3u << s2)) | (readers << s2);
+          const bool skip = g == p.test_skip_load;
+          if (g < 0x7fffffff) ++g;
+          if (skip) continue;  // test hook: this slot never fills
+          const uint32_t full = bar_kv_full + 8 * rp.stage;
+          mbar_arrive_expect_tx(full, C::kKVTileBytes);
+          const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(smem_u32(sKV + rp.stage * C::kKVTileBytes + c * C::kKVChunkBytes), map, full,
+                        c * C::kChunkElems, (it.cta_b + step) * BC, it.bh);
+          filled |= 1u << rp.stage;
+          fill_par = (fill_par & ~(1u << rp.stage)) | (rp.par << rp.stage);
+        }
+        ring_advance<C::kStages>(g_stage, g_par, n_pos);
       }
       // Every copy started here must land before the CTA may exit.
       for (int s = 0; s < C::kStages; ++s)
-        if ((issued_mask >> s) & 1u) wait_own(bar_kv_full + 8 * s, (issued_par >> s) & 1u, p.timeout_ns);
-      if (qbytes) wait_own(bar_q, 0, p.timeout_ns);
+        if ((filled >> s) & 1u) wait_own(bar_kv_full + 8 * s, (fill_par >> s) & 1u, p.timeout_ns);
+#pragma unroll
+      for (int i = 0; i < QT; ++i)
+        if (q_loads[i] > 0) wait_own(bar_qf + 8 * i, (q_loads[i] - 1) & 1, p.timeout_ns);
       }
       __syncwarp();
     } else if (warp >= C::kMmaWarp0 && warp < C::kMmaWarp0 + QT) {
@@ -363,80 +539,125 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       const uint32_t tS = tmem + C::kSCol + (C::kSharedS ? 0 : i * BC),
                      tP = tmem + C::kPCol + i * C::kPCols,
                      tO = tmem + C::kOCol + i * D;
-      const int n = n_i[i];
-      const int n_cta = kv_end_cta - cta_b;
-      auto kv_ready = [&](int pos) {
-        return warp_wait(bar_kv_full + 8 * (pos % C::kStages), (pos / C::kStages) & 1, wc);
-      };
-      // A shared S buffer is taken in the order S_0(0), S_1(0), S_0(1), ...
-      // (a tile past its last step drops out); a tile's own buffer holds
-      // S_i(0), S_i(1), ...  Each use waits until the previous one has been
-      // read into registers.  Previous use before S_i(q): bar / parity of its
-      // s_free, false if none.
-      auto prev_use = [&](int q, uint32_t& bar, uint32_t& par) {
-        if constexpr (QT == 2 && C::kSharedS) {
-          const int o = 1 - i, qo = i == 1 ? q : q - 1;
-          if (qo >= 0 && qo < n_i[o]) {
-            bar = bar_sfree + 8 * o, par = qo & 1;
-            return true;
+      // Phases carried across items: S products of this tile and of the other
+      // one so far (= the s_free / pv_ready / o_done phases), Q_i loads
+      // consumed, the ring base, and the last product in a shared S buffer.
+      int cs_me = 0, cs_ot = 0;
+      int q_loads = 0;
+      int g_stage = 0;
+      uint32_t g_par = 0;
+      int last_t = -1, last_c = 0;
+      bool ok = true, issued = false;
+      for (int r = 0; ok && r < rounds; ++r) {
+        const int idx = item_of_round(r, p);
+        if (idx < 0) continue;
+        Item<QT> it;
+        make_item<BC, QT>(idx, p, it);
+        const int n = pick<QT>(it.n, i);
+        const int n_ot = QT == 2 ? pick<QT>(it.n, 1 - i) : 0;
+        const int n_cta = it.n_cta;
+        auto kv_ready = [&](int pos) {
+          const RingPos rp = ring_at<C::kStages>(g_stage, g_par, pos);
+          return warp_wait(bar_kv_full + 8 * rp.stage, rp.par, wc);
+        };
+        // A shared S buffer is taken in the order S_0(0), S_1(0), S_0(1), ...
+        // (a tile past its last step drops out), continuing from the previous
+        // item's last product; a tile's own buffer holds S_i(0), S_i(1), ...
+        // Each use waits until the previous one has been read into registers.
+        auto prev_use = [&](int q, uint32_t& bar, uint32_t& par) {
+          if constexpr (QT == 2 && C::kSharedS) {
+            const int o = 1 - i, qo = i == 1 ? q : q - 1;
+            if (qo >= 0 && qo < n_ot) {
+              bar = bar_sfree + 8 * o, par = (cs_ot + qo) & 1;
+              return true;
+            }
+            if (q == 0) {
+              if (last_t < 0) return false;
+              bar = bar_sfree + 8 * last_t, par = last_c & 1;
+              return true;
+            }
+          } else {
+            if (q == 0) {
+              if (cs_me == 0) return false;
+              bar = bar_sfree + 8 * i, par = (cs_me - 1) & 1;
+              return true;
+            }
+          }
+          bar = bar_sfree + 8 * i, par = (cs_me + q - 1) & 1;
+          return true;
+        };
+        auto s_ready = [&](int q) {  // S_i(q) may be written: the buffer's previous product was read
+          uint32_t bar, par;
+          return !prev_use(q, bar, par) || warp_wait(bar, par, wc);
+        };
+        auto issue_qk = [&](int q) {  // S_i(q) = Q_i K_q^T, then release K_q's slot for tile i
+          const int stage = ring_at<C::kStages>(g_stage, g_par, ring_pos_k(q)).stage;
+          const uint32_t k_lo = lo_k + ((stage * C::kKVTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < D / C::kKStep; ++kk) {  // 32 bytes of K per step
+            const uint32_t off_q = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
+            const uint32_t off_k = ((kk / 4) * C::kKVChunkBytes + (kk % 4) * 32) >> 4;
+            mma(tS, hi_q | (lo_q + off_q), hi_k | (k_lo + off_k), kIdescQK, kk > 0);
+          }
+          mma_commit_elect(bar_s + 8 * i);
+          mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
+          // After this item's last S_i, Q_i may be overwritten.
+          if (q == n - 1) mma_commit_elect(bar_qe + 8 * i);
+        };
+        auto issue_pv = [&](int v) {  // O_i += P_i(v) V_v, then release V_v's slot for tile i
+          const int stage = ring_at<C::kStages>(g_stage, g_par, ring_pos_v(v, n_cta)).stage;
+          const uint32_t v_lo = lo_v + ((stage * C::kKVTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < BC / C::kKStep; ++kk) {
+            // P: one K-step (32 bytes = 8 TMEM columns of packed P).  V: kKStep
+            // keys = 8-row groups of 1024 B (SBO); D columns in 128-byte chunks
+            // BC*128 B apart (LBO).  The item's first product overwrites O_i.
+            mma_ts(tO, tP + 8 * kk, hi_v | (v_lo + ((kk * C::kKStep * 128) >> 4)), kIdescPV,
+                   (v > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit_elect(bar_o + 8 * i);
+          mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
+        };
+        if (n > 0) {
+          // S_i(j+1) first: it waits only for the other tile to read its S,
+          // which comes before P_i(j) is ready.
+          ok = warp_wait(bar_qf + 8 * i, q_loads & 1, wc) && s_ready(0) && kv_ready(ring_pos_k(0));
+          ++q_loads;
+          if (ok) {
+            tc_fence_after();
+            issue_qk(0);
+            issued = true;
+          }
+          for (int j = 0; ok && j < n; ++j) {
+            if (j + 1 < n) {
+              ok = s_ready(j + 1) && kv_ready(ring_pos_k(j + 1));
+              if (!ok) break;
+              tc_fence_after();
+              issue_qk(j + 1);
+            }
+            // O_i += P_i(j) V_j once P_i(j) is in TMEM and O_i rescaled
+            ok = warp_wait(bar_pv + 8 * i, (cs_me + j) & 1, wc) && kv_ready(ring_pos_v(j, n_cta));
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(j);
           }
         }
-        if (q == 0) return false;
-        bar = bar_sfree + 8 * i, par = (q - 1) & 1;
-        return true;
-      };
-      auto s_ready = [&](int q) {  // S_i(q) may be written: the buffer's previous product was read
-        uint32_t bar, par;
-        return !prev_use(q, bar, par) || warp_wait(bar, par, wc);
-      };
-      auto issue_qk = [&](int q) {  // S_i(q) = Q_i K_q^T, then release K_q's slot for tile i
-        const int stage = ring_pos_k(q) % C::kStages;
-        const uint32_t k_lo = lo_k + ((stage * C::kKVTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < D / C::kKStep; ++kk) {  // 32 bytes of K per step
-          const uint32_t off_q = ((kk / 4) * C::kQChunkBytes + (kk % 4) * 32) >> 4;
-          const uint32_t off_k = ((kk / 4) * C::kKVChunkBytes + (kk % 4) * 32) >> 4;
-          mma(tS, hi_q | (lo_q + off_q), hi_k | (k_lo + off_k), kIdescQK, kk > 0);
+        if constexpr (QT == 2 && C::kSharedS) {
+          // tile 1's last product comes last unless tile 0 has more steps
+          const int n0 = i == 0 ? n : n_ot, n1 = i == 0 ? n_ot : n;
+          const int c0 = i == 0 ? cs_me : cs_ot, c1 = i == 0 ? cs_ot : cs_me;
+          if (n0 > 0 || n1 > 0) {
+            if (n1 >= n0) {
+              last_t = 1, last_c = c1 + n1 - 1;
+            } else {
+              last_t = 0, last_c = c0 + n0 - 1;
+            }
+          }
         }
-        mma_commit_elect(bar_s + 8 * i);
-        mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
-      };
-      auto issue_pv = [&](int v) {  // O_i += P_i(v) V_v, then release V_v's slot for tile i
-        const int stage = ring_pos_v(v, n_cta) % C::kStages;
-        const uint32_t v_lo = lo_v + ((stage * C::kKVTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < BC / C::kKStep; ++kk) {
-          // P: one K-step (32 bytes = 8 TMEM columns of packed P).  V: kKStep
-          // keys = 8-row groups of 1024 B (SBO); D columns in 128-byte chunks
-          // BC*128 B apart (LBO).
-          mma_ts(tO, tP + 8 * kk, hi_v | (v_lo + ((kk * C::kKStep * 128) >> 4)), kIdescPV,
-                 (v > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit_elect(bar_o + 8 * i);
-        mma_commit_elect(bar_kv_empty + 16 * stage + 8 * i);
-      };
-      // S_i(j+1) first: it waits only for the other tile to read its S, which
-      // comes before P_i(j) is ready.
-      bool ok = n > 0;
-      bool issued = false;
-      if (ok) ok = warp_wait(bar_q, 0, wc) && s_ready(0) && kv_ready(ring_pos_k(0));
-      if (ok) {
-        tc_fence_after();
-        issue_qk(0);
-        issued = true;
-      }
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n) {
-          ok = s_ready(j + 1) && kv_ready(ring_pos_k(j + 1));
-          if (!ok) break;
-          tc_fence_after();
-          issue_qk(j + 1);
-        }
-        // O_i += P_i(j) V_j once P_i(j) is in TMEM and O_i rescaled
-        ok = warp_wait(bar_pv + 8 * i, j & 1, wc) && kv_ready(ring_pos_v(j, n_cta));
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(j);
+        cs_me += n;
+        cs_ot += n_ot;
+        bool oslot;
+        ring_advance<C::kStages>(g_stage, g_par, item_positions<C::kSlotStg, QT>(it, p, oslot));
       }
       if (issued) {
         // Everything issued above completes before TMEM may be freed.
@@ -450,16 +671,22 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
     // Serves the tiles in whatever order their inputs arrive: per tile,
     // (1) read alpha_i(j) as soon as it is published and release the slot,
     // (2) once O_i += P_i(j-1) V_{j-1} has completed, O_i <- alpha O_i, then
-    // let the MMA warp issue O_i += P_i(j) V_j.
+    // let the MMA warp issue O_i += P_i(j) V_j.  Steps are counted from the
+    // start of the CTA across its items; an item's first step publishes
+    // alpha = 1 (its first product overwrites O_i), so item boundaries need
+    // no handling here.  After its last item, tile i publishes one more
+    // alpha phase with corr_stop[i] set: that tile is finished.
     if constexpr (C::kSplitRegs && C::kRegCorr < C::kRegLaunch) setmaxnreg_dec<C::kRegCorr>();
     const int t = threadIdx.x & 127;
-    int jn[QT];        // next step of tile i
-    bool have[QT];     // alpha_i(jn) read, waiting for the previous P.V
+    int jn[QT];     // next step of tile i
+    bool have[QT];  // alpha_i(jn) read, waiting for the previous P.V
+    bool fin[QT];   // tile i finished
     float alpha_r[QT];
 #pragma unroll
     for (int i = 0; i < QT; ++i) {
       jn[i] = 0;
       have[i] = false;
+      fin[i] = false;
       alpha_r[i] = 1.f;
     }
     auto probe = [&](uint32_t bar, uint32_t parity) {
@@ -473,10 +700,15 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
 #pragma unroll
       for (int i = 0; i < QT; ++i) {
         const int j = jn[i];
-        if (j >= n_i[i]) continue;
+        if (fin[i]) continue;
         done = false;
         if (!have[i]) {
           if (!probe(bar_alpha + 8 * i, j & 1)) {
+            continue;
+          }
+          if (*reinterpret_cast<volatile int*>(&ctl->corr_stop[i])) {
+            fin[i] = true;
+            progressed = true;
             continue;
           }
           alpha_r[i] = ctl->alpha[i][t];
@@ -545,168 +777,209 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
     const uint32_t tS = tmem + lane_off + C::kSCol + (C::kSharedS ? 0 : i * BC);
     const uint32_t tP = tmem + lane_off + C::kPCol + i * C::kPCols;
     const uint32_t tO = tmem + lane_off + C::kOCol + i * D;
-    const int row = row0 + C::kBr * i + t;
-    const int n = n_i[i];
     const float c = p.scale_log2;
-    // The row sits at key position rq = row + Nk - Nq; keys visible to it are
-    // [rq - wl, rq + wr] within [0, Nk), a -1 bound leaving that side open.
-    // (|rq| < 2^30 and wl, wr <= 2^30, so the sums below stay within int.)
-    // K/V tiles [jf_b, jf_e) hold only keys that every row of this query tile
-    // sees; they skip the mask (a test uniform across the warpgroup).
-    const int rq = row + off;
-    int jf_b = 0, jf_e;
-    {
-      const int tr_first = row0 + C::kBr * i + off;
-      const int tr_last = min(row0 + C::kBr * (i + 1), p.Nq) - 1 + off;
-      if (p.wl >= 0) {
-        const int lo = tr_last - p.wl;  // highest first-visible key of the tile's rows
-        jf_b = lo <= 0 ? 0 : (lo + BC - 1) / BC;
+    const int off = p.Nk - p.Nq;
+    int cs = 0;            // steps of this tile in earlier items (s_full, pv_ready, o_done phases)
+    bool stg_pending = false;  // thread 0: a TMA store from the staging buffer may still read it
+    uint32_t g_sp = 0;     // ring position of the item's first K tile: stage | parity << 8
+    for (int r = 0; r < rounds; ++r) {
+      const int idx = item_of_round(r, p);
+      if (idx < 0) continue;
+      // Only what the step loop needs stays live through it; the epilogue
+      // decodes the item again.
+      int n, cta_b, row0;
+      {
+        Item<QT> it;
+        make_item<BC, QT>(idx, p, it);
+        n = pick<QT>(it.n, i);
+        cta_b = it.cta_b;
+        row0 = it.row0 + C::kBr * i;  // first row of this tile
       }
-      const int hi = p.wr < 0 ? p.Nk - 1 : min(p.Nk - 1, tr_first + p.wr);  // lowest last-visible key
-      jf_e = hi < 0 ? 0 : (hi + 1) / BC;
-    }
-
-    bool ok = true;
-    float m = -INFINITY;
-    float l = 0.f;
-    // bf16: sum over the tiles of bf16(P) - P at each tile's max element,
-    // rescaled like l.  O is normalised by l + l_fix, so the largest weights
-    // of a row enter O and its normaliser with the same rounding; LSE uses l.
-    float l_fix = 0.f;
-    for (int jj = 0; ok && jj < n; ++jj) {
-      const int j = cta_b + jj;
-      if (!warp_wait(bar_s + 8 * i, jj & 1, wc)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-
-      uint32_t r[BC];
-      if constexpr (BC == 128)
-        tmem_ld64x2_sync(tS, tS + 64, r);
-      else
-        tmem_ld64_sync(tS, r);
-      tc_fence_before();
-      mbar_arrive(bar_sfree + 8 * i);  // the S buffer may take the next product
-      float s[BC];
-#pragma unroll
-      for (int cc = 0; cc < BC; ++cc) s[cc] = __uint_as_float(r[cc]);
-      if (j < jf_b || j >= jf_e) {  // key-axis tail, causal diagonal, window edge
-        const int key0 = j * BC;
-        const int lim = p.wr < 0 ? p.Nk - 1 : min(p.Nk - 1, rq + p.wr);
-        const int lim_lo = p.wl < 0 ? 0 : rq - p.wl;
-#pragma unroll
-        for (int cc = 0; cc < BC; ++cc)
-          if (key0 + cc > lim || key0 + cc < lim_lo) s[cc] = -INFINITY;
+      const int row = row0 + t;
+      // The row sits at key position rq = row + Nk - Nq; keys visible to it are
+      // [rq - wl, rq + wr] within [0, Nk), a -1 bound leaving that side open.
+      // (|rq| < 2^30 and wl, wr <= 2^30, so the sums below stay within int.)
+      // K/V tiles [jf_b, jf_e) hold only keys that every row of this query tile
+      // sees; they skip the mask (a test uniform across the warpgroup).
+      const int rq = row + off;
+      int jf_b = 0, jf_e;
+      {
+        const int tr_first = row0 + off;
+        const int tr_last = min(row0 + C::kBr, p.Nq) - 1 + off;
+        if (p.wl >= 0) {
+          const int lo = tr_last - p.wl;  // highest first-visible key of the tile's rows
+          jf_b = lo <= 0 ? 0 : (lo + BC - 1) / BC;
+        }
+        const int hi = p.wr < 0 ? p.Nk - 1 : min(p.Nk - 1, tr_first + p.wr);  // lowest last-visible key
+        jf_e = hi < 0 ? 0 : (hi + 1) / BC;
       }
 
-      // m' = max(m, rowmax S): four independent chains of three-input max
-      float mx[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) mx[u] = fmaxf(s[2 * u], s[2 * u + 1]);
-#pragma unroll
-      for (int cc = 8; cc < BC; cc += 2) mx[(cc >> 1) & 3] = max3f(mx[(cc >> 1) & 3], s[cc], s[cc + 1]);
-      // The reference m moves to the tile's max only when that lies more
-      // than C::kLazy (base-2 exponent units) above it, so P stays within
-      // [0, 2^kLazy] and most steps leave O alone (alpha = 1).  The final
-      // O / l and LSE = m scale + ln l are the same for any reference.
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      const bool bump = mt > m && (m == -INFINITY || (mt - m) * c > C::kLazy);
-      const float m_new = bump ? mt : m;
-      const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = bump ? ex2_approx((m - m_ref) * c) : 1.f;
-      if constexpr (C::kCorr) {
-        // The correction must have read alpha_i(j-1) before the slot is reused
-        // (S_i(j) was issued before it ran, so this step can be ahead of it).
-        if (jj > 0 && !warp_wait(bar_afree + 8 * i, (jj - 1) & 1, wc)) {
+      bool ok = true;
+      float m = -INFINITY;
+      float l = 0.f;
+      // bf16: sum over the tiles of bf16(P) - P at each tile's max element,
+      // rescaled like l.  O is normalised by l + l_fix, so the largest weights
+      // of a row enter O and its normaliser with the same rounding; LSE uses l.
+      float l_fix = 0.f;
+      for (int jj = 0; ok && jj < n; ++jj) {
+        const int j = cta_b + jj;
+        if (!warp_wait(bar_s + 8 * i, (cs + jj) & 1, wc)) {
           ok = false;
           break;
         }
-        ctl->alpha[i][t] = alpha;  // the correction warpgroup rescales O_i by it
-        mbar_arrive(bar_alpha + 8 * i);
-      }
+        tc_fence_after();
 
-      // P = 2^(s*c - m_ref*c) (packed FFMA, then EX2); rowsum of the fp32 P
-      // (before the cast to bf16 / E4M3) in four packed partial sums.  FP8:
-      // Max_offset = 8 ("Online Softmax 算法详解" section 6): P' = 2^8 P, in
-      // [0, 256], to use the E4M3 range; the sum of P' is scaled back by 2^-8
-      // at the end and O by final_scale.
-      const uint64_t c2 = f2_pack(c, c);
-      const float neg = -m_ref * c + (F8 ? 8.f : 0.f);
-      const uint64_t neg2 = f2_pack(neg, neg);
-      float dfix = 0.f;
-      if constexpr (!F8) {
-        // P at the tile's max element, as the loop below computes it, and its
-        // bf16 rounding (0 for a fully masked tile: 2^-inf).
-        const float pm = ex2_approx(fmaf(mt, c, neg));
-        dfix = __uint_as_float(pack_bf16x2(0.f, pm) & 0xFFFF0000u) - pm;
-      }
-      uint64_t ls[4];
+        uint32_t rg[BC];
+        if constexpr (BC == 128)
+          tmem_ld64x2_sync(tS, tS + 64, rg);
+        else
+          tmem_ld64_sync(tS, rg);
+        tc_fence_before();
+        mbar_arrive(bar_sfree + 8 * i);  // the S buffer may take the next product
+        float s[BC];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) ls[u] = 0ull;
-      uint32_t pk[BC / (4 / C::kEs)];  // bf16 pairs or E4M3 quads
+        for (int cc = 0; cc < BC; ++cc) s[cc] = __uint_as_float(rg[cc]);
+        if (j < jf_b || j >= jf_e) {  // key-axis tail, causal diagonal, window edge
+          const int key0 = j * BC;
+          const int lim = p.wr < 0 ? p.Nk - 1 : min(p.Nk - 1, rq + p.wr);
+          const int lim_lo = p.wl < 0 ? 0 : rq - p.wl;
 #pragma unroll
-      for (int cc = 0; cc < BC; cc += 4) {
-        float x0, x1, x2, x3;
-        f2_unpack(ffma2(f2_pack(s[cc], s[cc + 1]), c2, neg2), x0, x1);
-        f2_unpack(ffma2(f2_pack(s[cc + 2], s[cc + 3]), c2, neg2), x2, x3);
-        const float p0 = ex2_approx(x0);
-        const float p1 = ex2_approx(x1);
-        const float p2 = ex2_approx(x2);
-        const float p3 = ex2_approx(x3);
-        ls[(cc >> 1) & 3] = fadd2(ls[(cc >> 1) & 3], f2_pack(p0, p1));
-        ls[((cc >> 1) + 1) & 3] = fadd2(ls[((cc >> 1) + 1) & 3], f2_pack(p2, p3));
-        if constexpr (F8) {
-          pk[cc >> 2] = pack_e4m3x4(p0, p1, p2, p3);
-        } else {
-          pk[cc >> 1] = pack_bf16x2(p0, p1);
-          pk[(cc >> 1) + 1] = pack_bf16x2(p2, p3);
+          for (int cc = 0; cc < BC; ++cc)
+            if (key0 + cc > lim || key0 + cc < lim_lo) s[cc] = -INFINITY;
         }
-      }
-      float lsum[4];
-      f2_unpack(fadd2(ls[0], ls[1]), lsum[0], lsum[1]);
-      f2_unpack(fadd2(ls[2], ls[3]), lsum[2], lsum[3]);
-      const float rowsum = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
-      // P_i(j) -> TMEM, row t in lane t (the A operand of O_i += P_i(j) V_j),
-      // once O_i += P_i(j-1) V_{j-1} has finished reading the columns.
-      if (jj > 0 && !warp_wait(bar_o + 8 * i, (jj - 1) & 1, wc)) {
-        ok = false;
-        break;
-      }
-      if constexpr (!C::kCorr) {
-        // O_i <- alpha O_i for this warp's 32 rows, now that O_i += P_i(j-1)
-        // V_{j-1} has landed; rare, as the reference seldom moves.
-        if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          tc_fence_after();
-          const uint64_t a2 = f2_pack(alpha, alpha);
+
+        // m' = max(m, rowmax S): four independent chains of three-input max
+        float mx[4];
 #pragma unroll
-          for (int cc = 0; cc < D; cc += 32) {
-            uint32_t o[32];
-            tmem_ld32_sync(tO + cc, o);
+        for (int u = 0; u < 4; ++u) mx[u] = fmaxf(s[2 * u], s[2 * u + 1]);
 #pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              float y0, y1;
-              f2_unpack(fmul2(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), a2), y0, y1);
-              o[k] = __float_as_uint(y0);
-              o[k + 1] = __float_as_uint(y1);
-            }
-            tmem_st32(tO + cc, o);
+        for (int cc = 8; cc < BC; cc += 2) mx[(cc >> 1) & 3] = max3f(mx[(cc >> 1) & 3], s[cc], s[cc + 1]);
+        // The reference m moves to the tile's max only when that lies more
+        // than C::kLazy (base-2 exponent units) above it, so P stays within
+        // [0, 2^kLazy] and most steps leave O alone (alpha = 1).  The final
+        // O / l and LSE = m scale + ln l are the same for any reference.
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        const bool bump = mt > m && (m == -INFINITY || (mt - m) * c > C::kLazy);
+        const float m_new = bump ? mt : m;
+        const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = bump ? ex2_approx((m - m_ref) * c) : 1.f;
+        if constexpr (C::kCorr) {
+          // The correction must have read the previous alpha_i before the slot
+          // is reused (S_i(j) was issued before it ran, so this step can be
+          // ahead of it).
+          if (cs + jj > 0 && !warp_wait(bar_afree + 8 * i, (cs + jj - 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          // the correction warpgroup rescales O_i by it (not at an item's
+          // first step: that product overwrites O_i)
+          ctl->alpha[i][t] = jj == 0 ? 1.f : alpha;
+          mbar_arrive(bar_alpha + 8 * i);
+        }
+
+        // P = 2^(s*c - m_ref*c) (packed FFMA, then EX2); rowsum of the fp32 P
+        // (before the cast to bf16 / E4M3) in four packed partial sums.  FP8:
+        // Max_offset = 8 ("Online Softmax 算法详解" section 6): P' = 2^8 P, in
+        // [0, 256], to use the E4M3 range; the sum of P' is scaled back by 2^-8
+        // at the end and O by final_scale.
+        const uint64_t c2 = f2_pack(c, c);
+        const float neg = -m_ref * c + (F8 ? 8.f : 0.f);
+        const uint64_t neg2 = f2_pack(neg, neg);
+        float dfix = 0.f;
+        if constexpr (!F8) {
+          // P at the tile's max element, as the loop below computes it, and its
+          // bf16 rounding (0 for a fully masked tile: 2^-inf).
+          const float pm = ex2_approx(fmaf(mt, c, neg));
+          dfix = __uint_as_float(pack_bf16x2(0.f, pm) & 0xFFFF0000u) - pm;
+        }
+        uint64_t ls[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ls[u] = 0ull;
+        uint32_t pk[BC / (4 / C::kEs)];  // bf16 pairs or E4M3 quads
+#pragma unroll
+        for (int cc = 0; cc < BC; cc += 4) {
+          float x0, x1, x2, x3;
+          f2_unpack(ffma2(f2_pack(s[cc], s[cc + 1]), c2, neg2), x0, x1);
+          f2_unpack(ffma2(f2_pack(s[cc + 2], s[cc + 3]), c2, neg2), x2, x3);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          const float p2 = ex2_approx(x2);
+          const float p3 = ex2_approx(x3);
+          ls[(cc >> 1) & 3] = fadd2(ls[(cc >> 1) & 3], f2_pack(p0, p1));
+          ls[((cc >> 1) + 1) & 3] = fadd2(ls[((cc >> 1) + 1) & 3], f2_pack(p2, p3));
+          if constexpr (F8) {
+            pk[cc >> 2] = pack_e4m3x4(p0, p1, p2, p3);
+          } else {
+            pk[cc >> 1] = pack_bf16x2(p0, p1);
+            pk[(cc >> 1) + 1] = pack_bf16x2(p2, p3);
           }
         }
-      }
+        float lsum[4];
+        f2_unpack(fadd2(ls[0], ls[1]), lsum[0], lsum[1]);
+        f2_unpack(fadd2(ls[2], ls[3]), lsum[2], lsum[3]);
+        const float rowsum = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+        // P_i(j) -> TMEM, row t in lane t (the A operand of O_i += P_i(j) V_j),
+        // once O_i += P_i(j-1) V_{j-1} has finished reading the columns.
+        if (jj > 0 && !warp_wait(bar_o + 8 * i, (cs + jj - 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        if constexpr (!C::kCorr) {
+          // O_i <- alpha O_i for this warp's 32 rows, now that O_i += P_i(j-1)
+          // V_{j-1} has landed; rare, as the reference seldom moves.
+          if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            tc_fence_after();
+            const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-      for (int u = 0; u < C::kPCols; u += 32) tmem_st32(tP + u, pk + u);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_pv + 8 * i);
-      l = alpha * l + rowsum;
-      l_fix = alpha * l_fix + dfix;
-      m = m_new;
-    }
-    if (ok && n > 0) ok = warp_wait(bar_o + 8 * i, (n - 1) & 1, wc);
-    const bool bad = named_bar_or(1 + i, 128, !ok || *wc.abort);
-    // A tile that starts past the last query row has nothing to write.
-    if (!bad && row0 + C::kBr * i < p.Nq) {
+            for (int cc = 0; cc < D; cc += 32) {
+              uint32_t o[32];
+              tmem_ld32_sync(tO + cc, o);
+#pragma unroll
+              for (int k = 0; k < 32; k += 2) {
+                float y0, y1;
+                f2_unpack(fmul2(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), a2), y0, y1);
+                o[k] = __float_as_uint(y0);
+                o[k + 1] = __float_as_uint(y1);
+              }
+              tmem_st32(tO + cc, o);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < C::kPCols; u += 32) tmem_st32(tP + u, pk + u);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_pv + 8 * i);
+        l = alpha * l + rowsum;
+        l_fix = alpha * l_fix + dfix;
+        m = m_new;
+      }
+      if (ok && n > 0) ok = warp_wait(bar_o + 8 * i, (cs + n - 1) & 1, wc);
+      cs += n;
+      Item<QT> it;
+      make_item<BC, QT>(idx, p, it);
+      const int bh = it.bh;
+      // this tile's O staging slot (after the item's K/V tiles), then the next
+      // item's ring base
+      RingPos slot;
+      {
+        int g_stage = static_cast<int>(g_sp & 0xffu);
+        uint32_t g_par = g_sp >> 8;
+        slot = ring_at<C::kStages>(g_stage, g_par, 2 * it.n_cta + i);
+        bool oslot;
+        ring_advance<C::kStages>(g_stage, g_par, item_positions<C::kSlotStg, QT>(it, p, oslot));
+        g_sp = static_cast<uint32_t>(g_stage) | (g_par << 8);
+      }
+      // The previous item's O store must have read the staging buffer before
+      // it is written again (the barrier below orders that for the others).
+      if (C::kOwnStg && stg_pending && t == 0) {
+        tma_store_wait_read();
+        stg_pending = false;
+      }
+      const bool bad = named_bar_or(1 + i, 128, !ok || *wc.abort);
+      if (bad) break;
+      // A tile that starts past the last query row has nothing to write.
+      if (row0 >= p.Nq) continue;
       if (n > 0) tc_fence_after();
       const bool empty = !(l > 0.f);
       // FP8: sum_scale l <- l 2^-8 undoes Max_offset in the row sum, and
@@ -715,53 +988,73 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       const float lc = F8 ? l * (1.f / 256.f) : l;
       const float inv = empty ? 0.f : (F8 ? p.o_scale / lc : 1.f / (l + l_fix));
       if (!p.partial) {
-        // bf16 O, staged in this tile's (now unused) Q buffer with the 128-byte
-        // swizzle, then TMA stores (rows past Nq are clipped by the map).  The
-        // FP8 Q buffer holds one 64-column chunk of bf16 O at a time.
-        const uint32_t stg = smem_u32(sQ + i * C::kQTileBytes);
-        constexpr int kOChunks = D / 64;
-        constexpr int kStageChunks = F8 ? 1 : kOChunks;  // O chunks staged per round
+        if (n == 0) {
+          // no visible key: O = 0 straight to global memory (the staging
+          // buffers may be in use by the next item's loads)
+          if (row < p.Nq) {
+            uint8_t* orow = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + row) * (D * 2);
 #pragma unroll
-        for (int round = 0; round < kOChunks / kStageChunks; ++round) {
-#pragma unroll
-        for (int cc = round * 64 * kStageChunks; cc < (round + 1) * 64 * kStageChunks; cc += 32) {
-          uint32_t o[32];
-          if (n > 0) {
-            tmem_ld32_sync(tO + cc, o);
+            for (int q = 0; q < D * 2 / 16; ++q) st_global_v4(orow + 16 * q, 0u, 0u, 0u, 0u);
+          }
+        } else {
+          // bf16 O, staged with the 128-byte swizzle, then TMA stores (rows past
+          // Nq are clipped by the map): all of O at once in the tile's ring
+          // slot, or 64 columns per round through its own 16 KB buffer.
+          uint32_t stg;
+          constexpr int kRounds = C::kSlotStg ? 1 : D / 64;
+          if constexpr (C::kSlotStg) {
+            // every warp of the tile agrees before any of them leaves
+            const bool got = warp_wait(bar_kv_full + 8 * slot.stage, slot.par, wc);
+            if (named_bar_or(1 + i, 128, !got)) break;
+            stg = smem_u32(sKV + slot.stage * C::kKVTileBytes);
           } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = 0u;
+            stg = smem_u32(sStg + i * C::kStgBytes);
           }
-          uint32_t w[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
-          const int chunk = cc / 64 - round * kStageChunks;
-          const int u0 = (cc % 64) / 8;
+          for (int round = 0; round < kRounds; ++round) {
+            if (round > 0) {  // staging buffer free again
+              if (t == 0) tma_store_wait_read();
+              named_bar_sync(1 + i, 128);
+            }
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int u = u0 + q;
-            st_shared_v4(stg + chunk * C::kQChunkBytes + t * 128 + ((u ^ (t & 7)) << 4), w[4 * q],
-                         w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            for (int ch = 0; ch < D / 64 / kRounds; ++ch) {  // 64-column chunks of this round
+              const int col = (round * (D / 64 / kRounds) + ch) * 64;
+              uint32_t o[64];
+              tmem_ld64_sync(tO + col, o);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                uint32_t wv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  wv[k] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * k]) * inv,
+                                      __uint_as_float(o[8 * q + 2 * k + 1]) * inv);
+                st_shared_v4(stg + ch * C::kStgBytes + t * 128 + ((q ^ (t & 7)) << 4), wv[0], wv[1],
+                             wv[2], wv[3]);
+              }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1 + i, 128);
+            if (t == 0) {
+#pragma unroll
+              for (int ch = 0; ch < D / 64 / kRounds; ++ch)
+                tma_store_3d(&tm_o, stg + ch * C::kStgBytes, (round * (D / 64 / kRounds) + ch) * 64, row0, bh);
+              tma_store_commit();
+            }
           }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1 + i, 128);
-        if (t == 0) {
-#pragma unroll
-          for (int ch = 0; ch < kStageChunks; ++ch)
-            tma_store_3d(&tm_o, stg + ch * C::kQChunkBytes, (round * kStageChunks + ch) * 64,
-                         row0 + C::kBr * i, bh);
-          tma_store_commit();
-          tma_store_wait_read();
-        }
-        if (kStageChunks < kOChunks) named_bar_sync(1 + i, 128);  // staging buffer free again
+          if (t == 0) {
+            if constexpr (C::kOwnStg) {
+              stg_pending = true;  // waited for before the next use
+            } else {
+              tma_store_wait_read();
+              mbar_arrive(bar_kv_empty + 16 * slot.stage + 8 * i);  // the slot goes back to the ring
+            }
+          }
         }
         if (row < p.Nq)
           p.lse[static_cast<size_t>(bh) * p.Nq + row] = empty ? -INFINITY : m * p.scale + logf(lc);
       } else {
         // fp32 partial triple (m in natural-log units, l, O/l) for the merge.
-        const size_t prow = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + row;
+        const size_t prow = (static_cast<size_t>(it.split) * p.BH + bh) * p.Nq + row;
         if (row < p.Nq) {
           p.m_part[prow] = empty ? -INFINITY : m * p.scale;
           p.l_part[prow] = empty ? 0.f : l;
@@ -784,6 +1077,16 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
               st_global_v4(op + cc + 4 * q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
           }
         }
+      }
+    }
+    if (C::kOwnStg && stg_pending && t == 0) tma_store_wait_read();
+    if constexpr (C::kCorr) {
+      // Tell the correction this tile is finished: one more alpha phase, with
+      // the stop flag set, once it has read the last alpha.
+      const bool ok2 = !*wc.abort && (cs == 0 || warp_wait(bar_afree + 8 * i, (cs - 1) & 1, wc));
+      if (!named_bar_or(1 + i, 128, !ok2)) {
+        if (t == 0) *reinterpret_cast<volatile int*>(&ctl->corr_stop[i]) = 1;
+        mbar_arrive(bar_alpha + 8 * i);  // after the flag store (release)
       }
     }
   }

@@ -16,8 +16,32 @@ enum : int {
   kDevTimeout = 1,  // a bounded mbarrier wait ran out; the CTA stopped cleanly
 };
 
+// Default K/V tile (keys per tile): split-KV ranges are counted in these.
+constexpr int kDefaultBc = 128;
+
+// Division of 0 <= n < 2^31 by a divisor fixed at launch, as a multiply-high
+// and a shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994): q = (mulhi(n, mul) + n) >> shift.
+struct FastDiv {
+  unsigned int mul;
+  unsigned int shift;
+  int d;
+};
+
+inline FastDiv make_fastdiv(int d) {
+  FastDiv f{0u, 0u, d};
+  unsigned int s = 0;
+  while ((1ull << s) < static_cast<unsigned long long>(d)) ++s;  // s = ceil(log2 d)
+  f.shift = s;
+  f.mul = static_cast<unsigned int>(((1ull << 32) * ((1ull << s) - static_cast<unsigned long long>(d))) /
+                                        static_cast<unsigned long long>(d) + 1ull);
+  return f;
+}
+
 struct FwdParams {
-  // n_splits == 1: final outputs.  o is written by TMA through the O map.
+  // n_splits == 1: final outputs.  o is written by TMA through the O map (rows
+  // with no visible key are zeroed through this pointer).
+  void* o;     // bf16 [B*H][Nq][d]
   float* lse;  // [B*H][Nq]
   // partial != 0: write partial triples instead, index ((split * BH + bh) * Nq + row).
   int partial;
@@ -28,7 +52,17 @@ struct FwdParams {
   int n_splits;
   int tiles_per_split;  // K/V tiles per split
   int kv_tiles;         // ceil(Nk / BC)
-  int causal;        // launch order only: heaviest query tiles first
+  // Work items of one launch of the persistent grid: (query-tile group, split,
+  // head) for heads [bh0, bh0 + n_bh) and splits [split0, split0 + n_split);
+  // the host keeps n_items below 2^31 by cutting a launch into several.
+  int n_items;          // n_qg * n_split * n_bh
+  int rounds;           // ceil(n_items / grid size)
+  int n_qg;             // groups of QT query tiles per head
+  int bh0, n_bh;
+  int split0, n_split;
+  FastDiv div_qg, div_split, div_per;  // by n_qg, n_split, n_split * n_bh
+  int qg_major;         // 1: item index = (group, head, split), else (head, split, group)
+  int qg_desc;          // 1: groups in descending order (later groups see more keys)
   int wl, wr;        // visible keys [r + off - wl, r + off + wr]; -1 = open side
   float scale;       // natural-units logit scale
   float scale_log2;  // scale * log2(e)

@@ -52,8 +52,8 @@ extern "C" int fa_fwd_split_noalloc(const void* q, const void* k, const void* v,
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(o) & 15) || (reinterpret_cast<uintptr_t>(lse) & 3))
     return FA_ERR_INVALID_ARG;
-  // Same split count as fa_fwd: at most one split per 128-key tile.
-  const int kv_tiles = (Nk + 127) / 128;
+  // Same split count as fa_fwd: at most one split per K/V tile of the default size.
+  const int kv_tiles = (Nk + fa::kDefaultBc - 1) / fa::kDefaultBc;
   const int splits = n_splits < kv_tiles ? n_splits : kv_tiles;
   if (splits < 2) return fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, 1, stream);
   const size_t rows = static_cast<size_t>(B) * H * Nq;

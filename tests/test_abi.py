@@ -25,7 +25,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_strerror(L):
-    assert fa.version() == 100
+    assert fa.version() == 101
     for code in (fa.FA_OK, fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED, fa.FA_ERR_CUDA,
                  fa.FA_ERR_DEVICE_TIMEOUT, fa.FA_ERR_NO_MEMORY, -99):
         s = fa.strerror(code)

@@ -51,6 +51,42 @@ def test_small_shapes_all_rows(B, H, Nq, Nk, d, causal, n_splits, bc, qt):
     print(diff.check(w.name))
 
 
+# Persistent grid: with at most 1-3 CTAs, each walks many work items, carrying
+# TMEM, barrier phases, the K/V ring and the Q / staging buffers across them.
+# Same arithmetic per item, so the result must equal the one-CTA-per-SM
+# launch bit for bit, and match the oracle.
+PERSIST = [
+    # B, H, Nq, Nk, d, causal, n_splits, bc, qt
+    (1, 3, 300, 700, 128, True, 1, 0, 0),
+    (2, 3, 200, 300, 64, False, 1, 0, 0),
+    (1, 2, 513, 513, 128, True, 1, 64, 0),
+    (2, 1, 300, 700, 64, False, 4, 0, 0),
+    (1, 1, 330, 130, 128, True, 2, 0, 0),     # masked rows, empty splits
+    (1, 2, 256, 512, 64, True, 1, 0, 1),
+    (1, 2, 257, 129, 64, True, 1, 0, 0),      # items whose tiles see no key
+    (1, 2, 640, 900, 128, False, 1, 0, 0),
+]
+
+
+@pytest.mark.parametrize("max_ctas", [1, 2, 3])
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal,n_splits,bc,qt", PERSIST,
+                         ids=[f"b{c[0]}h{c[1]}q{c[2]}k{c[3]}d{c[4]}{'c' if c[5] else ''}s{c[6]}bc{c[7]}qt{c[8]}"
+                              for c in PERSIST])
+def test_persistent_items_per_cta(B, H, Nq, Nk, d, causal, n_splits, bc, qt, max_ctas):
+    w = workloads.custom(B, H, Nq, Nk, d, seed=Nq * 5 + Nk + max_ctas, causal=causal,
+                         n_splits=n_splits, bc=bc, q_mult=2.0)
+    q, k, v = workloads.generate(w, device="cuda")
+    o0, l0 = fa.fwd(q, k, v, w.scale, causal, n_splits, bc=bc, q_tiles_per_cta=qt)
+    o1 = torch.full_like(q, float("nan"))
+    l1 = torch.full((B, H, Nq), float("nan"), device="cuda")
+    fa.fwd(q, k, v, w.scale, causal, n_splits, out=o1, lse=l1, bc=bc, q_tiles_per_cta=qt,
+           max_ctas=max_ctas)
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FA_OK
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    print(P.compare(q, k, v, o1, l1, w.scale, causal).check(f"{w.name} max_ctas={max_ctas}"))
+
+
 def test_large_logits_and_growing_max():
     # Logits far above the fp16 overflow point and a running max that grows
     # along the key axis: exercises every rescale path.
