@@ -74,6 +74,10 @@
 #include "fa_ptx.cuh"
 #include "fa_wait.cuh"
 
+#ifndef FA_STAGGER
+#define FA_STAGGER 1
+#endif
+
 namespace fa {
 
 // F8: Q, K, V and P are FP8 E4M3 (one byte per element) and the products use
@@ -127,6 +131,11 @@ struct FwdCfg {
   // Each tile has its own S buffer where that fits in 512 columns; otherwise
   // one S buffer that the tiles take in turn.
   static constexpr bool kSharedS = QT * (BC + kPCols + D) > 512;
+  // Two tiles with S buffers of their own would run their softmax steps in
+  // lockstep (both S products land together); tile 1 starts each item once
+  // tile 0 has its first row maxima, so one tile's exponentials overlap the
+  // other's loads and reductions.
+  static constexpr bool kStagger = FA_STAGGER != 0 && QT == 2 && !kSharedS;
   static constexpr int kSBufs = kSharedS ? 1 : QT;
   static constexpr int kSCol = 0;
   static constexpr int kPCol = kSBufs * BC;
@@ -173,6 +182,7 @@ struct __align__(8) Ctl {
   uint64_t pv_ready[2];     // P_i(j) in TMEM and O_i rescaled (128 softmax [+ 128 correction] arrivals)
   uint64_t o_done[2];       // O_i += P_i(j) V_j completed (MMA commit)
   uint64_t drain[2];        // every MMA of tile i's issuer has completed
+  uint64_t stagger;         // tile 0 has its first row maxima of the item (kStagger)
   uint32_t tmem_base;
   int abort;
   int corr_stop[2];         // tile i has no more steps (E4M3 correction)
@@ -373,6 +383,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       mbar_init(bar_o + 8 * i, 1);
       mbar_init(bar_drain + 8 * i, 1);
     }
+    mbar_init(smem_u32(&ctl->stagger), 128);
     ctl->abort = 0;
     ctl->corr_stop[0] = ctl->corr_stop[1] = 0;
     fence_mbar_init();
@@ -547,6 +558,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       int g_stage = 0;
       uint32_t g_par = 0;
       int last_t = -1, last_c = 0;
+      int stag = 0;  // stagger phases waited for (tile 1)
       bool ok = true, issued = false;
       for (int r = 0; ok && r < rounds; ++r) {
         const int idx = item_of_round(r, p);
@@ -623,6 +635,12 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
           // which comes before P_i(j) is ready.
           ok = warp_wait(bar_qf + 8 * i, q_loads & 1, wc) && s_ready(0) && kv_ready(ring_pos_k(0));
           ++q_loads;
+          if constexpr (C::kStagger) {
+            if (i == 1 && n_ot > 0) {
+              ok = ok && warp_wait(smem_u32(&ctl->stagger), stag & 1, wc);
+              ++stag;
+            }
+          }
           if (ok) {
             tc_fence_after();
             issue_qk(0);
@@ -788,12 +806,14 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       // Only what the step loop needs stays live through it; the epilogue
       // decodes the item again.
       int n, cta_b, row0;
+      bool stagger = false;  // tile 0 releases tile 1's first S product of the item
       {
         Item<QT> it;
         make_item<BC, QT>(idx, p, it);
         n = pick<QT>(it.n, i);
         cta_b = it.cta_b;
         row0 = it.row0 + C::kBr * i;  // first row of this tile
+        if constexpr (C::kStagger) stagger = i == 0 && it.n[1] > 0;
       }
       const int row = row0 + t;
       // The row sits at key position rq = row + Nk - Nq; keys visible to it are
@@ -859,6 +879,9 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
         // [0, 2^kLazy] and most steps leave O alone (alpha = 1).  The final
         // O / l and LSE = m scale + ln l are the same for any reference.
         const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        if constexpr (C::kStagger) {
+          if (stagger && jj == 0) mbar_arrive(smem_u32(&ctl->stagger));
+        }
         const bool bump = mt > m && (m == -INFINITY || (mt - m) * c > C::kLazy);
         const float m_new = bump ? mt : m;
         const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;

@@ -76,28 +76,51 @@ def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
     return np.where(ax > 0, np.exp2(e - 8), 0.0)
 
 
+def compare_many(q, k, v, outs, scale, causal, heads=None, rows=None, threads=None,
+                 window=None) -> list[Diff]:
+    """outs: list of (o, lse) pairs for the same q, k, v; one oracle run per
+    head serves all of them.  q/k/v/o: [B,H,N,d] (any device), lse [B,H,Nq];
+    heads: list of (b,h).  A bf16 `o` is compared with the half-ulp storage
+    allowance, fp32 `o` without.  window=(wl, wr): the oracle's local mask
+    instead of `causal`."""
+    diffs = [Diff() for _ in outs]
+    B, H = q.shape[0], q.shape[1]
+    every = heads is None
+    heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    # every head: one copy of each tensor to the host; a few heads: per head
+    host = (lambda t: t.cpu()) if every else (lambda t: t)
+    qc, kc, vc = host(q), host(k), host(v)
+    outs_c = [(host(o), host(lse), o.dtype == torch.bfloat16) for o, lse in outs]
+    for (b, h) in heads:
+        qh, kh, vh = qc[b, h].cpu(), kc[b, h].cpu(), vc[b, h].cpu()
+        if window is None:
+            o_ref, lse_ref = oracle.attention(qh, kh, vh, scale, causal, rows=rows, threads=threads)
+        else:
+            o_ref, lse_ref = oracle.attention_window(qh, kh, vh, scale, window[0], window[1], rows=rows,
+                                                     threads=threads)
+        for diff, (o, lse, bf16_out) in zip(diffs, outs_c):
+            og = o[b, h].cpu().double().numpy()
+            lg = lse[b, h].cpu().double().numpy()
+            if rows is not None:
+                og, lg = og[rows], lg[rows]
+            diff.add(og, lg, o_ref, lse_ref, bf16_output=bf16_out)
+    return diffs
+
+
 def compare(q, k, v, o, lse, scale, causal, heads=None, rows=None, diff: Diff | None = None,
             threads=None, window=None) -> Diff:
-    """q/k/v/o: [B,H,N,d] (any device), lse [B,H,Nq].  heads: list of (b,h).
-    A bf16 `o` is compared with the half-ulp storage allowance, fp32 `o` without.
-    window=(wl, wr): the oracle's local mask instead of `causal`."""
-    diff = diff or Diff()
-    bf16_out = (o.dtype == torch.bfloat16)
-    B, H = q.shape[0], q.shape[1]
-    heads = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
-    for (b, h) in heads:
-        if window is None:
-            o_ref, lse_ref = oracle.attention(q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu(), scale,
-                                              causal, rows=rows, threads=threads)
-        else:
-            o_ref, lse_ref = oracle.attention_window(q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu(),
-                                                     scale, window[0], window[1], rows=rows,
-                                                     threads=threads)
-        og = o[b, h].cpu().double().numpy()
-        lg = lse[b, h].cpu().double().numpy()
-        if rows is not None:
-            og, lg = og[rows], lg[rows]
-        diff.add(og, lg, o_ref, lse_ref, bf16_output=bf16_out)
+    """One output pair against the oracle (see compare_many)."""
+    d = compare_many(q, k, v, [(o, lse)], scale, causal, heads=heads, rows=rows, threads=threads,
+                     window=window)[0]
+    if diff is None:
+        return d
+    diff.max_o = max(diff.max_o, d.max_o)
+    diff.max_o_raw = max(getattr(diff, "max_o_raw", 0.0), getattr(d, "max_o_raw", 0.0))
+    diff.sum_o += d.sum_o
+    diff.n_o += d.n_o
+    diff.max_lse = max(diff.max_lse, d.max_lse)
+    diff.rows += d.rows
+    diff.masked_rows += d.masked_rows
     return diff
 
 
@@ -111,22 +134,24 @@ def run_workload(w: workloads.Workload, heads=None, rows=None, n_splits=None, bc
     o, lse = fa.fwd(q, k, v, w.scale, w.causal, ns, bc=bcv, q_tiles_per_cta=qt)
     torch.cuda.synchronize()
     assert fa.device_status() == fa.FA_OK
-    d_bf16 = compare(q, k, v, o, lse, w.scale, w.causal, heads=heads, rows=rows)
+    if not (bcv in (0, 128) and qt == 0):
+        d_bf16 = compare(q, k, v, o, lse, w.scale, w.causal, heads=heads, rows=rows)
+        d_bf16.check(w.name + " (bf16 O)")
+        return d_bf16
+    m_p, l_p, o_p = fa.fwd_partial(q, k, v, 1, w.scale, w.causal)
+    torch.cuda.synchronize()
+    lse32 = torch.where(l_p[0] > 0, m_p[0].double() + torch.log(l_p[0].double()),
+                        torch.full_like(l_p[0], float("-inf"), dtype=torch.float64))
+    d_bf16, d32 = compare_many(q, k, v, [(o, lse), (o_p[0], lse32)], w.scale, w.causal, heads=heads,
+                               rows=rows)
     d_bf16.check(w.name + " (bf16 O)")
-    if bcv in (0, 128) and qt == 0:
-        m_p, l_p, o_p = fa.fwd_partial(q, k, v, 1, w.scale, w.causal)
-        torch.cuda.synchronize()
-        lse32 = torch.where(l_p[0] > 0, m_p[0].double() + torch.log(l_p[0].double()),
-                            torch.full_like(l_p[0], float("-inf"), dtype=torch.float64))
-        d32 = compare(q, k, v, o_p[0], lse32, w.scale, w.causal, heads=heads, rows=rows)
-        d32.check(w.name + " (fp32 O)")
-        if ns == 1:
-            assert torch.equal(o, o_p[0].to(torch.bfloat16)), "bf16 O is not RNE of the fp32 result"
-            fin = torch.isfinite(lse)
-            assert torch.equal(fin, torch.isfinite(lse32))
-            assert (lse[fin].double() - lse32[fin]).abs().max().item() <= 1e-5
-        return d32
-    return d_bf16
+    d32.check(w.name + " (fp32 O)")
+    if ns == 1:
+        assert torch.equal(o, o_p[0].to(torch.bfloat16)), "bf16 O is not RNE of the fp32 result"
+        fin = torch.isfinite(lse)
+        assert torch.equal(fin, torch.isfinite(lse32))
+        assert (lse[fin].double() - lse32[fin]).abs().max().item() <= 1e-5
+    return d32
 
 
 def sample_rows(nq: int, tile: int = 128, extra: int = 64, seed: int = 0) -> list[int]:
