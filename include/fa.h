@@ -249,7 +249,11 @@ size_t fa_split_workspace_bytes(int B, int H, int Nq, int d, int n_splits);
 /*
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT if any kernel of this library
- * recorded a timed-out wait since the last call, or FA_ERR_CUDA.
+ * recorded a timed-out wait since the last call, or FA_ERR_CUDA.  The word is
+ * one per device, shared by every call on that device (all streams, and the
+ * host-buffer entry points, which read it before returning): a timeout from a
+ * kernel on another stream is reported to whichever caller reads the word
+ * first, and reading clears it.
  */
 int fa_get_device_status(void* stream);
 
@@ -261,13 +265,14 @@ const char* fa_strerror(int code);
  * Split-KV forward that allocates nothing.  No counterpart on the source
  * pages: this is a deployment variant of fa_fwd with n_splits > 1.
  *
- * For callers that cannot allocate device memory on this path: code that is
- * replayed from an already-captured CUDA graph, allocator-free runtimes, or
- * hosts whose device memory is owned by their own pool.  fa_fwd takes its
+ * For callers that cannot allocate device memory on this path: runtimes
+ * without a device allocator, hosts whose device memory all belongs to their
+ * own pool (a cudaMalloc there would fail or steal from it), and latency-bound
+ * loops where an allocation could block or synchronise.  fa_fwd takes its
  * split-KV workspace with cudaMallocAsync; this call puts the same partial
  * (m, l, O) triples in a fixed device array of FA_NOALLOC_SCRATCH_BYTES that
  * every GPU loading the library holds until the process exits, then merges
- * them exactly as fa_fwd does (fa_fwd_partial + fa_merge_splits).
+ * them as fa_fwd_partial + fa_merge_splits do.
  *
  * Arguments and results: as fa_fwd (q, k, v, o, lse, sizes, scale, causal,
  * stream), with 2 <= n_splits <= 65535, clamped to ceil(Nk/128) like fa_fwd;
@@ -279,9 +284,12 @@ const char* fa_strerror(int code);
  * No cudaMalloc, cudaFree or other allocating call is made.  The first call
  * on a device looks up the array's device address (cudaGetSymbolAddress,
  * with that device current); make that first call before any stream capture.
- * All calls share the one array and it keeps the last call's contents:
- * calls that may overlap on the GPU (different streams, or different host
- * threads without ordering) race on it and must be serialised by the caller.
+ * Like every entry point, the first call with a given head dimension and
+ * query-tile count also runs the library's one-time kernel set-up (attribute
+ * queries).  All calls share the one array and it keeps the last call's
+ * contents: calls that may overlap on the GPU (different streams, or
+ * different host threads without ordering) race on it and must be
+ * serialised by the caller.
  */
 #define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,

@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "fa.h"
 #include "fa_internal.h"
@@ -129,6 +130,68 @@ cudaError_t launch_fwd(int d, int bc, int qt, const CUtensorMap* maps, const fa:
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// K/V tiles item (query-tile group qg, whole key axis) streams: the host's
+// copy of the kernel's per-item range (make_item), for scheduling only.
+int item_steps(const fa::FwdParams& p, int qt, int qg, int bc) {
+  const int off = p.Nk - p.Nq;
+  int b = p.kv_tiles, e = 0;
+  for (int i = 0; i < qt; ++i) {
+    const int r_first = qg * 128 * qt + 128 * i;
+    if (r_first >= p.Nq) continue;
+    const int r_last = std::min(r_first + 128, p.Nq) - 1;
+    const int klo = p.wl < 0 ? 0 : std::max(0, r_first + off - p.wl);
+    const int khi = p.wr < 0 ? p.Nk - 1 : std::min(p.Nk - 1, r_last + off + p.wr);
+    if (khi < klo) continue;
+    b = std::min(b, klo / bc);
+    e = std::max(e, khi / bc + 1);
+  }
+  return e > b ? e - b : 0;
+}
+
+// Heads per block of the masked order.  A mask makes the query-tile groups'
+// work unequal; the snake deal evens out the CTAs' totals only for some block
+// sizes, and larger blocks keep more heads' K/V live in L2 at once.  The
+// balance of each candidate (powers of two, and all heads) is simulated on the
+// host (the deal is static); among the candidates within 3 % of the best
+// balance, the largest whose K/V fits in 64 MB wins, else the best-balanced.
+int choose_heads_blk(const fa::FwdParams& p, int qt, int bc, int G, long long kv_head) {
+  const int nb = p.n_bh;
+  const long long items = static_cast<long long>(p.n_qg) * p.n_split * nb;
+  if (nb <= 1 || items > (1 << 18) || p.n_split != 1) return nb;
+  std::vector<int> w(p.n_qg);
+  for (int x = 0; x < p.n_qg; ++x) w[x] = item_steps(p, qt, p.qg_desc ? p.n_qg - 1 - x : x, bc) + 2;
+  std::vector<int> cand;
+  for (int hb = 1; hb < nb; hb *= 2) cand.push_back(hb);
+  cand.push_back(nb);
+  std::vector<double> eff(cand.size());
+  std::vector<long long> load(G);
+  double best = 0.0;
+  for (size_t k = 0; k < cand.size(); ++k) {
+    const int hb = cand[k];
+    std::fill(load.begin(), load.end(), 0ll);
+    long long idx = 0, total = 0;
+    for (int b0 = 0; b0 < nb; b0 += hb) {
+      const int hbb = std::min(hb, nb - b0);
+      for (int x = 0; x < p.n_qg; ++x)
+        for (int h = 0; h < hbb; ++h, ++idx) {
+          const long long r = idx / G, c = idx % G;
+          load[(r & 1) ? G - 1 - c : c] += w[x];
+          total += w[x];
+        }
+    }
+    const long long mk = *std::max_element(load.begin(), load.end());
+    eff[k] = mk > 0 ? static_cast<double>(total) / G / mk : 1.0;
+    best = std::max(best, eff[k]);
+  }
+  int pick = -1;
+  for (size_t k = 0; k < cand.size(); ++k)
+    if (eff[k] >= 0.97 * best && cand[k] * kv_head <= (64ll << 20)) pick = static_cast<int>(k);
+  if (pick < 0)
+    for (size_t k = 0; k < cand.size(); ++k)
+      if (eff[k] == best) pick = static_cast<int>(k);
+  return cand[pick];
+}
+
 // Work items of the persistent forward grid: (query-tile group, split, head).
 // A mask makes the query-tile groups' work unequal, so the items then go out
 // group by group, heaviest groups first (with the snake order of the CTAs the
@@ -139,11 +202,13 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // that many items).  The grid has one CTA per SM (max_ctas CTAs if > 0), never
 // more than the launch's items.  launch(p, grid) issues one launch.
 template <class Launch>
-cudaError_t launch_items(fa::FwdParams p, int qt, int num_sms, int max_ctas, Launch&& launch) {
+cudaError_t launch_items(fa::FwdParams p, int qt, int bc, int d_bytes_per_row, int num_sms,
+                         int max_ctas, Launch&& launch) {
   constexpr long long kMaxItems = 0x7fffffffLL;
   p.n_qg = (p.Nq + 128 * qt - 1) / (128 * qt);
   p.qg_major = (p.wl >= 0 || p.wr >= 0) ? 1 : 0;
   p.qg_desc = p.wr >= 0 ? 1 : 0;  // a right bound: later query rows see more keys
+  const long long kv_head = 2ll * p.Nk * d_bytes_per_row;  // K and V of one head
   const long long per_head = static_cast<long long>(p.n_qg) * p.n_splits;
   const int heads_per = per_head > kMaxItems ? 1 : static_cast<int>(std::min<long long>(p.BH, kMaxItems / per_head));
   const int splits_per = per_head > kMaxItems ? static_cast<int>(kMaxItems / p.n_qg) : p.n_splits;
@@ -155,12 +220,19 @@ cudaError_t launch_items(fa::FwdParams p, int qt, int num_sms, int max_ctas, Lau
       p.n_split = std::min(splits_per, p.n_splits - s0);
       const long long items = static_cast<long long>(p.n_qg) * p.n_split * p.n_bh;
       p.n_items = static_cast<int>(items);
-      p.div_qg = fa::make_fastdiv(p.n_qg);
-      p.div_split = fa::make_fastdiv(p.n_split);
-      p.div_per = fa::make_fastdiv(p.n_split * p.n_bh);
       long long g = max_ctas > 0 ? max_ctas : (num_sms > 0 ? num_sms : 1);
       if (g > items) g = items;
       p.rounds = static_cast<int>((items + g - 1) / g);
+      p.hb = p.qg_major ? choose_heads_blk(p, qt, bc, static_cast<int>(g), kv_head) : p.n_bh;
+#ifdef FA_HEADS_BLK
+      p.hb = std::min(FA_HEADS_BLK, p.n_bh);
+#endif
+      p.div_qg = fa::make_fastdiv(p.n_qg);
+      p.div_split = fa::make_fastdiv(p.n_split);
+      p.div_blk = fa::make_fastdiv(p.n_qg * p.n_split * p.hb);
+      p.div_per = fa::make_fastdiv(p.n_split * p.hb);
+      const int last = p.n_bh - (p.n_bh - 1) / p.hb * p.hb;  // heads in the last block
+      p.div_per_last = fa::make_fastdiv(p.n_split * last);
       const cudaError_t e = launch(p, dim3(static_cast<unsigned>(g)));
       if (e != cudaSuccess) return e;
     }
@@ -250,7 +322,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   }
   const long long rows = static_cast<long long>(BH) * Nq;
   auto run = [&](const fa::FwdParams& pp) {
-    return launch_items(pp, qt, dev->num_sms, max_ctas, [&](const fa::FwdParams& pl, dim3 grid) {
+    return launch_items(pp, qt, bc, d * 2, dev->num_sms, max_ctas, [&](const fa::FwdParams& pl, dim3 grid) {
       return launch_fwd(d, bc, qt, maps, pl, grid, s);
     });
   };
@@ -539,7 +611,7 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
   if ((rc = make_map(&maps[1], k, d, Nk, BH, 128, true)) != FA_OK) return rc;
   if ((rc = make_map(&maps[2], v, d, Nk, BH, 128, true)) != FA_OK) return rc;
   if ((rc = make_map(&maps[3], o, d, Nq, BH, 128)) != FA_OK) return rc;
-  cudaError_t e = launch_items(p, qt, dev->num_sms, 0, [&](const fa::FwdParams& pl, dim3 grid) {
+  cudaError_t e = launch_items(p, qt, 128, d, dev->num_sms, 0, [&](const fa::FwdParams& pl, dim3 grid) {
     return fa::launch_fwd_fp8_d128(qt, maps, pl, grid, static_cast<cudaStream_t>(stream));
   });
   return e == cudaSuccess ? FA_OK : cuda_fail(e);

@@ -247,11 +247,15 @@ template <int QT>
 __device__ __forceinline__ void item_coords(int idx, const FwdParams& p, int& bh, int& split,
                                             int& row0) {
   int x;
-  if (p.qg_major) {  // query-tile group outermost: heaviest first across heads
-    x = fdiv(idx, p.div_per);
-    const int r = idx - x * p.div_per.d;
-    bh = fdiv(r, p.div_split);
-    split = r - bh * p.n_split;
+  if (p.qg_major) {  // blocks of hb heads; in a block, query-tile group outermost (heaviest first)
+    const int b = fdiv(idx, p.div_blk);
+    const int rem = idx - b * p.div_blk.d;
+    const FastDiv& per = (b + 1) * p.hb <= p.n_bh ? p.div_per : p.div_per_last;
+    x = fdiv(rem, per);
+    const int r = rem - x * per.d;
+    const int hl = fdiv(r, p.div_split);
+    bh = b * p.hb + hl;
+    split = r - hl * p.n_split;
   } else {  // head outermost: the query tiles of one head are neighbours (L2 reuse of K/V)
     const int r = fdiv(idx, p.div_qg);
     x = idx - r * p.n_qg;

@@ -60,8 +60,13 @@ struct FwdParams {
   int n_qg;             // groups of QT query tiles per head
   int bh0, n_bh;
   int split0, n_split;
-  FastDiv div_qg, div_split, div_per;  // by n_qg, n_split, n_split * n_bh
-  int qg_major;         // 1: item index = (group, head, split), else (head, split, group)
+  // qg_major: heads go in blocks of hb; within a block, item index =
+  // (group, head, split).  Otherwise item index = (head, split, group).
+  int qg_major;
+  int hb;               // heads per block (qg_major)
+  FastDiv div_qg, div_split;  // by n_qg, n_split
+  FastDiv div_blk;            // by n_qg * n_split * hb (items of a full block)
+  FastDiv div_per, div_per_last;  // by n_split * hb, and by n_split * (heads of the last block)
   int qg_desc;          // 1: groups in descending order (later groups see more keys)
   int wl, wr;        // visible keys [r + off - wl, r + off + wr]; -1 = open side
   float scale;       // natural-units logit scale

@@ -1,13 +1,13 @@
 // fa_noalloc.cu -- split-KV forward for callers that must not allocate.
 //
 // Some callers cannot call cudaMalloc (or any allocating routine) on the
-// path that runs attention: code replayed inside an already-captured CUDA
-// graph, allocator-free embedded runtimes, or a host that has handed all
-// device memory to its own pool.  fa_fwd with n_splits > 1 takes its fp32
-// workspace with cudaMallocAsync, so it is unusable there.  This entry point
-// runs the same split-KV computation (fa_fwd_partial, then fa_merge_splits)
-// with the workspace in a fixed device array that lives as long as the
-// library is loaded.
+// path that runs attention: runtimes without a device allocator, hosts that
+// have handed all device memory to their own pool, or latency-bound loops in
+// which an allocation could block or synchronise.  fa_fwd with n_splits > 1
+// takes its fp32 workspace with cudaMallocAsync, so it is unusable there.
+// This entry point runs the split-KV computation of fa_fwd_partial followed
+// by fa_merge_splits with the workspace in a fixed device array that lives as
+// long as the library is loaded.
 #include <cstdint>
 #include <mutex>
 

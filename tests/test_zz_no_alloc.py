@@ -1,10 +1,10 @@
 """fa_fwd_split_noalloc: the split-KV forward for callers that cannot allocate.
 
-Callers that replay work from an already-captured CUDA graph, allocator-free
-runtimes, or hosts whose device memory belongs to their own pool cannot let
-the library call cudaMallocAsync the way fa_fwd does for its split-KV
-workspace.  This entry point keeps that workspace in a fixed device array
-instead.  Checked here through the C ABI against fa_fwd with the same number
+Runtimes without a device allocator, hosts whose device memory belongs to
+their own pool, and latency-bound loops where an allocation could block
+cannot let the library call cudaMallocAsync the way fa_fwd does for its
+split-KV workspace.  This entry point keeps that workspace in a fixed device
+array instead.  Checked here through the C ABI against fa_fwd with the same number
 of splits, within the parity tolerances, on two calls in a row (the second
 with different shapes and inputs, so stale scratch contents would show), and
 its size limit is checked to be refused before anything is launched.
