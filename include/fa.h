@@ -55,6 +55,9 @@ extern "C" {
 #define FA_ERR_DEVICE_TIMEOUT (-4) /* a kernel wait ran out (fa_get_device_status) */
 #define FA_ERR_NO_MEMORY (-5)      /* the split-KV workspace could not be allocated */
 #define FA_ERR_SCRATCH_TOO_SMALL (-6) /* fa_fwd_split_noalloc: workspace over the fixed limit */
+#define FA_ERR_DEVICE_CHECK (-7)   /* debug build (libfa_debug.so) only: a device-side bounds
+                                      check failed (fa_get_device_status; fa_strerror gives
+                                      the kernel source line) */
 
 /*
  * Attention forward, O and LSE.
@@ -249,7 +252,8 @@ size_t fa_split_workspace_bytes(int B, int H, int Nq, int d, int n_splits);
 /*
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT if any kernel of this library
- * recorded a timed-out wait since the last call, or FA_ERR_CUDA.  The word is
+ * recorded a timed-out wait since the last call, FA_ERR_DEVICE_CHECK (debug
+ * build only) if a bounds check failed first, or FA_ERR_CUDA.  The word is
  * one per device, shared by every call on that device (all streams, and the
  * host-buffer entry points, which read it before returning): a timeout from a
  * kernel on another stream is reported to whichever caller reads the word

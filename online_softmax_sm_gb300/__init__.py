@@ -19,14 +19,14 @@ package is its Python binding plus the seeded workload generators:
 
 libfa.so is loaded on first use; importing the package loads nothing.
 """
-from ._binding import (FA_DTYPE_BF16, FA_DTYPE_F32, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT,
+from ._binding import (FA_DTYPE_BF16, FA_DTYPE_F32, FA_ERR_CUDA, FA_ERR_DEVICE_CHECK, FA_ERR_DEVICE_TIMEOUT,
                        FA_ERR_INVALID_ARG, FA_ERR_NO_MEMORY, FA_ERR_SCRATCH_TOO_SMALL,
-                       FA_ERR_UNSUPPORTED, FA_OK, FAError, bwd, bwd_host, device_status, fwd, fwd_fp8, fwd_fp8_host, fwd_host, fwd_local,
+                       FA_ERR_UNSUPPORTED, FA_OK, FAError, bwd, bwd_host, debug_library, device_status, fwd, fwd_fp8, fwd_fp8_host, fwd_host, fwd_local,
                        fwd_partial, fwd_split_noalloc, lib, merge_splits, softmax_rows,
                        split_workspace_bytes, strerror, version)
 
 __all__ = ["fwd", "fwd_host", "fwd_local", "fwd_fp8", "fwd_fp8_host", "bwd", "bwd_host", "fwd_partial", "merge_splits", "fwd_split_noalloc", "softmax_rows",
            "split_workspace_bytes", "device_status", "version", "strerror", "lib", "FAError",
            "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
-           "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_NO_MEMORY", "FA_ERR_SCRATCH_TOO_SMALL", "FA_DTYPE_F32",
+           "FA_ERR_DEVICE_TIMEOUT", "FA_ERR_DEVICE_CHECK", "debug_library", "FA_ERR_NO_MEMORY", "FA_ERR_SCRATCH_TOO_SMALL", "FA_DTYPE_F32",
            "FA_DTYPE_BF16"]

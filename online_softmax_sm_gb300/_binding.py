@@ -6,6 +6,7 @@ If libfa.so is missing, every call raises: there is no fallback path.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import re
@@ -14,6 +15,7 @@ import torch
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfa.so")
+LIB_DEBUG_PATH = os.path.join(PKG, "libfa_debug.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "fa.h")
 
 FA_OK = 0
@@ -23,6 +25,7 @@ FA_ERR_CUDA = -3
 FA_ERR_DEVICE_TIMEOUT = -4
 FA_ERR_NO_MEMORY = -5
 FA_ERR_SCRATCH_TOO_SMALL = -6
+FA_ERR_DEVICE_CHECK = -7
 FA_DTYPE_F32 = 0
 FA_DTYPE_BF16 = 1
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -101,6 +104,24 @@ def lib():
         _declare(L)
         _lib = L
     return _lib
+
+
+@contextlib.contextmanager
+def debug_library():
+    """Within the block every call goes through libfa_debug.so, the FA_DEBUG
+    build: device-side index, shared-memory and TMEM range checks that record
+    FA_ERR_DEVICE_CHECK (with the kernel source line, see strerror) in the
+    status word and skip the access instead of trapping."""
+    global _lib
+    if not os.path.exists(LIB_DEBUG_PATH):
+        raise RuntimeError(f"{LIB_DEBUG_PATH} is not built; run `python -m online_softmax_sm_gb300.build --debug`")
+    L = ctypes.CDLL(LIB_DEBUG_PATH)
+    _declare(L)
+    saved, _lib = _lib, L
+    try:
+        yield L
+    finally:
+        _lib = saved
 
 
 def declared_symbols(header: str = HEADER) -> list[str]:

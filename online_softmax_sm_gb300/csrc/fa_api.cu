@@ -19,9 +19,12 @@ constexpr int kMaxSeq = 1 << 30;
 
 thread_local cudaError_t t_last_cuda = cudaSuccess;
 thread_local char t_msg[256];
+thread_local char t_check_msg[160] = "debug build: a device-side bounds check failed";
 
-// Device status word, one per device (kernels record timed-out waits here).
-__device__ int g_fa_status;
+// Device status words, one pair per device: [0] what went wrong (kernels
+// record timed-out waits, and failed debug-build checks, here), [1] the
+// source line of the first failed check.
+__device__ int g_fa_status[2];
 
 struct DevState {
   bool checked = false;
@@ -826,14 +829,21 @@ int fa_get_device_status(void* stream) {
   int rc = device_state(&dev);
   if (rc != FA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int host = 0;
-  const int zero = 0;
+  int host[2] = {0, 0};
+  const int zero[2] = {0, 0};
   cudaError_t e = cudaStreamSynchronize(s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(&host, dev->status, sizeof(int), cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(host, dev->status, sizeof(host), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dev->status, zero, sizeof(zero), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e);
-  return host == fa::kDevTimeout ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+  if (host[0] == fa::kDevCheck) {
+    std::snprintf(t_check_msg, sizeof(t_check_msg),
+                  "debug build: a device-side bounds check failed (kernel source line %d); the "
+                  "access was skipped",
+                  host[1]);
+    return FA_ERR_DEVICE_CHECK;
+  }
+  return host[0] == fa::kDevTimeout ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
 }
 
 const char* fa_strerror(int code) {
@@ -842,6 +852,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_INVALID_ARG: return "invalid argument";
     case FA_ERR_UNSUPPORTED: return "unsupported (head dim must be 64 or 128; device must be sm_103)";
     case FA_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out; the affected CTAs stopped without writing";
+    case FA_ERR_DEVICE_CHECK: return t_check_msg;
     case FA_ERR_NO_MEMORY: return "could not allocate the split-KV workspace";
     case FA_ERR_SCRATCH_TOO_SMALL:
       return "split-KV workspace larger than the fixed no-alloc scratch (FA_NOALLOC_SCRATCH_BYTES)";

@@ -141,10 +141,12 @@ struct FwdCfg {
   static constexpr int kPCol = kSBufs * BC;
   static constexpr int kOCol = (kPCol + QT * kPCols + D - 1) / D * D;
   static constexpr int kTmemNeed = kOCol + QT * D;
+  static_assert(kPCol >= kSCol + kSBufs * BC && kOCol >= kPCol + QT * kPCols, "TMEM regions overlap");
   static constexpr int kTmemCols = kTmemNeed <= 64    ? 64
                                    : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256
                                                       : 512;
+  static_assert(kTmemNeed <= kTmemCols && kTmemCols <= 512, "TMEM columns");
   static constexpr int kCtlBytes = 2048;
   static constexpr int kSmemLimit = 227 * 1024;
   // bf16 O is staged for the TMA store 64 columns (one 128-byte swizzle row)
@@ -454,11 +456,13 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
             if (it.n[i] <= 0) continue;
             if (q_loads[i] > 0 && !wait_bounded(bar_qe + 8 * i, (q_loads[i] - 1) & 1, wc)) return false;
             const uint32_t full = bar_qf + 8 * i;
-            mbar_arrive_expect_tx(full, C::kQTileBytes);
+            if (FA_DCHECK(it.bh < p.BH && it.row0 + C::kBr * i < p.Nq, p.status)) {
+              mbar_arrive_expect_tx(full, C::kQTileBytes);
 #pragma unroll
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(smem_u32(sQ + i * C::kQTileBytes + c * C::kQChunkBytes), &tm_q, full,
-                          c * C::kChunkElems, it.row0 + C::kBr * i, it.bh);
+              for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(smem_u32(sQ + i * C::kQTileBytes + c * C::kQChunkBytes), &tm_q, full,
+                            c * C::kChunkElems, it.row0 + C::kBr * i, it.bh);
+            }
             ++q_loads[i];
           }
           return true;
@@ -484,6 +488,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
             // O staging slot of tile pos - n_kv: no copy; that tile releases
             // it if it stages O
             const int ti = pos - n_kv;
+            if (!FA_DCHECK(rp.stage < C::kStages && ti < QT, p.status)) continue;
             uint32_t stager = 0;
 #pragma unroll
             for (int i = 0; i < QT; ++i) stager |= (i == ti && it.n[i] > 0 ? 1u : 0u) << i;
@@ -504,6 +509,10 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
           if (g < 0x7fffffff) ++g;
           if (skip) continue;  // test hook: this slot never fills
           const uint32_t full = bar_kv_full + 8 * rp.stage;
+          if (!FA_DCHECK(rp.stage < C::kStages && step < it.n_cta && (it.cta_b + step) * BC < p.Nk &&
+                             it.bh < p.BH,
+                         p.status))
+            continue;
           mbar_arrive_expect_tx(full, C::kKVTileBytes);
           const CUtensorMap* map = is_v ? &tm_v : &tm_k;
 #pragma unroll
@@ -608,6 +617,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
         };
         auto issue_qk = [&](int q) {  // S_i(q) = Q_i K_q^T, then release K_q's slot for tile i
           const int stage = ring_at<C::kStages>(g_stage, g_par, ring_pos_k(q)).stage;
+          if (!FA_DCHECK(stage < C::kStages && q < n, p.status)) return;
           const uint32_t k_lo = lo_k + ((stage * C::kKVTileBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / C::kKStep; ++kk) {  // 32 bytes of K per step
@@ -622,6 +632,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
         };
         auto issue_pv = [&](int v) {  // O_i += P_i(v) V_v, then release V_v's slot for tile i
           const int stage = ring_at<C::kStages>(g_stage, g_par, ring_pos_v(v, n_cta)).stage;
+          if (!FA_DCHECK(stage < C::kStages && v < n, p.status)) return;
           const uint32_t v_lo = lo_v + ((stage * C::kKVTileBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < BC / C::kKStep; ++kk) {
@@ -785,7 +796,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
         if (now - t_idle > p.timeout_ns) {
           if ((threadIdx.x & 31) == 0) {
             *wc.abort = 1;
-            atomicExch(p.status, kDevTimeout);
+            record_status(p.status, kDevTimeout);
           }
           break;
         }
@@ -1018,7 +1029,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
         if (n == 0) {
           // no visible key: O = 0 straight to global memory (the staging
           // buffers may be in use by the next item's loads)
-          if (row < p.Nq) {
+          if (row < p.Nq && FA_DCHECK(bh < p.BH, p.status)) {
             uint8_t* orow = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + row) * (D * 2);
 #pragma unroll
             for (int q = 0; q < D * 2 / 16; ++q) st_global_v4(orow + 16 * q, 0u, 0u, 0u, 0u);
@@ -1031,7 +1042,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
           constexpr int kRounds = C::kSlotStg ? 1 : D / 64;
           if constexpr (C::kSlotStg) {
             // every warp of the tile agrees before any of them leaves
-            const bool got = warp_wait(bar_kv_full + 8 * slot.stage, slot.par, wc);
+            const bool got = FA_DCHECK(slot.stage < C::kStages && bh < p.BH, p.status) &&
+                             warp_wait(bar_kv_full + 8 * slot.stage, slot.par, wc);
             if (named_bar_or(1 + i, 128, !got)) break;
             stg = smem_u32(sKV + slot.stage * C::kKVTileBytes);
           } else {
@@ -1077,11 +1089,12 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
             }
           }
         }
-        if (row < p.Nq)
+        if (row < p.Nq && FA_DCHECK(bh < p.BH, p.status))
           p.lse[static_cast<size_t>(bh) * p.Nq + row] = empty ? -INFINITY : m * p.scale + logf(lc);
       } else {
         // fp32 partial triple (m in natural-log units, l, O/l) for the merge.
         const size_t prow = (static_cast<size_t>(it.split) * p.BH + bh) * p.Nq + row;
+        if (!FA_DCHECK(it.split < p.n_splits && bh < p.BH, p.status)) continue;
         if (row < p.Nq) {
           p.m_part[prow] = empty ? -INFINITY : m * p.scale;
           p.l_part[prow] = empty ? 0.f : l;

@@ -14,7 +14,10 @@ namespace fa {
 enum : int {
   kDevOk = 0,
   kDevTimeout = 1,  // a bounded mbarrier wait ran out; the CTA stopped cleanly
+  kDevCheck = 2,    // debug build (FA_DEBUG): a bounds check failed; the access was skipped
 };
+// The status word is the first of two ints per device; the second holds the
+// source line of the first failed debug-build check.
 
 // Default K/V tile (keys per tile): split-KV ranges are counted in these.
 constexpr int kDefaultBc = 128;

@@ -14,6 +14,24 @@ struct WaitCtx {
   unsigned long long timeout_ns;
 };
 
+// Records a failure in the device status word unless one is recorded already
+// (the first failure wins).
+__device__ __forceinline__ void record_status(int* status, int code) { atomicCAS(status, kDevOk, code); }
+
+// Debug build (FA_DEBUG): FA_DCHECK(cond, status) is true when cond holds;
+// otherwise it records kDevCheck and the source line in the status words and
+// is false, so the guarded access is skipped (nothing traps).  In the release
+// build it is the constant true and costs nothing.
+#ifdef FA_DEBUG
+__device__ __forceinline__ bool dcheck(bool ok, int* status, int line) {
+  if (!ok && atomicCAS(status, kDevOk, kDevCheck) == kDevOk) atomicExch(status + 1, line);
+  return ok;
+}
+#define FA_DCHECK(cond, status) ::fa::dcheck(static_cast<bool>(cond), (status), __LINE__)
+#else
+#define FA_DCHECK(cond, status) true
+#endif
+
 // Bounded wait on a phase; false if the CTA aborted or the limit ran out.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& w) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -23,7 +41,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     if (*w.abort) return false;
     if (global_timer_ns() - t0 > w.timeout_ns) {
       *w.abort = 1;
-      atomicExch(w.status, kDevTimeout);
+      record_status(w.status, kDevTimeout);
       return false;
     }
   }
