@@ -16,16 +16,16 @@
 //
 // A row that fits one CTA (up to 1024 threads x 16 fp32 or 32 bf16 values)
 // runs fa_softmax_rows_kernel: 16-byte (or element) loads straight into
-// registers, several CTAs per SM overlapping one another.  Longer rows with
-// 16-byte aligned starts run fa_softmax_ring_kernel on a cluster of up to 8
-// CTAs of 1024 threads: each CTA's columns of each row arrive through a ring
-// of shared-memory stages filled by 1-D bulk copies (TMA) issued rows ahead,
-// so loads overlap the arithmetic and the stores of earlier rows; the threads
-// copy their slice into registers and free the stage at once.  Either way a
-// row that fits the registers of its CTA or cluster is read from HBM once and
-// pass 2 rescales the exponentials kept from pass 1 by exp(m_thread - M) / L.
-// Longer rows are cut into sub-chunks and pass 2 streams them through the
-// ring again; pass 1 marks them to stay in L2 for that second read.
+// registers, several CTAs per SM overlapping one another, the row read from
+// HBM once; pass 2 rescales the exponentials kept from pass 1 by
+// exp(m_thread - M) / L.  Longer rows with 16-byte aligned starts, when there
+// are at least two per SM, run fa_softmax_stream_kernel: one CTA per row at a
+// time (two per SM), the row streamed through a shared-memory ring of 1-D bulk
+// copies (TMA) twice, the second time from L2, and no CTA ever waits for
+// another.  Fewer long rows run fa_softmax_ring_kernel on a cluster of up to 8
+// CTAs of 1024 threads that share the row: each CTA's columns arrive through
+// its own ring; a row that fits the cluster's registers is read once, longer
+// rows are cut into sub-chunks that pass 2 streams through the ring again.
 //
 // Exponentials: exp(x - m) = 2^((x - m) log2 e), the difference taken first
 // (so the exponent's rounding error scales with |x - m|, not with |m|) and
@@ -46,6 +46,28 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxCluster = 8;
+// The streaming kernel runs two CTAs per SM; a group of CTAs shares each
+// row, and long rows stream that way when there is at least one row per
+// group.  Fewer rows share each row across a cluster of the ring kernel.
+constexpr long long kStreamCtasPerSm = 2;
+
+// CTAs per row for the streaming kernel: the group sizes that measured
+// fastest on GB300 for rows of 32K-2M elements.  Longer chunks per CTA keep
+// more rows in flight (more L2 misses between the passes, longer pipeline
+// fill per row); more CTAs per row pay more exchanges and smaller loads.
+template <typename T>
+int stream_group(long long cols) {
+  if (sizeof(T) == 4) {
+    if (cols <= 20480) return 1;
+    if (cols <= 40960) return 2;
+    if (cols <= 131072) return 4;
+    return 8;
+  }
+  if (cols <= 65536) return 1;
+  if (cols <= 262144) return 2;
+  if (cols <= 524288) return 4;
+  return 8;
+}
 
 template <typename T>
 struct Io;
@@ -95,6 +117,18 @@ struct Io<__nv_bfloat16> {
   __device__ static void store_one(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 };
 
+// Shared-memory add with acquire-release order at CTA scope; returns the old
+// value.  The caller's earlier shared-memory accesses happen before it, and
+// whatever the caller does next happens after every earlier add to `addr`.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_smem(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 // (m, l) <- (m, l) merged with (m2, l2): the two-block rule.  The pair with
 // the larger max keeps its sum as is (its factor exp(0) is exactly 1), so one
 // exponential suffices; a -inf max carries l = 0 and contributes nothing.
@@ -105,6 +139,23 @@ __device__ __forceinline__ void merge_pair(float& m, float& l, float m2, float l
     l = (m != -INFINITY ? l * ex2_approx((m - m2) * kLog2e) : 0.f) + l2;
     m = m2;
   }
+}
+
+// Largest of v[0..N) with three-input max instructions (N a multiple of 4):
+// four running maxima, each taking two new values per step.
+template <int N>
+__device__ __forceinline__ float max_of(const float* v) {
+  float mx[4] = {v[0], v[1], v[2], v[3]};
+  int i = 4;
+#pragma unroll
+  for (; i + 8 <= N; i += 8)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) mx[u] = max3f(mx[u], v[i + u], v[i + 4 + u]);
+#pragma unroll
+  for (; i < N; i += 4)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) mx[u] = fmaxf(mx[u], v[i + u]);
+  return fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]);
 }
 
 // Tree of merges over the 32 lanes (fixed order); lane 0's pair is broadcast.
@@ -473,6 +524,274 @@ __global__ void __launch_bounds__(kThreads) fa_softmax_ring_kernel(const Softmax
   if (ncta > 1) cluster_sync();  // no CTA leaves while a peer may still address its shared memory
 }
 
+// Long rows, at least one per resident CTA group: a group of kCta CTAs (a
+// cluster when kCta > 1) takes one row at a time, each CTA streaming its
+// chunk of the row through a ring of kStages shared-memory stages filled by
+// 1-D bulk copies -- pass 1 from HBM (the copies ask L2 to keep the lines),
+// pass 2 again from L2 -- so every group works on its own rows and L2 holds
+// about one row per group between the passes.  Pass 1 ends on the chunk's
+// last sub-chunk, whose exponentials are still in registers: pass 2 writes
+// that sub-chunk first, from the registers, and reloads only the other
+// nsub - 1 (so pass 1 marks the last one evict-first).  Loads of a row, in
+// order: sub-chunks 0 .. nsub-1 (pass 1), then 0 .. nsub-2 (pass 2).
+//
+// The warps never meet at a CTA-wide barrier.  Each waits for a stage on its
+// own, copies its vectors to registers and counts itself out of the stage; the
+// warp that counts the stage empty starts the load kStages ahead into it
+// (stages are released in load order, so load g lives in stage g % kStages).
+// At the end of pass 1 every warp publishes its (m, l) and arrives on the
+// row's mbarrier; each warp then merges all warps' pairs itself (the same tree
+// in every warp) while the ring keeps loading.  In a cluster, warp 0 of each
+// CTA then sends the CTA's pair to every CTA of the group (st.async, counted
+// on the receiver's mbarrier) and every warp merges the group's pairs in rank
+// order, so all CTAs of a row get the same (M, L).
+template <typename T, int kWarps, int kVec, int kStages, int kCta>
+__global__ void __launch_bounds__(kWarps * 32, 1024 / (kWarps * 32))
+    fa_softmax_stream_kernel(const SoftmaxParams p) {
+  using IO = Io<T>;
+  constexpr int kThreads = kWarps * 32;
+  constexpr int E = IO::E;
+  constexpr int kPer = kVec * E;
+  constexpr int kSub = kThreads * kPer;  // columns per sub-chunk
+  constexpr uint32_t kStageBytes = kThreads * kVec * 16;
+  // Pair slots and their mbarriers cycle over 4 rows.  A warp publishes row
+  // it+4 after its wait for the last pass-1 load of that row, started only
+  // once every warp had released the load kStages earlier -- one of row it+1
+  // or later, as rows hold per_row = 2 * nsub - 1 loads and
+  // 3 * per_row + nsub - 1 >= 3 >= kStages -- and every warp reads the pairs
+  // of row it before releasing any load of row it+1.  A peer CTA sends its
+  // pair of row it+4 only after receiving ours of row it+3, which we send
+  // after every warp here has finished with row it.
+  constexpr int kSlots = 4;
+  static_assert(kStages >= 2 && kStages <= 3, "ring depth");
+  static_assert(kCta >= 1 && kCta <= kMaxCluster, "group size");
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ __align__(8) uint64_t red[kSlots];        // all warps' pairs of a row are published
+  __shared__ __align__(8) uint64_t peer_full[kSlots];  // all CTAs' pairs of a row have landed
+  __shared__ uint32_t reads[kStages];                  // warp releases of the stage, ever
+  __shared__ float2 warp_part[kSlots][kWarps];
+  __shared__ __align__(16) float4 peer_part[kSlots][kCta];  // (m, l, failed, -) per CTA
+  __shared__ long long issued_sh;  // loads whose copies have been started
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rank = kCta > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const long long groups = gridDim.x / kCta;
+  const long long group = blockIdx.x / kCta;
+  const int c0 = rank * p.chunk;  // this CTA's columns [c0, c1) of every row
+  const int c1 = min(p.cols, c0 + p.chunk);
+  const int nsub = c1 > c0 ? (c1 - c0 + kSub - 1) / kSub : 0;
+  const int per_row = nsub > 0 ? 2 * nsub - 1 : 0;  // loads per row
+  const long long my_rows = group < p.rows ? (p.rows - 1 - group) / groups + 1 : 0;
+  const long long total = my_rows * per_row;
+  const T* __restrict__ xg = static_cast<const T*>(p.x);
+  T* __restrict__ yg = static_cast<T*>(p.y);
+  const uint32_t ring0 = smem_u32(ring);
+  const uint32_t bar0 = smem_u32(&full[0]);
+  const uint32_t red0 = smem_u32(&red[0]);
+  const uint32_t peer0 = smem_u32(&peer_full[0]);
+  const uint32_t reads0 = smem_u32(&reads[0]);
+
+  // Start load g (if it exists) into stage g % kStages.
+  auto issue = [&](long long g) {
+    if (g >= total) return;
+    const long long row = group + (g / per_row) * groups;
+    const int k = static_cast<int>(g % per_row);
+    const int col = c0 + (k < nsub ? k : k - nsub) * kSub;
+    const uint32_t bytes = static_cast<uint32_t>(min(kSub, c1 - col)) * sizeof(T);
+    const int s = static_cast<int>(g % kStages);
+    // pass-1 loads that pass 2 reads again ask L2 to keep them
+    const uint64_t pol = k < nsub - 1 ? l2_policy_evict_last() : l2_policy_evict_first();
+    if (FA_DCHECK(row < p.rows && col < c1, p.status)) {
+      mbar_arrive_expect_tx(bar0 + 8 * s, bytes);
+      bulk_load(ring0 + s * kStageBytes, xg + row * p.cols + col, bytes, bar0 + 8 * s, pol);
+    }
+    *reinterpret_cast<volatile long long*>(&issued_sh) = g + 1;
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar0 + 8 * s, 1);
+      reads[s] = 0;
+    }
+    for (int r = 0; r < kSlots; ++r) {
+      mbar_init(red0 + 8 * r, kWarps);
+      mbar_init(peer0 + 8 * r, 1);
+    }
+    abort_flag = 0;
+    issued_sh = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (kCta > 1) cluster_sync();  // every CTA of the group runs before any DSMEM store
+  if (tid == 0)
+    for (int g = 0; g < kStages; ++g) issue(g);
+  const WaitCtx wc{&abort_flag, p.status, p.timeout_ns};
+
+  long long g = 0;  // next load this warp uses
+  float v[kPer];
+  // Wait for load g, copy this thread's vectors of it (columns from `base`,
+  // -inf past the chunk's end), count the warp out of the stage (the last
+  // warp out refills it).  False (warp-uniform) if the wait failed.
+  auto take = [&](int base) -> bool {
+    const int s = static_cast<int>(g % kStages);
+    if (!warp_wait(bar0 + 8 * s, static_cast<uint32_t>((g / kStages) & 1), wc)) return false;
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int slot = k * kThreads + tid;
+      if (base + slot * E < c1) {
+        uint32_t w[4];
+        ld_shared_v4(ring0 + s * kStageBytes + slot * 16, w[0], w[1], w[2], w[3]);
+        if constexpr (E == 4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[k * 4 + e] = __uint_as_float(w[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[k * 8 + 2 * e] = __uint_as_float(w[e] << 16);
+            v[k * 8 + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[k * E + e] = -INFINITY;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t before = atom_add_acq_rel_smem(reads0 + 4 * s, 1);
+      if ((before + 1) % kWarps == 0) {
+        fence_proxy_async_smem();
+        issue(g + kStages);
+      }
+    }
+    ++g;
+    return true;
+  };
+  auto store = [&](T* yr, int base) {
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int col0 = base + (k * kThreads + tid) * E;
+      if (col0 < c1) IO::store_vec(yr + col0, v + k * E);
+    }
+  };
+
+  const uint64_t l2e = f2_pack(kLog2e, kLog2e);
+  bool failed = false;
+  for (long long it = 0; it < my_rows && !failed; ++it) {
+    const long long row = group + it * groups;
+    T* yr = yg + row * p.cols;
+    const int slot = static_cast<int>(it % kSlots);
+    const uint32_t slot_par = static_cast<uint32_t>((it / kSlots) & 1);
+    // this CTA expects every group member's pair of the row (its own included)
+    if (kCta > 1 && tid == 0) mbar_arrive_expect_tx(peer0 + 8 * slot, 16u * kCta);
+
+    // ---- pass 1: running (m, l) of this thread's columns; v keeps the last
+    // sub-chunk's exponentials, taken against `ref`
+    float m = -INFINITY, l = 0.f, ref = 0.f;
+    for (int sc = 0; sc < nsub; ++sc) {
+      if (!take(c0 + sc * kSub)) {
+        failed = true;
+        break;
+      }
+      const float gmax = max_of<kPer>(v);
+      if (gmax > m) {  // new running max: rescale the sum so far (l = 0 while m = -inf)
+        l *= ex2_approx((m - gmax) * kLog2e);
+        m = gmax;
+      }
+      ref = (m == -INFINITY) ? 0.f : m;
+      const uint64_t nref = f2_pack(-ref, -ref);
+      uint64_t acc[2] = {0, 0};
+#pragma unroll
+      for (int i = 0; i < kPer; i += 2) {
+        float a, b;
+        f2_unpack(fmul2(fadd2(f2_pack(v[i], v[i + 1]), nref), l2e), a, b);
+        const uint64_t e = f2_pack(ex2_approx(a), ex2_approx(b));
+        acc[(i >> 1) & 1] = fadd2(acc[(i >> 1) & 1], e);
+        f2_unpack(e, v[i], v[i + 1]);
+      }
+      float a0, a1, a2, a3;
+      f2_unpack(acc[0], a0, a1);
+      f2_unpack(acc[1], a2, a3);
+      l += (a0 + a1) + (a2 + a3);
+    }
+    // a failed CTA still publishes (flagged) so that its group does not wait
+    // for it until the limit
+
+    // ---- (M, L) of the CTA's chunk from every warp's pair
+    const float2 wp = warp_pair(m, l);
+    if (lane == 0) {
+      warp_part[slot][warp] = wp;
+      mbar_arrive(red0 + 8 * slot);  // release: the pair is written before the arrival
+    }
+    if (!warp_wait(red0 + 8 * slot, slot_par, wc)) failed = true;
+    const float2 bp = lane < kWarps ? warp_part[slot][lane] : make_float2(-INFINITY, 0.f);
+    float2 ML = warp_pair(bp.x, bp.y);
+    if (kCta > 1) {
+      // ---- the group's pairs, merged in rank order
+      if (warp == 0 && lane < kCta)
+        st_async_f32x4(mapa_shared(smem_u32(&peer_part[slot][rank]), lane), ML.x, ML.y,
+                       failed ? 1.f : 0.f, 0.f, mapa_shared(peer0 + 8 * slot, lane));
+      if (!warp_wait(peer0 + 8 * slot, slot_par, wc)) {
+        failed = true;
+        break;
+      }
+      const float4 q0 = peer_part[slot][0];
+      ML = make_float2(q0.x, q0.y);
+      bool any_failed = q0.z != 0.f;
+#pragma unroll
+      for (int r = 1; r < kCta; ++r) {
+        const float4 qr = peer_part[slot][r];
+        merge_pair(ML.x, ML.y, qr.x, qr.y);
+        any_failed = any_failed || qr.z != 0.f;
+      }
+      if (any_failed) failed = true;
+    }
+    if (failed) break;
+    const float M = ML.x, L = ML.y;
+    if (rank == 0 && warp == 0 && lane == 0 && p.lse)
+      p.lse[row] = L > 0.f ? M + logf(L) : -INFINITY;
+
+    // ---- pass 2: y = exp(x - M) / L, the last sub-chunk from the registers
+    // (exp(x - ref) * exp(ref - M) / L), the others reloaded
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const float rM = (M == -INFINITY) ? 0.f : M;
+    if (nsub > 0) {
+      const float f = ex2_approx((ref - rM) * kLog2e) * inv;
+      const uint64_t f2 = f2_pack(f, f);
+#pragma unroll
+      for (int i = 0; i < kPer; i += 2)
+        f2_unpack(fmul2(f2_pack(v[i], v[i + 1]), f2), v[i], v[i + 1]);
+      store(yr, c0 + (nsub - 1) * kSub);
+    }
+    const uint64_t nrM = f2_pack(-rM, -rM), inv2 = f2_pack(inv, inv);
+    for (int sc = 0; sc + 1 < nsub; ++sc) {
+      if (!take(c0 + sc * kSub)) {
+        failed = true;
+        break;
+      }
+#pragma unroll
+      for (int i = 0; i < kPer; i += 2) {
+        float a, c;
+        f2_unpack(fmul2(fadd2(f2_pack(v[i], v[i + 1]), nrM), l2e), a, c);
+        f2_unpack(fmul2(f2_pack(ex2_approx(a), ex2_approx(c)), inv2), v[i], v[i + 1]);
+      }
+      store(yr, c0 + sc * kSub);
+    }
+  }
+  // Copies still in flight (after a failure) land before the CTA may exit:
+  // each stage's latest copy is one of the last kStages issued.
+  __syncthreads();
+  if (tid == 0) {
+    const long long issued = issued_sh;
+    for (long long i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+      wait_own(bar0 + 8 * static_cast<int>(i % kStages), static_cast<uint32_t>((i / kStages) & 1),
+               p.timeout_ns);
+  }
+  if (kCta > 1) cluster_sync();  // no CTA leaves while a peer may still address its shared memory
+}
+
 // Persistent launch: as many CTAs (or clusters of p.cluster CTAs) as are
 // resident at once, each looping over rows.  Clusters are co-scheduled inside
 // one GPC, so their count comes from the occupancy query for that cluster
@@ -529,6 +848,24 @@ cudaError_t launch_ring(const SoftmaxParams& p, int num_sms, cudaStream_t s) {
   return launch_persistent(kern, kThreads, kSmem, per_sm, clusters, p, num_sms, s);
 }
 
+template <typename T, int kWarps, int kVec, int kStages, int kCta>
+cudaError_t launch_stream(const SoftmaxParams& p, int num_sms, cudaStream_t s) {
+  constexpr int kSmem = kStages * kWarps * 32 * kVec * 16;
+  auto kern = fa_softmax_stream_kernel<T, kWarps, kVec, kStages, kCta>;
+  static std::atomic<int> cached{0};  // resident CTAs per SM (same on every sm_103 device)
+  int per_sm = cached.load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, kSmem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    cached.store(per_sm, std::memory_order_relaxed);
+  }
+  static std::atomic<int> clusters[kMaxCluster + 1] = {};
+  return launch_persistent(kern, kWarps * 32, kSmem, per_sm, clusters, p, num_sms, s);
+}
+
 template <typename T, int kThreads, bool kVecIO>
 cudaError_t launch_one(const SoftmaxParams& p, int num_sms, cudaStream_t s) {
   auto kern = fa_softmax_rows_kernel<T, kThreads, 4, kVecIO>;
@@ -565,9 +902,25 @@ cudaError_t launch_typed(SoftmaxParams p, int num_sms, cudaStream_t s) {
       }
     }
   }
-  // A cluster of CTAs of 1024 threads shares the row in equal chunks (whole
-  // 16-byte vectors): resident up to 8 CTAs, beyond that 8 CTAs stream
-  // sub-chunks of their chunk.
+  // Long rows, at least one per group of CTAs: each group (a cluster of
+  // stream_group CTAs) takes one row at a time and streams it twice (the
+  // second time mostly from L2).
+  if (kVecIO) {
+    const int cta = stream_group<T>(p.cols);
+    if (p.rows * cta >= kStreamCtasPerSm * static_cast<long long>(num_sms)) {
+      p.cluster = cta;
+      p.chunk = static_cast<int>((static_cast<long long>(p.cols) + cta * E - 1) / (cta * E) * E);
+      switch (cta) {
+        case 1: return launch_stream<T, 16, 4, 3, 1>(p, num_sms, s);
+        case 2: return launch_stream<T, 16, 4, 3, 2>(p, num_sms, s);
+        case 4: return launch_stream<T, 16, 4, 3, 4>(p, num_sms, s);
+        default: return launch_stream<T, 16, 4, 3, 8>(p, num_sms, s);
+      }
+    }
+  }
+  // Otherwise a cluster of CTAs of 1024 threads shares the row in equal
+  // chunks (whole 16-byte vectors): resident up to 8 CTAs, beyond that 8 CTAs
+  // stream sub-chunks of their chunk.
   constexpr int kCap = 1024 * kPer;
   const long long need = (static_cast<long long>(p.cols) + kCap - 1) / kCap;
   p.cluster = static_cast<int>(need < kMaxCluster ? need : kMaxCluster);

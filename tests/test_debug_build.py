@@ -72,3 +72,24 @@ def test_debug_build_partials_window_and_fp8(debug_lib):
     o_r, lse_r = fa.fwd_fp8(q8, k8, v8, w.scale, 1.0, 1.0, 1.0, True)
     torch.cuda.synchronize()
     assert torch.equal(o_8, o_r) and torch.equal(lse_8, lse_r)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("rows_per_sm,cols,dt", [(2, 32776, torch.bfloat16), (2, 131080, torch.bfloat16),
+                                                  (0, 50000, torch.float32)],
+                         ids=["stream_bf16", "stream_group2_bf16", "cluster_f32"])
+def test_debug_build_softmax_long_rows(debug_lib, rows_per_sm, cols, dt):
+    """The long-row softmax kernels (streaming, one CTA or a group per row,
+    and the ring kernel's cluster for few rows) under the debug build's
+    bounds checks, bit-equal to release."""
+    rows = max(3, rows_per_sm * torch.cuda.get_device_properties(0).multi_processor_count + 3)
+    x = (torch.randn(rows, cols, device="cuda", generator=torch.Generator("cuda").manual_seed(cols))
+         * 4.0).to(dt)
+    with fa.debug_library():
+        y_d, lse_d = fa.softmax_rows(x)
+        torch.cuda.synchronize()
+        st = fa.device_status()
+        assert st == fa.FA_OK, fa.strerror(st)
+    y_r, lse_r = fa.softmax_rows(x)
+    torch.cuda.synchronize()
+    assert torch.equal(y_d, y_r) and torch.equal(lse_d, lse_r)

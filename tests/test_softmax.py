@@ -10,8 +10,9 @@ and the division each add a few ulp.  So
 flush-to-zero exponential sends to 0.  bf16 results may also differ by half a
 bf16 ulp (their rounding).  |dLSE| <= 1e-5 (1 + |LSE|).
 Shapes cover every launch form: one CTA per row at each width, vector and
-scalar access, clusters of 2..8 CTAs holding the row on chip, and the
-streaming form whose second pass reads the row again.
+scalar access, clusters of 2..8 CTAs holding the row on chip or streaming it
+twice, and -- with at least two long rows per SM -- one CTA per row streaming
+it twice through its ring.
 """
 import numpy as np
 import pytest
@@ -82,6 +83,25 @@ def test_softmax_rows_all_elements(rows, cols, dtype):
     y, lse = fa.softmax_rows(x)
     torch.cuda.synchronize()
     _check(x, y, lse, what=f"{rows}x{cols} {dtype}")
+
+
+# Long rows, at least two per SM: the streaming form, a group of 1, 2, 4 or 8
+# CTAs per row by row length, two passes through each CTA's ring of bulk
+# copies.  Ragged last sub-chunks (a few columns past a multiple of the
+# sub-chunk), chunks of exactly two sub-chunks, and many.
+STREAM_SHAPES = [(32776, "bf16"), (16392, "f32"), (65536, "bf16"), (40000, "f32"),
+                 (131080, "bf16"), (90000, "f32"), (262152, "bf16"), (131080, "f32")]
+
+
+@pytest.mark.parametrize("cols,dt", STREAM_SHAPES, ids=[f"c{c}_{d}" for c, d in STREAM_SHAPES])
+def test_streaming_rows_all_elements(cols, dt):
+    rows = 2 * torch.cuda.get_device_properties(0).multi_processor_count + 5
+    dtype = torch.float32 if dt == "f32" else torch.bfloat16
+    x = _logits(rows, cols, dtype, seed=rows + cols)
+    y, lse = fa.softmax_rows(x)
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FA_OK
+    _check(x, y, lse, what=f"{rows}x{cols} {dt}")
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
