@@ -82,10 +82,14 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 /*
  * fa_fwd on HOST buffers, the copies included: Q, K, V go to the device, the
  * forward runs, O and LSE come back; returns once o and lse hold the result.
- * The (b, h) heads are cut into n_chunks groups of consecutive heads that pass
- * through three internal streams (host-to-device copies, kernels,
- * device-to-host copies), so one group's copies overlap another's kernel.
- * n_chunks <= 0 picks min(B*H, 8); larger values are clamped to min(B*H, 64).
+ * The (b, h) heads are cut into groups of consecutive heads that pass through
+ * internal streams (host-to-device copies; kernels, on two streams used in
+ * turn; device-to-host copies), so one group's copies overlap other groups'
+ * kernels.  n_chunks > 0: that many groups of equal size (clamped to
+ * min(B*H, 64)).  n_chunks <= 0: groups of a quarter of the heads, then
+ * halving toward the end (64 heads: 16, 16, 16, 8, 4, 2, 2) -- few large
+ * copies in, and a small last group, whose kernel and copy out nothing
+ * overlaps.  Every grouping gives the same bits as fa_fwd.
  *
  * q, k, v : in,  host bf16 [B][H][Nq|Nk][d]
  * o       : out, host bf16 [B][H][Nq][d]

@@ -374,21 +374,50 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 // fa_fwd_host: per-device device buffer and streams, held across calls.
 constexpr int kMaxHostChunks = 64;
+constexpr int kHostRunStreams = 2;  // kernel streams of the host pipeline, used in turn
 struct HostPipe {
   std::mutex mu;
   bool init = false;
   char* buf = nullptr;
   size_t cap = 0;
-  cudaStream_t s_in = nullptr, s_run = nullptr, s_out = nullptr;
+  cudaStream_t s_in = nullptr, s_run[kHostRunStreams] = {}, s_out = nullptr;
   cudaEvent_t in_done[kMaxHostChunks], run_done[kMaxHostChunks];
 };
+
+// Head groups of the host pipeline: n_chunks > 0 gives that many groups of
+// equal size (clamped to [1, min(BH, kMaxHostChunks)]); otherwise groups of
+// a quarter of the heads, then halving toward the end (64 heads: 16, 16, 16,
+// 8, 4, 2, 2), so the copies in run in few large transfers while the last
+// group -- whose kernel and copy out nothing overlaps -- is small.  Returns
+// the number of groups; sizes[g] heads in group g.
+int host_groups(int BH, int n_chunks, int* sizes) {
+  int n = 0;
+  if (n_chunks > 0) {
+    int chunks = std::min(std::min(n_chunks, BH), kMaxHostChunks);
+    const int per = (BH + chunks - 1) / chunks;
+    for (int h0 = 0; h0 < BH; h0 += per) sizes[n++] = std::min(per, BH - h0);
+    return n;
+  }
+  const int big = std::max(1, (BH + 3) / 4);
+  int rest = BH;
+  while (rest > 2 * big) sizes[n++] = big, rest -= big;
+  while (rest > 2) {
+    const int g = (rest + 1) / 2;
+    sizes[n++] = g;
+    rest -= g;
+  }
+  if (rest > 0) sizes[n++] = rest;
+  return n;
+}
 HostPipe g_pipe[kMaxDevices];
 
 int host_pipe_init(HostPipe& hp) {
   if (hp.init) return FA_OK;
   cudaError_t e = cudaSuccess;
-  for (cudaStream_t* st : {&hp.s_in, &hp.s_run, &hp.s_out})
+  for (cudaStream_t* st : {&hp.s_in, &hp.s_out})
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
+  for (cudaStream_t& st : hp.s_run)
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
   for (int c = 0; e == cudaSuccess && c < kMaxHostChunks; ++c) {
     e = cudaEventCreateWithFlags(&hp.in_done[c], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.run_done[c], cudaEventDisableTiming);
@@ -459,36 +488,35 @@ static int fwd_host_impl(const void* q, const void* k, const void* v, void* o, f
   const char* hv = static_cast<const char*>(v);
   char* ho = static_cast<char*>(o);
 
-  int chunks = n_chunks <= 0 ? (BH < 8 ? BH : 8) : n_chunks;
-  if (chunks > BH) chunks = BH;
-  if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;
-  const int per = (BH + chunks - 1) / chunks;
-  // Group c: heads [c per, min(BH, (c + 1) per)): copies in on s_in, the
-  // kernel on s_run after them, copies out on s_out after the kernel.  (A
-  // second copy-in stream gained nothing: one stream already fills the
+  int sizes[kMaxHostChunks];
+  const int groups = host_groups(BH, n_chunks, sizes);
+  // Group c: its heads' copies in on s_in, the kernel on s_run[c %
+  // kHostRunStreams] after them (kernel streams in turn, so a small group's
+  // kernel need not wait for the previous group's), copies out on s_out after
+  // the kernel.  (A second
+  // copy-in stream gained nothing: one stream already fills the
   // host-to-device link, about 205 GB/s on GB300.)
-  for (int c = 0; c < chunks && rc == FA_OK && e == cudaSuccess; ++c) {
-    const int h0 = c * per, nh = (BH - h0 < per) ? BH - h0 : per;
-    if (nh <= 0) break;
-    cudaStream_t si = hp.s_in;
+  for (int c = 0, h0 = 0; c < groups && rc == FA_OK && e == cudaSuccess; h0 += sizes[c++]) {
+    const int nh = sizes[c];
+    cudaStream_t si = hp.s_in, sr = hp.s_run[c % kHostRunStreams];
     e = cudaMemcpyAsync(dq + h0 * q_head, hq + h0 * q_head, nh * q_head, cudaMemcpyHostToDevice, si);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(dk + h0 * kv_head, hk + h0 * kv_head, nh * kv_head, cudaMemcpyHostToDevice, si);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(dv + h0 * kv_head, hv + h0 * kv_head, nh * kv_head, cudaMemcpyHostToDevice, si);
     if (e == cudaSuccess) e = cudaEventRecord(hp.in_done[c], si);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_run, hp.in_done[c], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(sr, hp.in_done[c], 0);
     if (e != cudaSuccess) break;
     if (fp8)
       rc = fa_fwd_fp8(dq + h0 * q_head, dk + h0 * kv_head, dv + h0 * kv_head, dout + h0 * o_head,
                       dl + static_cast<size_t>(h0) * Nq, 1, nh, Nq, Nk, d, scale, fp8[0], fp8[1], fp8[2],
-                      wr == 0 ? 1 : 0, hp.s_run);
+                      wr == 0 ? 1 : 0, sr);
     else
       rc = fwd_impl(dq + h0 * q_head, dk + h0 * kv_head, dv + h0 * kv_head, dout + h0 * o_head,
-                    dl + static_cast<size_t>(h0) * Nq, 1, nh, Nq, Nk, d, scale, wl, wr, 1,
-                    hp.s_run, nullptr, nullptr, nullptr, nullptr);
+                    dl + static_cast<size_t>(h0) * Nq, 1, nh, Nq, Nk, d, scale, wl, wr, 1, sr, nullptr,
+                    nullptr, nullptr, nullptr);
     if (rc != FA_OK) break;
-    e = cudaEventRecord(hp.run_done[c], hp.s_run);
+    e = cudaEventRecord(hp.run_done[c], sr);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_out, hp.run_done[c], 0);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(ho + h0 * o_head, dout + h0 * o_head, nh * o_head, cudaMemcpyDeviceToHost,
@@ -497,9 +525,13 @@ static int fwd_host_impl(const void* q, const void* k, const void* v, void* o, f
       e = cudaMemcpyAsync(lse + static_cast<size_t>(h0) * Nq, dl + static_cast<size_t>(h0) * Nq,
                           nh * lse_head, cudaMemcpyDeviceToHost, hp.s_out);
   }
-  // drain all three streams whatever happened above
+  // drain every stream whatever happened above
   cudaError_t es = cudaStreamSynchronize(hp.s_in);
-  cudaError_t er = cudaStreamSynchronize(hp.s_run);
+  cudaError_t er = cudaSuccess;
+  for (cudaStream_t st : hp.s_run) {
+    const cudaError_t x = cudaStreamSynchronize(st);
+    if (er == cudaSuccess) er = x;
+  }
   cudaError_t eo = cudaStreamSynchronize(hp.s_out);
   if (rc != FA_OK) return rc;
   if (e != cudaSuccess) return cuda_fail(e);
@@ -741,13 +773,11 @@ static int bwd_host_impl(const void* q, const void* k, const void* v, const void
                          static_cast<const char*>(dout), reinterpret_cast<const char*>(lse)};
   char* h_out[3] = {static_cast<char*>(dq), static_cast<char*>(dk), static_cast<char*>(dv)};
 
-  int chunks = n_chunks <= 0 ? (BH < 8 ? BH : 8) : n_chunks;
-  if (chunks > BH) chunks = BH;
-  if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;
-  const int per = (BH + chunks - 1) / chunks;
-  for (int c = 0; c < chunks && rc == FA_OK && e == cudaSuccess; ++c) {
-    const int h0 = c * per, nh = (BH - h0 < per) ? BH - h0 : per;
-    if (nh <= 0) break;
+  int sizes[kMaxHostChunks];
+  const int groups = host_groups(BH, n_chunks, sizes);
+  for (int c = 0, h0 = 0; c < groups && rc == FA_OK && e == cudaSuccess; h0 += sizes[c++]) {
+    const int nh = sizes[c];
+    cudaStream_t sr = hp.s_run[c % kHostRunStreams];
     char* d_in[6];
     char* d_out[3];
     for (int a = 0; a < 6; ++a) d_in[a] = hp.buf + off_in[a] + h0 * in_head[a];
@@ -756,20 +786,24 @@ static int bwd_host_impl(const void* q, const void* k, const void* v, const void
       e = cudaMemcpyAsync(d_in[a], h_in[a] + h0 * in_head[a], nh * in_head[a], cudaMemcpyHostToDevice,
                           hp.s_in);
     if (e == cudaSuccess) e = cudaEventRecord(hp.in_done[c], hp.s_in);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_run, hp.in_done[c], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(sr, hp.in_done[c], 0);
     if (e != cudaSuccess) break;
     rc = bwd_impl(d_in[0], d_in[1], d_in[2], d_in[3], reinterpret_cast<const float*>(d_in[5]), d_in[4],
-                  d_out[0], d_out[1], d_out[2], 1, nh, Nq, Nk, d, scale, wl, wr, hp.s_run);
+                  d_out[0], d_out[1], d_out[2], 1, nh, Nq, Nk, d, scale, wl, wr, sr);
     if (rc != FA_OK) break;
-    e = cudaEventRecord(hp.run_done[c], hp.s_run);
+    e = cudaEventRecord(hp.run_done[c], sr);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp.s_out, hp.run_done[c], 0);
     for (int a = 0; a < 3 && e == cudaSuccess; ++a)
       e = cudaMemcpyAsync(h_out[a] + h0 * out_head[a], d_out[a], nh * out_head[a], cudaMemcpyDeviceToHost,
                           hp.s_out);
   }
-  // drain all three streams whatever happened above
+  // drain every stream whatever happened above
   cudaError_t es = cudaStreamSynchronize(hp.s_in);
-  cudaError_t er = cudaStreamSynchronize(hp.s_run);
+  cudaError_t er = cudaSuccess;
+  for (cudaStream_t st : hp.s_run) {
+    const cudaError_t x = cudaStreamSynchronize(st);
+    if (er == cudaSuccess) er = x;
+  }
   cudaError_t eo = cudaStreamSynchronize(hp.s_out);
   if (rc != FA_OK) return rc;
   if (e != cudaSuccess) return cuda_fail(e);
