@@ -572,7 +572,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
       uint32_t g_par = 0;
       int last_t = -1, last_c = 0;
       int stag = 0;  // stagger phases waited for (tile 1)
-      bool ok = true, issued = false;
+      // debug build: this tile's TMEM columns lie inside the allocation
+      bool ok = FA_DCHECK(i < QT && (tmem & 0xFFFFu) + C::kTmemNeed <= 512u, p.status), issued = false;
       for (int r = 0; ok && r < rounds; ++r) {
         const int idx = item_of_round(r, p);
         if (idx < 0) continue;
@@ -815,7 +816,10 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
     int cs = 0;            // steps of this tile in earlier items (s_full, pv_ready, o_done phases)
     bool stg_pending = false;  // thread 0: a TMA store from the staging buffer may still read it
     uint32_t g_sp = 0;     // ring position of the item's first K tile: stage | parity << 8
-    for (int r = 0; r < rounds; ++r) {
+    // debug build: this tile's TMEM columns lie inside the allocation
+    const int my_rounds =
+        FA_DCHECK(i < QT && (tmem & 0xFFFFu) + C::kTmemNeed <= 512u, p.status) ? rounds : 0;
+    for (int r = 0; r < my_rounds; ++r) {
       const int idx = item_of_round(r, p);
       if (idx < 0) continue;
       // Only what the step loop needs stays live through it; the epilogue
