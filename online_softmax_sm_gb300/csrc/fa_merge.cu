@@ -11,8 +11,8 @@
 //   LSE = M + ln l;  a row with l = 0 gets O = 0 and LSE = -inf.
 // m_s is in natural-log units of the scaled logits.  HBM-bound: each row reads
 // n_splits * (d + 2) fp32 and writes d bf16 + one fp32.  d/8 lanes own a row,
-// eight consecutive columns each: two 16-byte loads per split, one 16-byte
-// store of bf16 O.
+// eight consecutive columns each: two 16-byte loads per split (four splits'
+// loads in flight at once), one 16-byte store of bf16 O.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -22,6 +22,7 @@ namespace fa {
 template <int D>
 __global__ void __launch_bounds__(256) fa_merge_kernel(const MergeParams p) {
   constexpr int kLanesPerRow = D / 8;
+  constexpr int kU = 4;  // splits whose loads are in flight together
   const long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long row = g / kLanesPerRow;
   const int part = static_cast<int>(g % kLanesPerRow);
@@ -35,24 +36,43 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const MergeParams p) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) acc[k] = 0.f;
   float lsum = 0.f;
+  // Splits in ascending order, as one sequence of FMAs; groups of kU splits
+  // issue all their loads before the first use, so each thread keeps 2 * kU
+  // 16-byte loads in flight instead of two.
+  auto fold = [&](float ms, float ls, const float4& a, const float4& b) {
+    if (ms == -INFINITY) return;  // an empty split adds nothing
+    const float w = ls * expf(ms - M);
+    lsum += w;
+    acc[0] = fmaf(w, a.x, acc[0]);
+    acc[1] = fmaf(w, a.y, acc[1]);
+    acc[2] = fmaf(w, a.z, acc[2]);
+    acc[3] = fmaf(w, a.w, acc[3]);
+    acc[4] = fmaf(w, b.x, acc[4]);
+    acc[5] = fmaf(w, b.y, acc[5]);
+    acc[6] = fmaf(w, b.z, acc[6]);
+    acc[7] = fmaf(w, b.w, acc[7]);
+  };
   if (M != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const long long idx = s * p.rows + row;
-      const float ms = __ldg(p.m_part + idx);
-      if (ms == -INFINITY) continue;
-      const float w = __ldg(p.l_part + idx) * expf(ms - M);
-      lsum += w;
+    int s = 0;
+    for (; s + kU <= S; s += kU) {
+      float ms[kU], ls[kU];
+      float4 a[kU], b[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const long long idx = static_cast<long long>(s + u) * p.rows + row;
+        ms[u] = __ldg(p.m_part + idx);
+        ls[u] = __ldg(p.l_part + idx);
+        const float4* src = reinterpret_cast<const float4*>(p.o_part + idx * D + part * 8);
+        a[u] = __ldg(src);
+        b[u] = __ldg(src + 1);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) fold(ms[u], ls[u], a[u], b[u]);
+    }
+    for (; s < S; ++s) {
+      const long long idx = static_cast<long long>(s) * p.rows + row;
       const float4* src = reinterpret_cast<const float4*>(p.o_part + idx * D + part * 8);
-      const float4 a = __ldg(src);
-      const float4 b = __ldg(src + 1);
-      acc[0] = fmaf(w, a.x, acc[0]);
-      acc[1] = fmaf(w, a.y, acc[1]);
-      acc[2] = fmaf(w, a.z, acc[2]);
-      acc[3] = fmaf(w, a.w, acc[3]);
-      acc[4] = fmaf(w, b.x, acc[4]);
-      acc[5] = fmaf(w, b.y, acc[5]);
-      acc[6] = fmaf(w, b.z, acc[6]);
-      acc[7] = fmaf(w, b.w, acc[7]);
+      fold(__ldg(p.m_part + idx), __ldg(p.l_part + idx), __ldg(src), __ldg(src + 1));
     }
   }
   const bool empty = !(lsum > 0.f);
