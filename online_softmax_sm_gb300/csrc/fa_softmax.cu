@@ -50,6 +50,9 @@ constexpr int kMaxCluster = 8;
 // row, and long rows stream that way when there is at least one row per
 // group.  Fewer rows share each row across a cluster of the ring kernel.
 constexpr long long kStreamCtasPerSm = 2;
+// The streaming kernel asks L2 for the next row's first sub-chunk only while
+// the rows in flight (one per group) take at most this much of L2.
+constexpr long long kStreamPrefetchL2Bytes = 96ll << 20;
 
 // CTAs per row for the streaming kernel: the group sizes that measured
 // fastest on GB300 for rows of 32K-2M elements.  Longer chunks per CTA keep
@@ -127,6 +130,14 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_smem(uint32_t addr, uint32_
                : "r"(addr), "r"(v)
                : "memory");
   return old;
+}
+
+// Global -> L2 only (no shared memory, no completion signal), `bytes` a
+// multiple of 16 from a 16-byte aligned address.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
+               "r"(bytes), "l"(policy)
+               : "memory");
 }
 
 // (m, l) <- (m, l) merged with (m2, l2): the two-block rule.  The pair with
@@ -585,6 +596,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1024 / (kWarps * 32))
   const int per_row = nsub > 0 ? 2 * nsub - 1 : 0;  // loads per row
   const long long my_rows = group < p.rows ? (p.rows - 1 - group) / groups + 1 : 0;
   const long long total = my_rows * per_row;
+  const bool pf_ok = groups * p.cols * static_cast<long long>(sizeof(T)) <= kStreamPrefetchL2Bytes;
   const T* __restrict__ xg = static_cast<const T*>(p.x);
   T* __restrict__ yg = static_cast<T*>(p.y);
   const uint32_t ring0 = smem_u32(ring);
@@ -755,6 +767,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1024 / (kWarps * 32))
 
     // ---- pass 2: y = exp(x - M) / L, the last sub-chunk from the registers
     // (exp(x - ref) * exp(ref - M) / L), the others reloaded
+    // While this CTA re-reads the row from L2, ask L2 for the first sub-chunk
+    // of its next row, so HBM stays busy and that row's first load hits L2 --
+    // unless the rows in flight already overflow L2 (one per group), or the
+    // chunk has fewer than three sub-chunks (measured slower either way).
+    if (warp == 0 && lane == 0 && it + 1 < my_rows && nsub >= 3 && pf_ok) {
+      const long long nrow = row + groups;
+      for (int sc = 0; sc < 1 && sc < nsub; ++sc) {
+        const int col = c0 + sc * kSub;
+        const uint32_t bytes = static_cast<uint32_t>(min(kSub, c1 - col)) * sizeof(T);
+        bulk_prefetch_l2(xg + nrow * p.cols + col, bytes,
+                         sc < nsub - 1 ? l2_policy_evict_last() : l2_policy_evict_first());
+      }
+    }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const float rM = (M == -INFINITY) ? 0.f : M;
     if (nsub > 0) {
@@ -765,7 +790,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1024 / (kWarps * 32))
         f2_unpack(fmul2(f2_pack(v[i], v[i + 1]), f2), v[i], v[i + 1]);
       store(yr, c0 + (nsub - 1) * kSub);
     }
-    const uint64_t nrM = f2_pack(-rM, -rM), inv2 = f2_pack(inv, inv);
+    // the reloaded sub-chunks: y = 2^((x - M) log2 e - log2 L), the division
+    // folded into the exponent.  L >= 1 (the row max contributes 1), so
+    // log2 L = e + log2 f with L = 2^e f, f in [1, 2): the exponent field plus
+    // lg2.approx on f (absolute error about 2^-22), and the rounded sum adds at
+    // most 2^-19 (|log2 L| <= 31) to the exponent's error.
+    float nl2L = -INFINITY;
+    if (L > 0.f) {
+      const uint32_t bits = __float_as_uint(L);
+      const float f = __uint_as_float((bits & 0x007FFFFFu) | 0x3F800000u);
+      nl2L = -(static_cast<float>(static_cast<int>(bits >> 23) - 127) + __log2f(f));
+    }
+    const uint64_t nrM = f2_pack(-rM, -rM), nl2 = f2_pack(nl2L, nl2L);
     for (int sc = 0; sc + 1 < nsub; ++sc) {
       if (!take(c0 + sc * kSub)) {
         failed = true;
@@ -774,8 +810,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1024 / (kWarps * 32))
 #pragma unroll
       for (int i = 0; i < kPer; i += 2) {
         float a, c;
-        f2_unpack(fmul2(fadd2(f2_pack(v[i], v[i + 1]), nrM), l2e), a, c);
-        f2_unpack(fmul2(f2_pack(ex2_approx(a), ex2_approx(c)), inv2), v[i], v[i + 1]);
+        f2_unpack(ffma2(fadd2(f2_pack(v[i], v[i + 1]), nrM), l2e, nl2), a, c);
+        v[i] = ex2_approx(a);
+        v[i + 1] = ex2_approx(c);
       }
       store(yr, c0 + sc * kSub);
     }
