@@ -46,6 +46,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxCluster = 8;
+constexpr int kMaxStreamGroup = 16;  // a non-portable cluster size, allowed per kernel
 // The streaming kernel runs two CTAs per SM; a group of CTAs shares each
 // row, and long rows stream that way when there is at least one row per
 // group.  Fewer rows share each row across a cluster of the ring kernel.
@@ -55,7 +56,7 @@ constexpr long long kStreamCtasPerSm = 2;
 constexpr long long kStreamPrefetchL2Bytes = 96ll << 20;
 
 // CTAs per row for the streaming kernel: the group sizes that measured
-// fastest on GB300 for rows of 32K-2M elements.  Longer chunks per CTA keep
+// fastest on GB300 for rows of 32K-4M elements.  Longer chunks per CTA keep
 // more rows in flight (more L2 misses between the passes, longer pipeline
 // fill per row); more CTAs per row pay more exchanges and smaller loads.
 template <typename T>
@@ -64,12 +65,13 @@ int stream_group(long long cols) {
     if (cols <= 20480) return 1;
     if (cols <= 40960) return 2;
     if (cols <= 131072) return 4;
-    return 8;
+    if (cols <= 524288) return 8;
+    return 16;
   }
   if (cols <= 65536) return 1;
   if (cols <= 262144) return 2;
   if (cols <= 524288) return 4;
-  return 8;
+  return 8;  // 16 measured slower for bf16 rows of 2M
 }
 
 template <typename T>
@@ -575,7 +577,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1024 / (kWarps * 32))
   // after every warp here has finished with row it.
   constexpr int kSlots = 4;
   static_assert(kStages >= 2 && kStages <= 3, "ring depth");
-  static_assert(kCta >= 1 && kCta <= kMaxCluster, "group size");
+  static_assert(kCta >= 1 && kCta <= kMaxStreamGroup, "group size");
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ __align__(8) uint64_t red[kSlots];        // all warps' pairs of a row are published
@@ -894,12 +896,16 @@ cudaError_t launch_stream(const SoftmaxParams& p, int num_sms, cudaStream_t s) {
   if (per_sm == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
+    if (kCta > kMaxCluster) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, kSmem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     cached.store(per_sm, std::memory_order_relaxed);
   }
-  static std::atomic<int> clusters[kMaxCluster + 1] = {};
+  static std::atomic<int> clusters[kCta + 1] = {};
   return launch_persistent(kern, kWarps * 32, kSmem, per_sm, clusters, p, num_sms, s);
 }
 
@@ -951,7 +957,8 @@ cudaError_t launch_typed(SoftmaxParams p, int num_sms, cudaStream_t s) {
         case 1: return launch_stream<T, 16, 4, 3, 1>(p, num_sms, s);
         case 2: return launch_stream<T, 16, 4, 3, 2>(p, num_sms, s);
         case 4: return launch_stream<T, 16, 4, 3, 4>(p, num_sms, s);
-        default: return launch_stream<T, 16, 4, 3, 8>(p, num_sms, s);
+        case 8: return launch_stream<T, 16, 4, 3, 8>(p, num_sms, s);
+        default: return launch_stream<T, 16, 4, 3, 16>(p, num_sms, s);
       }
     }
   }

@@ -104,6 +104,20 @@ def test_streaming_rows_all_elements(cols, dt):
     _check(x, y, lse, what=f"{rows}x{cols} {dt}")
 
 
+@pytest.mark.parametrize("cols,dt", [(600008, "f32"), (1200016, "bf16")], ids=["c600008_f32", "c1200016_bf16"])
+def test_streaming_very_long_rows_all_elements(cols, dt):
+    """Rows long enough for the largest groups: 16 CTAs for fp32 (a
+    non-portable cluster size), 8 for bf16; enough rows for every group of
+    the grid, every element checked."""
+    rows = 40
+    dtype = torch.float32 if dt == "f32" else torch.bfloat16
+    x = _logits(rows, cols, dtype, seed=cols)
+    y, lse = fa.softmax_rows(x)
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FA_OK
+    _check(x, y, lse, what=f"{rows}x{cols} {dt}")
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 def test_in_place_and_without_lse(dtype):
     x = _logits(40, 3000, dtype, seed=5)
