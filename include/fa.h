@@ -67,9 +67,12 @@ extern "C" {
  * n_splits  > 1: split-KV.  The key axis is cut into n_splits contiguous
  *   ranges of K/V tiles (clamped to the number of 128-key tiles); each range
  *   yields a partial (m, l, O) triple per row, combined by the two-block merge
- *   rule (see fa_merge_splits).  The fp32 workspace for the partials is taken
- *   with cudaMallocAsync on `stream` and released with cudaFreeAsync on the
- *   same stream (FA_ERR_NO_MEMORY if that fails).
+ *   rule (see fa_merge_splits).  The workspace for the partials (m and l in
+ *   fp32, O_s / l_s rounded to bf16: half the bytes of fa_fwd_partial's fp32
+ *   triples through HBM, written and read back) is taken with
+ *   cudaMallocAsync on `stream` and released with cudaFreeAsync on the same
+ *   stream (FA_ERR_NO_MEMORY if that fails).  The bf16 partials add at most
+ *   2^-8 max_s |O_s| to each element of O before its own bf16 rounding.
  *
  * q, k, v : in,  bf16 [B][H][Nq|Nk][d]
  * o       : out, bf16 [B][H][Nq][d]
@@ -249,8 +252,9 @@ int fa_fwd_partial(const void* q, const void* k, const void* v, float* m_part, f
 int fa_merge_splits(const float* m_part, const float* l_part, const float* o_part, void* o,
                     float* lse, int B, int H, int Nq, int d, int n_splits, void* stream);
 
-/* Bytes of fp32 workspace fa_fwd takes for split-KV with these sizes
- * (0 for n_splits <= 1 or invalid sizes). */
+/* Bytes of workspace fa_fwd takes for split-KV with these sizes: m and l
+ * fp32, O bf16, each block 256-byte aligned (0 for n_splits <= 1 or invalid
+ * sizes). */
 size_t fa_split_workspace_bytes(int B, int H, int Nq, int d, int n_splits);
 
 /*
@@ -280,12 +284,13 @@ const char* fa_strerror(int code);
  * split-KV workspace with cudaMallocAsync; this call puts the same partial
  * (m, l, O) triples in a fixed device array of FA_NOALLOC_SCRATCH_BYTES that
  * every GPU loading the library holds until the process exits, then merges
- * them as fa_fwd_partial + fa_merge_splits do.
+ * them with the same kernels.
  *
  * Arguments and results: as fa_fwd (q, k, v, o, lse, sizes, scale, causal,
  * stream), with 2 <= n_splits <= 65535, clamped to ceil(Nk/128) like fa_fwd;
  * if that leaves one split, the call is fa_fwd with n_splits = 1.
- * The workspace needs about n_splits * B*H*Nq * (d + 2) * 4 bytes; a call
+ * The workspace needs about n_splits * B*H*Nq * (2 d + 8) bytes
+ * (fa_split_workspace_bytes); a call
  * that needs more than FA_NOALLOC_SCRATCH_BYTES returns
  * FA_ERR_SCRATCH_TOO_SMALL before launching anything.
  *

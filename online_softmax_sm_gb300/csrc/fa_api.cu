@@ -243,6 +243,8 @@ cudaError_t launch_items(fa::FwdParams p, int qt, int bc, int d_bytes_per_row, i
   return cudaSuccess;
 }
 
+// fa_fwd's own split-KV workspace: m and l in fp32, O_s / l_s in bf16 (the
+// merge upcasts it exactly; fa_fwd_partial's public triples stay fp32).
 struct SplitLayout {
   size_t m_off, l_off, o_off, total;
 };
@@ -253,14 +255,15 @@ SplitLayout split_layout(long long rows, int d, int n_splits) {
   L.m_off = 0;
   L.l_off = ml;
   L.o_off = 2 * ml;
-  L.total = 2 * ml + align256(static_cast<size_t>(n_splits) * rows * d * sizeof(float));
+  L.total = 2 * ml + align256(static_cast<size_t>(n_splits) * rows * d * 2);
   return L;
 }
 
 // Shared body of fa_fwd / fa_fwd_ex / fa_fwd_partial.
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
              int Nk, int d, float scale, int wl, int wr, int n_splits, void* stream,
-             const fa_opts* opts, float* m_part, float* l_part, float* o_part) {
+             const fa_opts* opts, float* m_part, float* l_part, float* o_part,
+             void* split_ws = nullptr, size_t split_ws_bytes = 0) {
   const bool partial = (m_part != nullptr);
   int rc = check_sizes(B, H, Nq, Nk, d, scale);
   if (rc != FA_OK) return rc;
@@ -342,31 +345,36 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
   }
 
-  // split-KV: stream-ordered workspace, partial kernel, merge, release
+  // split-KV: workspace (stream-ordered, or the caller's), partial kernel,
+  // merge, release
   const SplitLayout L = split_layout(rows, d, splits);
-  void* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(&ws, L.total, s);
-  if (e != cudaSuccess) {
+  void* ws = split_ws;
+  cudaError_t e = cudaSuccess;
+  if (ws) {
+    if (split_ws_bytes < L.total) return FA_ERR_SCRATCH_TOO_SMALL;
+  } else if ((e = cudaMallocAsync(&ws, L.total, s)) != cudaSuccess) {
     t_last_cuda = e;
     return FA_ERR_NO_MEMORY;
   }
   char* base = static_cast<char*>(ws);
   p.m_part = reinterpret_cast<float*>(base + L.m_off);
   p.l_part = reinterpret_cast<float*>(base + L.l_off);
-  p.o_part = reinterpret_cast<float*>(base + L.o_off);
+  p.o_part = base + L.o_off;
+  p.part_bf16 = 1;
   e = run(p);
   if (e == cudaSuccess) {
     fa::MergeParams mp{};
     mp.m_part = p.m_part;
     mp.l_part = p.l_part;
     mp.o_part = p.o_part;
+    mp.o_part_bf16 = 1;
     mp.o = o;
     mp.lse = lse;
     mp.rows = rows;
     mp.n_splits = splits;
     e = fa::launch_merge(d, mp, s);
   }
-  cudaError_t ef = cudaFreeAsync(ws, s);
+  const cudaError_t ef = split_ws ? cudaSuccess : cudaFreeAsync(ws, s);
   if (e != cudaSuccess) return cuda_fail(e);
   if (ef != cudaSuccess) return cuda_fail(ef);
   return FA_OK;
@@ -428,6 +436,17 @@ int host_pipe_init(HostPipe& hp) {
 }
 
 }  // namespace
+
+namespace fa {
+// fa_fwd with n_splits > 1 and its workspace in the caller's device memory
+// (ws_bytes of it, FA_ERR_SCRATCH_TOO_SMALL if the split layout needs more).
+int fwd_split_into(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int Nq, int Nk, int d, float scale, int causal, int n_splits, void* stream,
+                   void* ws, size_t ws_bytes) {
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, -1, causal ? 0 : -1, n_splits, stream,
+                  nullptr, nullptr, nullptr, nullptr, ws, ws_bytes);
+}
+}  // namespace fa
 
 extern "C" {
 

@@ -1103,7 +1103,10 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
           p.m_part[prow] = empty ? -INFINITY : m * p.scale;
           p.l_part[prow] = empty ? 0.f : l;
         }
-        float* op = p.o_part + prow * D;
+        // O/l in fp32 (fa_fwd_partial), or rounded to bf16 (fa_fwd's own
+        // split workspace: half the bytes through HBM on both sides of the merge)
+        const bool bf = p.part_bf16 != 0;
+        uint8_t* op = static_cast<uint8_t*>(p.o_part) + prow * (D * (bf ? 2 : 4));
 #pragma unroll
         for (int cc = 0; cc < D; cc += 32) {
           uint32_t o[32];
@@ -1116,9 +1119,20 @@ __global__ void __launch_bounds__(FwdCfg<D, BC, QT, F8>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * inv);
           if (row < p.Nq) {
+            if (bf) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              st_global_v4(op + cc + 4 * q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+              for (int q = 0; q < 4; ++q) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  w[k] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * k]), __uint_as_float(o[8 * q + 2 * k + 1]));
+                st_global_v4(op + 2 * cc + 16 * q, w[0], w[1], w[2], w[3]);
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                st_global_v4(op + 4 * cc + 16 * q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            }
           }
         }
       }

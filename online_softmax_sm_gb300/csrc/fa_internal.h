@@ -50,7 +50,8 @@ struct FwdParams {
   int partial;
   float* m_part;  // natural-log units (scale * raw max), -inf if empty
   float* l_part;  // sum of exp(scale*s - m_part)
-  float* o_part;  // [.., d] fp32, O_split / l_split (0 if empty)
+  void* o_part;   // [.., d] O_split / l_split (0 if empty): fp32, or bf16 if part_bf16
+  int part_bf16;
   int Nq, Nk, BH;
   int n_splits;
   int tiles_per_split;  // K/V tiles per split
@@ -83,7 +84,8 @@ struct FwdParams {
 struct MergeParams {
   const float* m_part;
   const float* l_part;
-  const float* o_part;
+  const void* o_part;  // fp32, or bf16 if o_part_bf16
+  int o_part_bf16;
   void* o;     // bf16 [rows][d]
   float* lse;  // [rows]
   long long rows;  // B*H*Nq
@@ -103,6 +105,13 @@ cudaError_t launch_fwd_d128_bc128(int qt, const CUtensorMap* maps, const FwdPara
 cudaError_t launch_fwd_fp8_d128(int qt, const CUtensorMap* maps, const FwdParams& p, dim3 grid,
                                 cudaStream_t s);
 cudaError_t launch_merge(int d, const MergeParams& p, cudaStream_t s);
+
+// fa_fwd with n_splits > 1 and its split workspace in the caller's device
+// memory (fa_api.cu; used by the no-alloc entry point): same kernels and
+// layout as fa_fwd, so the same bits.
+int fwd_split_into(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int Nq, int Nk, int d, float scale, int causal, int n_splits, void* stream,
+                   void* ws, size_t ws_bytes);
 
 // Attention backward (fa_bwd_kernel.cuh).
 struct BwdParams {

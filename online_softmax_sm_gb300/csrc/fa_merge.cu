@@ -10,16 +10,17 @@
 //   O   = sum_s w_s O_s / l      (O_s already normalised by l_s)
 //   LSE = M + ln l;  a row with l = 0 gets O = 0 and LSE = -inf.
 // m_s is in natural-log units of the scaled logits.  HBM-bound: each row reads
-// n_splits * (d + 2) fp32 and writes d bf16 + one fp32.  d/8 lanes own a row,
-// eight consecutive columns each: two 16-byte loads per split (four splits'
-// loads in flight at once), one 16-byte store of bf16 O.
+// n_splits * (d + 2) fp32 (or n_splits * (2 fp32 + d bf16) when fa_fwd's own
+// workspace holds O_s in bf16) and writes d bf16 + one fp32.  d/8 lanes own a
+// row, eight consecutive columns each: two 16-byte loads per split (one for
+// bf16; four splits' loads in flight at once), one 16-byte store of bf16 O.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
 
 namespace fa {
 
-template <int D>
+template <int D, bool kBf16Part>
 __global__ void __launch_bounds__(256) fa_merge_kernel(const MergeParams p) {
   constexpr int kLanesPerRow = D / 8;
   constexpr int kU = 4;  // splits whose loads are in flight together
@@ -36,6 +37,22 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const MergeParams p) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) acc[k] = 0.f;
   float lsum = 0.f;
+  // this lane's eight columns of split row idx: two 16-byte fp32 loads, or
+  // one 16-byte load of bf16 (exact in fp32)
+  auto load_o = [&](long long idx, float4& a, float4& b) {
+    if constexpr (kBf16Part) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(
+          static_cast<const __nv_bfloat16*>(p.o_part) + idx * D + part * 8));
+      a = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                      __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+      b = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u),
+                      __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.o_part) + idx * D + part * 8);
+      a = __ldg(src);
+      b = __ldg(src + 1);
+    }
+  };
   // Splits in ascending order, as one sequence of FMAs; groups of kU splits
   // issue all their loads before the first use, so each thread keeps 2 * kU
   // 16-byte loads in flight instead of two.
@@ -62,17 +79,16 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const MergeParams p) {
         const long long idx = static_cast<long long>(s + u) * p.rows + row;
         ms[u] = __ldg(p.m_part + idx);
         ls[u] = __ldg(p.l_part + idx);
-        const float4* src = reinterpret_cast<const float4*>(p.o_part + idx * D + part * 8);
-        a[u] = __ldg(src);
-        b[u] = __ldg(src + 1);
+        load_o(idx, a[u], b[u]);
       }
 #pragma unroll
       for (int u = 0; u < kU; ++u) fold(ms[u], ls[u], a[u], b[u]);
     }
     for (; s < S; ++s) {
       const long long idx = static_cast<long long>(s) * p.rows + row;
-      const float4* src = reinterpret_cast<const float4*>(p.o_part + idx * D + part * 8);
-      fold(__ldg(p.m_part + idx), __ldg(p.l_part + idx), __ldg(src), __ldg(src + 1));
+      float4 a, b;
+      load_o(idx, a, b);
+      fold(__ldg(p.m_part + idx), __ldg(p.l_part + idx), a, b);
     }
   }
   const bool empty = !(lsum > 0.f);
@@ -94,10 +110,17 @@ cudaError_t launch_merge(int d, const MergeParams& p, cudaStream_t s) {
   const long long threads = p.rows * (d / 8);
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
   if (blocks == 0) return cudaSuccess;
-  if (d == 64)
-    fa_merge_kernel<64><<<blocks, 256, 0, s>>>(p);
-  else
-    fa_merge_kernel<128><<<blocks, 256, 0, s>>>(p);
+  if (d == 64) {
+    if (p.o_part_bf16)
+      fa_merge_kernel<64, true><<<blocks, 256, 0, s>>>(p);
+    else
+      fa_merge_kernel<64, false><<<blocks, 256, 0, s>>>(p);
+  } else {
+    if (p.o_part_bf16)
+      fa_merge_kernel<128, true><<<blocks, 256, 0, s>>>(p);
+    else
+      fa_merge_kernel<128, false><<<blocks, 256, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

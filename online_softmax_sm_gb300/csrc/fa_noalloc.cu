@@ -4,10 +4,10 @@
 // path that runs attention: runtimes without a device allocator, hosts that
 // have handed all device memory to their own pool, or latency-bound loops in
 // which an allocation could block or synchronise.  fa_fwd with n_splits > 1
-// takes its fp32 workspace with cudaMallocAsync, so it is unusable there.
-// This entry point runs the split-KV computation of fa_fwd_partial followed
-// by fa_merge_splits with the workspace in a fixed device array that lives as
-// long as the library is loaded.
+// takes its workspace with cudaMallocAsync, so it is unusable there.  This
+// entry point runs fa_fwd's own split-KV path (partial kernel, then merge)
+// with the workspace in a fixed device array that lives as long as the
+// library is loaded.
 #include <cstdint>
 #include <mutex>
 
@@ -56,19 +56,16 @@ extern "C" int fa_fwd_split_noalloc(const void* q, const void* k, const void* v,
   const int kv_tiles = (Nk + fa::kDefaultBc - 1) / fa::kDefaultBc;
   const int splits = n_splits < kv_tiles ? n_splits : kv_tiles;
   if (splits < 2) return fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, 1, stream);
+  // fa_fwd's split workspace layout: m, l fp32 and O_s in bf16, each 256-byte aligned
   const size_t rows = static_cast<size_t>(B) * H * Nq;
   const size_t ml = align256(static_cast<size_t>(splits) * rows * sizeof(float));
-  const size_t need = 2 * ml + align256(static_cast<size_t>(splits) * rows * d * sizeof(float));
+  const size_t need = 2 * ml + align256(static_cast<size_t>(splits) * rows * d * 2);
   if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH_TOO_SMALL;
   void* base = nullptr;
   int rc = scratch_address(&base);
   if (rc != FA_OK) return rc;
-  // Every entry the merge reads is written by fa_fwd_partial first (empty
+  // Every entry the merge reads is written by the partial kernel first (empty
   // splits write m = -inf, l = 0, O = 0), so nothing has to start at zero.
-  float* m_part = static_cast<float*>(base);
-  float* l_part = reinterpret_cast<float*>(static_cast<char*>(base) + ml);
-  float* o_part = reinterpret_cast<float*>(static_cast<char*>(base) + 2 * ml);
-  rc = fa_fwd_partial(q, k, v, m_part, l_part, o_part, B, H, Nq, Nk, d, scale, causal, splits, stream);
-  if (rc != FA_OK) return rc;
-  return fa_merge_splits(m_part, l_part, o_part, o, lse, B, H, Nq, d, splits, stream);
+  return fa::fwd_split_into(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, splits, stream, base,
+                            FA_NOALLOC_SCRATCH_BYTES);
 }
