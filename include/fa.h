@@ -50,7 +50,9 @@ extern "C" {
 
 #define FA_OK 0
 #define FA_ERR_INVALID_ARG (-1)    /* null/misaligned pointer, bad size, bad scale */
-#define FA_ERR_UNSUPPORTED (-2)    /* d not in {64,128}, or device is not sm_103 */
+#define FA_ERR_UNSUPPORTED (-2)    /* d not in {64,128}, device is not sm_103, or (from
+                                      fa_get_device_status) a shared memory base the
+                                      backward's layout cannot use */
 #define FA_ERR_CUDA (-3)           /* a CUDA call failed; fa_strerror() has details */
 #define FA_ERR_DEVICE_TIMEOUT (-4) /* a kernel wait ran out (fa_get_device_status) */
 #define FA_ERR_NO_MEMORY (-5)      /* the split-KV workspace could not be allocated */
@@ -261,7 +263,10 @@ size_t fa_split_workspace_bytes(int B, int H, int Nq, int d, int n_splits);
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT if any kernel of this library
  * recorded a timed-out wait since the last call, FA_ERR_DEVICE_CHECK (debug
- * build only) if a bounds check failed first, or FA_ERR_CUDA.  The word is
+ * build only) if a bounds check failed first, FA_ERR_UNSUPPORTED if a
+ * backward kernel found its dynamic shared memory base less than 1024-byte
+ * aligned (its layout fills the 227 KB limit and has no room to realign; it
+ * then writes nothing), or FA_ERR_CUDA.  The word is
  * one per device, shared by every call on that device (all streams, and the
  * host-buffer entry points, which read it before returning): a timeout from a
  * kernel on another stream is reported to whichever caller reads the word

@@ -896,6 +896,7 @@ int fa_get_device_status(void* stream) {
                   host[1]);
     return FA_ERR_DEVICE_CHECK;
   }
+  if (host[0] == fa::kDevLayout) return FA_ERR_UNSUPPORTED;
   return host[0] == fa::kDevTimeout ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
 }
 

@@ -12,18 +12,17 @@
 // Two kernels, no atomics (dQ would otherwise need fp32 reductions from every
 // key tile of a head):
 //   fa_bwd_dkdv_kernel  one 128-key tile per CTA, K_j and V_j in shared memory,
-//     looping over the query tiles that see it, each as two half-steps of 64
-//     queries.  S^T = K_j Q^T and dP^T = V_j dO^T of a half-step go to TMEM
-//     buffer b (two buffers of 64 + 64 columns, then dV and dK: 512 columns at
-//     d = 128); compute warpgroup b owns buffer b (queries [64b, 64b + 64) of
-//     every tile): thread t owns key t (TMEM lane t) and writes P^T and dS^T
-//     (bf16 pairs) back into the columns it has just read; dV_j += P^T dO and
-//     dK_j += dS^T Q then take them as the TMEM A operand.  P^T is released
-//     on its own, before dS^T is formed, so dV (and after it the next S^T of
-//     the buffer) overlaps the second half of the warpgroup's work.  The MMA warp issues
-//     dV, dK of half-step h, then S^T of h+2 once dV(h) is done and dP^T of h+2
-//     once dK(h) is done: each follows the previous MMA on the tensor pipe, and
-//     each warpgroup has two half-steps of MMA time for its exponentials.
+//     looping over the 128-query tiles that see it.  S^T = K_j Q^T (N = 128)
+//     goes to a TMEM buffer that is free again as soon as the compute threads
+//     have loaded it, so the next S^T overlaps this step's exponentials.
+//     dP^T = V_j dO^T is issued per query half h (N = 64) into buffer h;
+//     compute warpgroup h owns half h of every tile: thread t owns key t
+//     (TMEM lane t), keeps P^T in registers, and writes P^T and dS^T (bf16
+//     pairs) into the 64 buffer columns it has just read.  dV_j += P^T dO and
+//     dK_j += dS^T Q take them as the TMEM A operand half by half, and each
+//     half's buffer goes back to the next dP^T as soon as its dK is done, so
+//     the two halves hand off independently.  Q_i sits in a ring one slot
+//     deeper than dO_i's: it is read first (S^T) and released last (dK).
 //   fa_bwd_dq_kernel  one 128-row query tile per CTA, Q_i and dO_i in shared
 //     memory, looping over the key tiles it sees: S = Q_i K_j^T and
 //     dP = dO_i V_j^T, each released as soon as every row has read it, dS
@@ -57,19 +56,29 @@ struct BwdCfg {
   static constexpr int kChunkBytes = kRows * 128;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
   static constexpr int kVecBytes = kRows * 4;     // nlse2 or nd of one tile
-  static constexpr int kStages = D == 128 ? 2 : 4;
-  static constexpr int kStageBytesA = 2 * kTileBytes + 2 * kVecBytes;  // Q_i, dO_i, nlse2, nd
+  // dK/dV kernel: Q_i in a ring of kQSlots, dO_i (with the row vectors
+  // nlse2, nd) in a ring of kDoSlots.  A Q slot is needed first (S^T) and
+  // released last (dK), so its ring is one slot deeper: Q_{i+1} lands while
+  // step i - 1 still holds its slot.
+  static constexpr int kQSlots = D == 128 ? 3 : 4;
+  static constexpr int kDoSlots = D == 128 ? 2 : 4;
+  static constexpr int kVecSlotBytes = 2 * kVecBytes;  // nlse2, nd
   // dQ kernel: K_j and V_j in separate slots of a ring, K_j at position 2 j
   // and V_j at 2 j + 1; each slot is released by its own last reader.
   static constexpr int kSlotsFit = (227 * 1024 - 1024 - 2 * kTileBytes - 1024) / kTileBytes;
   static constexpr int kSlotsB = kSlotsFit > 8 ? 8 : kSlotsFit;
   static constexpr int kStageBytesB = kTileBytes;
   static constexpr int kCtlBytes = 1024;
-  static constexpr int kSmemA = 1024 + 2 * kTileBytes + kStages * kStageBytesA + kCtlBytes;
+  static constexpr int kCtlBytesA = 512;
+  // K_j, V_j, the Q ring, the dO ring, the row vectors, the barriers.  At
+  // d = 128 this leaves no room for padding: the dynamic shared memory base
+  // must itself be 1024-byte aligned (checked at kernel entry).
+  static constexpr int kSmemA = 2 * kTileBytes + kQSlots * kTileBytes + kDoSlots * kTileBytes +
+                                kDoSlots * kVecSlotBytes + kCtlBytesA;
   static constexpr int kSmemB = 1024 + 2 * kTileBytes + kSlotsB * kStageBytesB + kCtlBytes;
   static_assert(kSlotsB >= 4, "dQ kernel ring");
+  static_assert(kQSlots + kDoSlots <= 8, "dK/dV kernel barriers");
   static_assert(kSmemA <= 227 * 1024 && kSmemB <= 227 * 1024, "shared memory");
-  static_assert(kStageBytesA % 1024 == 0, "stage alignment");
   static constexpr int kThreads = 384;  // two compute warpgroups + load / MMA / alloc warps
   // Two MMA issuers: one for the products that fill S / dP, one for the
   // products that consume P / dS (dK/dV kernel: dV, dK; dQ kernel: dQ).
@@ -80,25 +89,25 @@ struct BwdCfg {
   static constexpr int kRegLaunchA = 168, kRegComputeA = 216, kRegOtherA = 72;
   static_assert(2 * kRegComputeA + kRegOtherA == 3 * kRegLaunchA, "setmaxnreg split");
   static constexpr int kTmemCols = 512;
-  // dK/dV kernel: S^T / P^T buffers at 64 b, dP^T / dS^T at 128 + 64 b, then
-  // the two accumulators.
+  // dK/dV kernel: S^T (fp32, 128 columns), the two dP^T half buffers (64
+  // columns each, later P^T and dS^T pairs), then the two accumulators.
   static constexpr int kS = 0, kDP = 128, kDV = 256, kDK = 256 + D;
   // dQ kernel: S, dP, two bf16 dS buffers of 64 columns, dQ.
   static constexpr int kDPq = 128, kDS0 = 256, kDQ = 384;
 };
 
-struct __align__(8) BwdCtl {
+struct __align__(8) BwdCtl {  // at most BwdCfg::kCtlBytesA bytes
   uint64_t fixed_full;  // K_j, V_j (dK/dV) or Q_i, dO_i (dQ) landed
   uint64_t full[8];     // ring stage / slot landed
   uint64_t empty[8];    // every MMA reading the stage / slot completed
-  uint64_t s_full[2];   // S(^T) of this step in TMEM (dK/dV: per buffer)
-  uint64_t s_free;      // dQ kernel: S read by all 256 compute threads
+  uint64_t s_full[2];   // S(^T) of this step in TMEM
+  uint64_t s_free;      // S(^T) read by all 256 compute threads
   uint64_t dp_free;     // dQ kernel: dP read by all 256 compute threads
-  uint64_t dp_full[2];  // dP(^T) in TMEM (buffer)
-  uint64_t ready[2];    // bf16 P^T (dK/dV kernel) or dS (dQ kernel) written back to TMEM
-  uint64_t ds_ready[2]; // dK/dV kernel: bf16 dS^T written back to TMEM
-  uint64_t done_a[2];   // dK/dV kernel: dV MMA of a buffer done (its S columns free)
-  uint64_t done_b[2];   // dK MMA of a buffer done (dP columns free) / dQ MMA of a buffer done
+  uint64_t dp_full[2];  // dP(^T) in TMEM (dK/dV kernel: per query half)
+  uint64_t ready[2];    // bf16 P^T (dK/dV kernel, per half) or dS (dQ kernel) written back to TMEM
+  uint64_t ds_ready[2]; // dK/dV kernel: bf16 dS^T of a half written back to TMEM
+  uint64_t done_a[2];   // unused
+  uint64_t done_b[2];   // dV and dK of a half done (its buffer free) / dQ MMA of a buffer done
   uint64_t drain;       // every MMA of the CTA completed
   uint32_t tmem_base;
   int abort;
@@ -164,13 +173,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_dk,
                        const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
   using C = BwdCfg<D>;
+  static_assert(sizeof(BwdCtl) <= C::kCtlBytesA, "barrier block");
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_s = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
-  uint8_t* sK = smem;
+  // The layout fills the shared memory limit, so it starts at the base
+  // itself: a base that is not 1024-byte aligned (the 128-byte swizzle
+  // atom) is reported and nothing runs.  The test is the same in every CTA.
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_status(p.status, kDevLayout);
+    return;
+  }
+  uint8_t* sK = smem_raw;
   uint8_t* sV = sK + C::kTileBytes;
-  uint8_t* sRing = sV + C::kTileBytes;  // stage: Q_i, dO_i, nlse2[128], nd[128]
-  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sRing + C::kStages * C::kStageBytesA);
+  uint8_t* sQr = sV + C::kTileBytes;                   // Q ring
+  uint8_t* sDOr = sQr + C::kQSlots * C::kTileBytes;    // dO ring
+  uint8_t* sVec = sDOr + C::kDoSlots * C::kTileBytes;  // per dO slot: nlse2[128], nd[128]
+  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sVec + C::kDoSlots * C::kVecSlotBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -186,30 +203,32 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const int n = qhi >= qlo ? qhi / C::kRows + 1 - i_lo : 0;
 
   const uint32_t bar_fixed = smem_u32(&ctl->fixed_full);
-  const uint32_t bar_full = smem_u32(&ctl->full[0]);
-  const uint32_t bar_empty = smem_u32(&ctl->empty[0]);
-  // per buffer b: + 8 b
+  // Q slot i: full / empty[i]; dO slot j: full / empty[kQSlots + j]
+  const uint32_t bar_qfull = smem_u32(&ctl->full[0]);
+  const uint32_t bar_qempty = smem_u32(&ctl->empty[0]);
+  const uint32_t bar_dofull = smem_u32(&ctl->full[C::kQSlots]);
+  const uint32_t bar_doempty = smem_u32(&ctl->empty[C::kQSlots]);
   const uint32_t bar_s = smem_u32(&ctl->s_full[0]);
+  const uint32_t bar_sfree = smem_u32(&ctl->s_free);
   const uint32_t bar_dp = smem_u32(&ctl->dp_full[0]);
   const uint32_t bar_ready = smem_u32(&ctl->ready[0]);
   const uint32_t bar_dsr = smem_u32(&ctl->ds_ready[0]);
-  const uint32_t bar_dv = smem_u32(&ctl->done_a[0]);
   const uint32_t bar_dk = smem_u32(&ctl->done_b[0]);
   const uint32_t bar_drain = smem_u32(&ctl->drain);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_fixed, 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+    for (int s = 0; s < C::kQSlots + C::kDoSlots; ++s) {
+      mbar_init(bar_qfull + 8 * s, 1);
+      mbar_init(bar_qempty + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_s + 8 * b, 1);
-      mbar_init(bar_dp + 8 * b, 1);
-      mbar_init(bar_ready + 8 * b, 128);
-      mbar_init(bar_dsr + 8 * b, 128);
-      mbar_init(bar_dv + 8 * b, 1);
-      mbar_init(bar_dk + 8 * b, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_sfree, 256);  // every compute thread has its S^T columns in registers
+    for (int h = 0; h < 2; ++h) {  // per query half h (dP^T buffer h, compute warpgroup h)
+      mbar_init(bar_dp + 8 * h, 1);
+      mbar_init(bar_ready + 8 * h, 128);  // the warpgroup's P^T pairs written
+      mbar_init(bar_dsr + 8 * h, 128);    // and its dS^T pairs
+      mbar_init(bar_dk + 8 * h, 1);       // dV and dK of the half done: buffer h free
     }
     mbar_init(bar_drain, 2);  // one commit per MMA issuer
     ctl->abort = 0;
@@ -240,117 +259,138 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
       }
       const uint64_t pol = l2_policy_evict_last();
+      // per barrier (Q slots, then dO slots): a copy was issued; its parity
       uint32_t issued_mask = 0, issued_par = 0;
       bool ok = true;
+      auto note = [&](int b, int use) {
+        issued_mask |= 1u << b;
+        issued_par = (issued_par & ~(1u << b)) | (static_cast<uint32_t>(use & 1) << b);
+      };
       for (int s = 0; ok && s < n; ++s) {
-        const int st = s % C::kStages, use = s / C::kStages;
-        if (use > 0 && !wait_bounded(bar_empty + 8 * st, (use - 1) & 1, wc)) {
+        const int q0 = (i_lo + s) * C::kRows;
+        // Q_s: its slot was last read by dK of step s - kQSlots
+        const int qs = s % C::kQSlots, qu = s / C::kQSlots;
+        if (qu > 0 && !wait_bounded(bar_qempty + 8 * qs, (qu - 1) & 1, wc)) {
           ok = false;
           break;
         }
-        const int q0 = (i_lo + s) * C::kRows;
-        uint8_t* base = sRing + st * C::kStageBytesA;
-        const uint32_t full = bar_full + 8 * st;
-        mbar_arrive_expect_tx(full, 2 * C::kTileBytes + 2 * C::kVecBytes);
+        const uint32_t qfull = bar_qfull + 8 * qs;
+        mbar_arrive_expect_tx(qfull, C::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(smem_u32(base + c * C::kChunkBytes), &tm_q, full, c * 64, q0, bh);
-          tma_load_3d(smem_u32(base + C::kTileBytes + c * C::kChunkBytes), &tm_do, full, c * 64, q0,
-                      bh);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem_u32(sQr + qs * C::kTileBytes + c * C::kChunkBytes), &tm_q, qfull, c * 64, q0, bh);
+        note(qs, qu);
+        // dO_s, nlse2, nd: the slot was last read in step s - kDoSlots
+        const int ds = s % C::kDoSlots, du = s / C::kDoSlots;
+        if (du > 0 && !wait_bounded(bar_doempty + 8 * ds, (du - 1) & 1, wc)) {
+          ok = false;
+          break;
         }
+        const uint32_t dfull = bar_dofull + 8 * ds;
+        mbar_arrive_expect_tx(dfull, C::kTileBytes + 2 * C::kVecBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem_u32(sDOr + ds * C::kTileBytes + c * C::kChunkBytes), &tm_do, dfull, c * 64, q0,
+                      bh);
         const size_t vrow = static_cast<size_t>(bh) * p.nq_pad + q0;
-        bulk_load(smem_u32(base + 2 * C::kTileBytes), p.nlse2 + vrow, C::kVecBytes, full, pol);
-        bulk_load(smem_u32(base + 2 * C::kTileBytes + C::kVecBytes), p.nd + vrow, C::kVecBytes,
-                  full, pol);
-        issued_mask |= 1u << st;
-        issued_par = (issued_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+        uint8_t* vec = sVec + ds * C::kVecSlotBytes;
+        bulk_load(smem_u32(vec), p.nlse2 + vrow, C::kVecBytes, dfull, pol);
+        bulk_load(smem_u32(vec + C::kVecBytes), p.nd + vrow, C::kVecBytes, dfull, pol);
+        note(C::kQSlots + ds, du);
       }
-      for (int s = 0; s < C::kStages; ++s)
-        if ((issued_mask >> s) & 1u) wait_own(bar_full + 8 * s, (issued_par >> s) & 1u, p.timeout_ns);
+      for (int b = 0; b < C::kQSlots + C::kDoSlots; ++b)
+        if ((issued_mask >> b) & 1u) wait_own(bar_qfull + 8 * b, (issued_par >> b) & 1u, p.timeout_ns);
       if (n > 0) wait_own(bar_fixed, 0, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == C::kMmaWarp || warp == C::kMmaWarp2) {
     // --------------------------------------------------------- MMA issuers
-    // Half-step hs = 2 s + b covers queries [64 b, 64 b + 64) of query tile
-    // s and uses TMEM buffer b.  Warp kMmaWarp2 fills buffers (S^T, dP^T);
-    // warp kMmaWarp consumes them (dV, dK).  Between the two only barriers:
-    // S^T of hs+2 once dV of hs has read P^T, dP^T once dK has read dS^T.
-    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false);  // A = K or V, B = Q or dO rows (K-major)
-    constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, true);  // B = dO or Q rows (MN-major)
-    const int nh = 2 * n;
-    auto stage_base = [&](int hs) {
-      return smem_u32(sRing + ((hs >> 1) % C::kStages) * C::kStageBytesA);
-    };
+    // Query tile s (128 queries) per step.  S^T = K_j Q_s^T (N = 128) has a
+    // TMEM buffer of its own, freed as soon as the compute threads have loaded
+    // it into registers, so S^T(s+1) runs while P(s) is formed.  dP^T is
+    // issued per query half h (N = 64) into buffer h, which compute
+    // warpgroup h turns into bf16 pairs in place: P^T pairs in its first 32
+    // columns, dS^T pairs in the next 32.  dV and dK then take the half's
+    // four K-slices from TMEM, and dP^T(s+1, h) waits only for those, so the
+    // two halves hand off independently.  Warp kMmaWarp2 issues S^T and dP^T,
+    // warp kMmaWarp issues dV and dK.
+    constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);  // A = K, B = Q (K-major)
+    constexpr uint32_t kIdescDP = idesc_bf16_f32(128, 64, false);  // A = V, B = 64 rows of dO
+    constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, true);   // B = dO or Q rows (MN-major)
+    auto q_base = [&](int s) { return smem_u32(sQr + (s % C::kQSlots) * C::kTileBytes); };
+    auto do_base = [&](int s) { return smem_u32(sDOr + (s % C::kDoSlots) * C::kTileBytes); };
+    // TMEM column of the P^T pairs of K-slice kk (16 queries, 8 columns):
+    // buffer kk / 4, 8 columns per slice; dS^T pairs 32 further
+    auto a_col = [](int kk) { return static_cast<uint32_t>(C::kDP + 64 * (kk >> 2) + 8 * (kk & 3)); };
     bool ok = n > 0 && warp_wait(bar_fixed, 0, wc);
     if (warp == C::kMmaWarp2) {
       const uint64_t dK = desc_kmajor<D>(smem_u32(sK));
       const uint64_t dV = desc_kmajor<D>(smem_u32(sV));
-      // S^T = K_j Q_h^T into buffer hs & 1 (Q_h: 64 rows, 8 KB into every chunk)
-      auto issue_s = [&](int hs) {
-        const uint64_t dQk = desc_kmajor<D>(stage_base(hs) + (hs & 1) * 64 * 128);
-        const uint32_t dst = tmem + C::kS + 64 * (hs & 1);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss_elect(dst, dK + kslice_kmajor<D>(kk), dQk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
-        mma_commit_elect(bar_s + 8 * (hs & 1));
-      };
-      auto issue_dp = [&](int hs) {  // dP^T = V_j dO_h^T
-        const uint64_t dOk = desc_kmajor<D>(stage_base(hs) + C::kTileBytes + (hs & 1) * 64 * 128);
-        const uint32_t dst = tmem + C::kDP + 64 * (hs & 1);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss_elect(dst, dV + kslice_kmajor<D>(kk), dOk + kslice_kmajor<D>(kk), kIdescS, kk > 0);
-        mma_commit_elect(bar_dp + 8 * (hs & 1));
-      };
-      if (ok) ok = warp_wait(bar_full, 0, wc);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
-        issue_s(1);
-        issue_dp(1);
-      }
-      for (int hs = 0; ok && hs + 2 < nh; ++hs) {
-        const int b = hs & 1, nx = hs + 2;
-        const uint32_t par = static_cast<uint32_t>((hs >> 1) & 1);
-        if (b == 0) ok = warp_wait(bar_full + 8 * ((nx >> 1) % C::kStages), ((nx >> 1) / C::kStages) & 1, wc);
-        ok = ok && warp_wait(bar_dv + 8 * b, par, wc);
+      for (int s = 0; ok && s < n; ++s) {
+        const uint32_t par = static_cast<uint32_t>((s - 1) & 1);
+        ok = warp_wait(bar_qfull + 8 * (s % C::kQSlots), (s / C::kQSlots) & 1, wc) &&
+             (s == 0 || warp_wait(bar_sfree, par, wc));
         if (!ok) break;
         tc_fence_after();
-        issue_s(nx);
-        ok = warp_wait(bar_dk + 8 * b, par, wc);
-        if (!ok) break;
-        tc_fence_after();
-        issue_dp(nx);
+        const uint64_t dQk = desc_kmajor<D>(q_base(s));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)  // S^T = K_j Q_s^T
+          mma_bf16_ss_elect(tmem + C::kS, dK + kslice_kmajor<D>(kk), dQk + kslice_kmajor<D>(kk), kIdescS,
+                            kk > 0);
+        mma_commit_elect(bar_s);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if ((s > 0 && !warp_wait(bar_dk + 8 * h, par, wc)) ||
+              (h == 0 && !warp_wait(bar_dofull + 8 * (s % C::kDoSlots), (s / C::kDoSlots) & 1, wc))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // rows [64 h, 64 h + 64) of dO_s: 64 rows of 128 bytes into each chunk
+          const uint64_t dOk = desc_kmajor<D>(do_base(s) + 64 * 128 * h);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)  // dP^T (half h) = V_j dO_s,h^T
+            mma_bf16_ss_elect(tmem + C::kDP + 64 * h, dV + kslice_kmajor<D>(kk), dOk + kslice_kmajor<D>(kk),
+                              kIdescDP, kk > 0);
+          mma_commit_elect(bar_dp + 8 * h);
+        }
       }
     } else {
-      for (int hs = 0; ok && hs < nh; ++hs) {
-        const int b = hs & 1;
-        ok = warp_wait(bar_ready + 8 * b, static_cast<uint32_t>((hs >> 1) & 1), wc);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t base = stage_base(hs);
-        const uint64_t dOmn = desc_mnmajor<D>(base + C::kTileBytes);
-        const uint64_t dQmn = desc_mnmajor<D>(base);
-        const uint32_t pa = tmem + C::kS + 64 * b, da = tmem + C::kDP + 64 * b;
+      for (int s = 0; ok && s < n; ++s) {
+        const uint32_t par = static_cast<uint32_t>(s & 1);
+        const uint64_t dOmn = desc_mnmajor<D>(do_base(s));
+        const uint64_t dQmn = desc_mnmajor<D>(q_base(s));
+        // half by half: dV once its P^T is written, dK once its dS^T is, then
+        // the half's buffer goes back to dP^T(s+1, h) while the other half
+        // is still being formed
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // dV += P^T dO_h (K = 64 queries: rows 64 b + 16 kk)
-          mma_bf16_ts_elect(tmem + C::kDV, pa + 8 * kk, dOmn + kslice_mnmajor(4 * b + kk), kIdescAcc,
-                            (hs > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_elect(bar_dv + 8 * b);
-        ok = warp_wait(bar_dsr + 8 * b, static_cast<uint32_t>((hs >> 1) & 1), wc);
-        if (!ok) break;
-        tc_fence_after();
+        for (int h = 0; h < 2; ++h) {
+          if (!warp_wait(bar_ready + 8 * h, par, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q_h
-          mma_bf16_ts_elect(tmem + C::kDK, da + 8 * kk, dQmn + kslice_mnmajor(4 * b + kk), kIdescAcc,
-                            (hs > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_elect(bar_dk + 8 * b);
-        // both halves of the tile done: S^T / dP^T (the other warp) completed
-        // before their P^T / dS^T were written back, so this commit covers
-        // every read of the stage
-        if (b == 1) mma_commit_elect(bar_empty + 8 * ((hs >> 1) % C::kStages));
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)  // dV += P^T dO_s (rows 16 kk)
+            mma_bf16_ts_elect(tmem + C::kDV, tmem + a_col(kk), dOmn + kslice_mnmajor(kk), kIdescAcc,
+                              (s > 0 || kk > 0) ? 1u : 0u);
+          if (!warp_wait(bar_dsr + 8 * h, par, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)  // dK += dS^T Q_s
+            mma_bf16_ts_elect(tmem + C::kDK, tmem + a_col(kk) + 32, dQmn + kslice_mnmajor(kk), kIdescAcc,
+                              (s > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_elect(bar_dk + 8 * h);  // buffer h read by dV and dK
+        }
+        if (!ok) break;
+        // S^T and dP^T of the step completed before P^T / dS^T were written
+        // back, and the compute warps read nlse2 / nd before that: after dK
+        // of both halves, nothing reads the step's Q or dO slot again
+        mma_commit_elect(bar_qempty + 8 * (s % C::kQSlots));
+        mma_commit_elect(bar_doempty + 8 * (s % C::kDoSlots));
       }
     }
     // everything issued completes before the epilogue reads TMEM / TMEM is freed
@@ -361,30 +401,32 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   } else {
     setmaxnreg_inc<C::kRegComputeA>();
     // ------------------------------------------------ compute warpgroups
-    const int h = warp >> 2;               // buffer / query half of every tile
+    const int h = warp >> 2;               // query half of every tile
     const int t = (warp & 3) * 32 + lane;  // key row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int key = key0 + t;
     const float c = p.scale_log2;
+    // this warpgroup's 64 columns of S^T and of dP^T
     const uint32_t tS = tmem + lane_off + C::kS + 64 * h;
     const uint32_t tDP = tmem + lane_off + C::kDP + 64 * h;
     bool ok = true;
     for (int s = 0; ok && s < n; ++s) {
-      const int st = s % C::kStages;
-      const int q0 = (i_lo + s) * C::kRows + 64 * h;  // this half's first query
-      const float* nlv = reinterpret_cast<const float*>(sRing + st * C::kStageBytesA + 2 * C::kTileBytes) + 64 * h;
+      const int ds = s % C::kDoSlots;
+      const int qt0 = (i_lo + s) * C::kRows;   // the tile's first query
+      const int q0 = qt0 + 64 * h;             // this half's first query
+      const float* nlv = reinterpret_cast<const float*>(sVec + ds * C::kVecSlotBytes) + 64 * h;
       const float* ndv = nlv + C::kRows;
-      // P^T first, from S^T alone, so dV += P^T dO (and S^T of half-step
-      // h + 2 after it) can start while dS^T is still being formed.  The
-      // stage's own barrier makes the bulk-copied nlse2 / nd visible here.
-      ok = warp_wait(bar_full + 8 * st, (s / C::kStages) & 1, wc) && warp_wait(bar_s + 8 * h, s & 1, wc);
+      // The dO slot's barrier makes the bulk-copied nlse2 / nd visible here.
+      ok = warp_wait(bar_dofull + 8 * ds, (s / C::kDoSlots) & 1, wc) && warp_wait(bar_s, s & 1, wc);
       if (!ok) break;
       tc_fence_after();
-      const bool all_vis = bwd_tile_all_visible(q0, key0, p);  // (a superset test: 128 queries)
+      const bool all_vis = bwd_tile_all_visible(qt0, key0, p);  // the whole 128 x 128 tile pair
       float pv[64];
       {
         uint32_t srow[64];
         tmem_ld64_sync(tS, srow);
+        tc_fence_before();
+        mbar_arrive(bar_sfree);  // S^T(s+1) may overwrite the buffer now
         const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
         for (int k = 0; k < 64; k += 4) {  // 2^(S c - LSE log2 e), two lanes per FMA
@@ -407,24 +449,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int k = 0; k < 64; ++k)
           if (!bwd_visible(q0 + k, key, p)) pv[k] = 0.f;
       }
-      {
-        uint32_t pk[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) pk[k] = pack_bf16x2(pv[2 * k], pv[2 * k + 1]);
-        tmem_st32(tS, pk);  // pairs into columns already read: [0, 32)
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_ready + 8 * h);
-      // dS^T = P^T (dP^T - D) once dP^T has landed
+      // dP^T(s) of this half in buffer h: load it, then P^T pairs into the
+      // first 32 of the columns just read (dV starts on them), then
+      // dS^T = P^T (dP^T - D) into the next 32
       if (!warp_wait(bar_dp + 8 * h, s & 1, wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      uint32_t drow[64];
+      tmem_ld64_sync(tDP, drow);
       {
-        uint32_t drow[64];
-        tmem_ld64_sync(tDP, drow);
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pk[k] = pack_bf16x2(pv[2 * k], pv[2 * k + 1]);
+        tmem_st32(tDP, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_ready + 8 * h);
+      {
         uint32_t dk[32];
 #pragma unroll
         for (int k = 0; k < 64; k += 4) {  // P (dP - D), two lanes per add / multiply
@@ -439,7 +483,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           dk[k >> 1] = pack_bf16x2(y0, y1);
           dk[(k >> 1) + 1] = pack_bf16x2(y2, y3);
         }
-        tmem_st32(tDP, dk);
+        tmem_st32(tDP + 32, dk);
       }
       tmem_wait_st();
       tc_fence_before();
