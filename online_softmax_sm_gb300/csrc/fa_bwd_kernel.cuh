@@ -63,11 +63,11 @@ struct BwdCfg {
   static constexpr int kQSlots = D == 128 ? 3 : 4;
   static constexpr int kDoSlots = D == 128 ? 2 : 4;
   static constexpr int kVecSlotBytes = 2 * kVecBytes;  // nlse2, nd
-  // dQ kernel: K_j and V_j in separate slots of a ring, K_j at position 2 j
-  // and V_j at 2 j + 1; each slot is released by its own last reader.
-  static constexpr int kSlotsFit = (227 * 1024 - 1024 - 2 * kTileBytes - 1024) / kTileBytes;
-  static constexpr int kSlotsB = kSlotsFit > 8 ? 8 : kSlotsFit;
-  static constexpr int kStageBytesB = kTileBytes;
+  // dQ kernel: K_j in a ring of kKSlots, V_j in a ring of kVSlots.  K_j is
+  // read first (S) and released last (dQ), V_j only by dP, so the K ring is
+  // the deeper one and a V load never waits for a dQ.
+  static constexpr int kKSlots = D == 128 ? 3 : 4;
+  static constexpr int kVSlots = D == 128 ? 2 : 4;
   static constexpr int kCtlBytes = 1024;
   static constexpr int kCtlBytesA = 512;
   // K_j, V_j, the Q ring, the dO ring, the row vectors, the barriers.  At
@@ -75,8 +75,8 @@ struct BwdCfg {
   // must itself be 1024-byte aligned (checked at kernel entry).
   static constexpr int kSmemA = 2 * kTileBytes + kQSlots * kTileBytes + kDoSlots * kTileBytes +
                                 kDoSlots * kVecSlotBytes + kCtlBytesA;
-  static constexpr int kSmemB = 1024 + 2 * kTileBytes + kSlotsB * kStageBytesB + kCtlBytes;
-  static_assert(kSlotsB >= 4, "dQ kernel ring");
+  static constexpr int kSmemB = 1024 + 2 * kTileBytes + (kKSlots + kVSlots) * kTileBytes + kCtlBytes;
+  static_assert(kKSlots + kVSlots <= 8, "dQ kernel barriers");
   static_assert(kQSlots + kDoSlots <= 8, "dK/dV kernel barriers");
   static_assert(kSmemA <= 227 * 1024 && kSmemB <= 227 * 1024, "shared memory");
   static constexpr int kThreads = 384;  // two compute warpgroups + load / MMA / alloc warps
@@ -552,8 +552,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint8_t* sQ = smem;
   uint8_t* sDO = sQ + C::kTileBytes;
-  uint8_t* sRing = sDO + C::kTileBytes;  // slots: K_j at position 2 j, V_j at 2 j + 1
-  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sRing + C::kSlotsB * C::kStageBytesB);
+  uint8_t* sKr = sDO + C::kTileBytes;                // K ring
+  uint8_t* sVr = sKr + C::kKSlots * C::kTileBytes;   // V ring
+  BwdCtl* ctl = reinterpret_cast<BwdCtl*>(sVr + C::kVSlots * C::kTileBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -569,8 +570,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const int n = khi >= klo ? khi / C::kRows + 1 - j_lo : 0;
 
   const uint32_t bar_fixed = smem_u32(&ctl->fixed_full);
-  const uint32_t bar_full = smem_u32(&ctl->full[0]);
-  const uint32_t bar_empty = smem_u32(&ctl->empty[0]);
+  // K slot i: full / empty[i]; V slot i: full / empty[kKSlots + i]
+  const uint32_t bar_kfull = smem_u32(&ctl->full[0]);
+  const uint32_t bar_kempty = smem_u32(&ctl->empty[0]);
+  const uint32_t bar_vfull = smem_u32(&ctl->full[C::kKSlots]);
+  const uint32_t bar_vempty = smem_u32(&ctl->empty[C::kKSlots]);
   const uint32_t bar_s = smem_u32(&ctl->s_full[0]);
   const uint32_t bar_sfree = smem_u32(&ctl->s_free);
   const uint32_t bar_dp = smem_u32(&ctl->dp_full[0]);
@@ -581,9 +585,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_fixed, 1);
-    for (int s = 0; s < C::kSlotsB; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+    for (int s = 0; s < C::kKSlots + C::kVSlots; ++s) {
+      mbar_init(bar_kfull + 8 * s, 1);
+      mbar_init(bar_kempty + 8 * s, 1);
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_sfree, 256);
@@ -618,23 +622,32 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           tma_load_3d(smem_u32(sDO + c * C::kChunkBytes), &tm_do, bar_fixed, c * 64, q0, bh);
         }
       }
+      // per barrier (K slots, then V slots): a copy was issued; its parity
       uint32_t issued_mask = 0, issued_par = 0;
-      for (int pos = 0; pos < 2 * n; ++pos) {
-        const int sl = pos % C::kSlotsB, use = pos / C::kSlotsB;
-        if (use > 0 && !wait_bounded(bar_empty + 8 * sl, (use - 1) & 1, wc)) break;
-        const int k0 = (j_lo + (pos >> 1)) * C::kRows;
-        uint8_t* base = sRing + sl * C::kStageBytesB;
-        const uint32_t full = bar_full + 8 * sl;
-        const CUtensorMap* map = (pos & 1) ? &tm_v : &tm_k;
-        mbar_arrive_expect_tx(full, C::kTileBytes);
+      for (int j = 0; j < n; ++j) {
+        const int k0 = (j_lo + j) * C::kRows;
+        const int ks = j % C::kKSlots, ku = j / C::kKSlots;  // K_j: slot last read by dQ(j - kKSlots)
+        if (ku > 0 && !wait_bounded(bar_kempty + 8 * ks, (ku - 1) & 1, wc)) break;
+        const uint32_t kfull = bar_kfull + 8 * ks;
+        mbar_arrive_expect_tx(kfull, C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem_u32(base + c * C::kChunkBytes), map, full, c * 64, k0, bh);
-        issued_mask |= 1u << sl;
-        issued_par = (issued_par & ~(1u << sl)) | (static_cast<uint32_t>(use & 1) << sl);
+          tma_load_3d(smem_u32(sKr + ks * C::kTileBytes + c * C::kChunkBytes), &tm_k, kfull, c * 64, k0, bh);
+        issued_mask |= 1u << ks;
+        issued_par = (issued_par & ~(1u << ks)) | (static_cast<uint32_t>(ku & 1) << ks);
+        const int vs = j % C::kVSlots, vu = j / C::kVSlots;  // V_j: slot last read by dP(j - kVSlots)
+        if (vu > 0 && !wait_bounded(bar_vempty + 8 * vs, (vu - 1) & 1, wc)) break;
+        const uint32_t vfull = bar_vfull + 8 * vs;
+        mbar_arrive_expect_tx(vfull, C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem_u32(sVr + vs * C::kTileBytes + c * C::kChunkBytes), &tm_v, vfull, c * 64, k0, bh);
+        const int vb = C::kKSlots + vs;
+        issued_mask |= 1u << vb;
+        issued_par = (issued_par & ~(1u << vb)) | (static_cast<uint32_t>(vu & 1) << vb);
       }
-      for (int s = 0; s < C::kSlotsB; ++s)
-        if ((issued_mask >> s) & 1u) wait_own(bar_full + 8 * s, (issued_par >> s) & 1u, p.timeout_ns);
+      for (int s = 0; s < C::kKSlots + C::kVSlots; ++s)
+        if ((issued_mask >> s) & 1u) wait_own(bar_kfull + 8 * s, (issued_par >> s) & 1u, p.timeout_ns);
       if (n > 0) wait_own(bar_fixed, 0, p.timeout_ns);
     }
     __syncwarp();
@@ -645,37 +658,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     // Warp kMmaWarp2: dQ += dS(j) K_j once dS(j) is in its TMEM buffer j & 1.
     constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
     constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, D, true);  // B = K_j (MN-major)
-    auto slot = [&](int pos) { return smem_u32(sRing + (pos % C::kSlotsB) * C::kStageBytesB); };
-    auto slot_full = [&](int pos) {
-      return warp_wait(bar_full + 8 * (pos % C::kSlotsB), (pos / C::kSlotsB) & 1, wc);
-    };
+    auto k_slot = [&](int j) { return smem_u32(sKr + (j % C::kKSlots) * C::kTileBytes); };
+    auto v_slot = [&](int j) { return smem_u32(sVr + (j % C::kVSlots) * C::kTileBytes); };
     bool ok = n > 0 && warp_wait(bar_fixed, 0, wc);
     if (warp == C::kMmaWarp) {
       const uint64_t dQk = desc_kmajor<D>(smem_u32(sQ));
       const uint64_t dOk = desc_kmajor<D>(smem_u32(sDO));
       for (int j = 0; ok && j < n; ++j) {
-        ok = slot_full(2 * j) && (j == 0 || warp_wait(bar_sfree, (j - 1) & 1, wc));
+        ok = warp_wait(bar_kfull + 8 * (j % C::kKSlots), (j / C::kKSlots) & 1, wc) &&
+             (j == 0 || warp_wait(bar_sfree, (j - 1) & 1, wc));
         if (!ok) break;
         tc_fence_after();
         {
-          const uint64_t dKk = desc_kmajor<D>(slot(2 * j));
+          const uint64_t dKk = desc_kmajor<D>(k_slot(j));
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_bf16_ss_elect(tmem + C::kS, dQk + kslice_kmajor<D>(kk), dKk + kslice_kmajor<D>(kk),
                               kIdescS, kk > 0);
           mma_commit_elect(bar_s);
         }
-        ok = slot_full(2 * j + 1) && (j == 0 || warp_wait(bar_dpfree, (j - 1) & 1, wc));
+        ok = warp_wait(bar_vfull + 8 * (j % C::kVSlots), (j / C::kVSlots) & 1, wc) &&
+             (j == 0 || warp_wait(bar_dpfree, (j - 1) & 1, wc));
         if (!ok) break;
         tc_fence_after();
         {
-          const uint64_t dVk = desc_kmajor<D>(slot(2 * j + 1));
+          const uint64_t dVk = desc_kmajor<D>(v_slot(j));
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_bf16_ss_elect(tmem + C::kDPq, dOk + kslice_kmajor<D>(kk), dVk + kslice_kmajor<D>(kk),
                               kIdescS, kk > 0);
           mma_commit_elect(bar_dp);
-          mma_commit_elect(bar_empty + 8 * ((2 * j + 1) % C::kSlotsB));  // V_j read
+          mma_commit_elect(bar_vempty + 8 * (j % C::kVSlots));  // V_j read
         }
       }
     } else {
@@ -683,7 +696,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         ok = warp_wait(bar_ready + 8 * (j & 1), (j >> 1) & 1, wc);  // dS(j) written back
         if (!ok) break;
         tc_fence_after();
-        const uint64_t dKmn = desc_mnmajor<D>(slot(2 * j));
+        const uint64_t dKmn = desc_mnmajor<D>(k_slot(j));
         const uint32_t src = tmem + C::kDS0 + 64 * (j & 1);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j (K = 128 keys, 8 columns per K-step)
@@ -691,7 +704,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                             (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit_elect(bar_dq + 8 * (j & 1));
         // K_j: S(j) (the other warp) completed before dS(j) could exist
-        mma_commit_elect(bar_empty + 8 * ((2 * j) % C::kSlotsB));
+        mma_commit_elect(bar_kempty + 8 * (j % C::kKSlots));
       }
     }
     mma_commit_elect(bar_drain);
