@@ -98,7 +98,7 @@ FWD_SOURCES = ["fa_fwd_kernel.cuh", "fa_fwd_d64_bc64.cu", "fa_fwd_d64_bc128.cu",
                "fa_internal.h"]
 SOFTMAX_SOURCES = ["fa_softmax.cu", "fa_ptx.cuh", "fa_wait.cuh", "fa_internal.h"]
 BWD_SOURCES = ["fa_bwd_kernel.cuh", "fa_bwd_d64.cu", "fa_bwd_d128.cu", "fa_ptx.cuh", "fa_wait.cuh",
-               "fa_internal.h"]
+               "fa_internal.h", "fa_status.h"]
 
 
 def kernel_source_hash(files=None) -> str:

@@ -9,6 +9,7 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "fa_status.h"
 
 namespace {
 

@@ -44,6 +44,7 @@
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
+#include "fa_status.h"
 #include "fa_wait.cuh"
 
 namespace fa {

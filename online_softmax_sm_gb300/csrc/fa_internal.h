@@ -15,7 +15,6 @@ enum : int {
   kDevOk = 0,
   kDevTimeout = 1,  // a bounded mbarrier wait ran out; the CTA stopped cleanly
   kDevCheck = 2,    // debug build (FA_DEBUG): a bounds check failed; the access was skipped
-  kDevLayout = 3,   // a kernel's shared memory base was not aligned as its layout needs; it did nothing
 };
 // The status word is the first of two ints per device; the second holds the
 // source line of the first failed debug-build check.
