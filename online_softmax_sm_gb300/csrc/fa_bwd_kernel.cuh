@@ -24,7 +24,8 @@
 //     the two halves hand off independently.  Q_i sits in a ring one slot
 //     deeper than dO_i's: it is read first (S^T) and released last (dK).
 //   fa_bwd_dq_kernel  one 128-row query tile per CTA, Q_i and dO_i in shared
-//     memory, looping over the key tiles it sees: S = Q_i K_j^T and
+//     memory, looping over the key tiles it sees (K_j and V_j in rings of
+//     their own: K_j is released by dQ, V_j already by dP): S = Q_i K_j^T and
 //     dP = dO_i V_j^T, each released as soon as every row has read it, dS
 //     (bf16) into one of two TMEM buffers of its own, and dQ_i += dS K_j.
 //   S and dP are recomputed by both: 7 MMAs per tile pair instead of 5.
@@ -107,7 +108,6 @@ struct __align__(8) BwdCtl {  // at most BwdCfg::kCtlBytesA bytes
   uint64_t dp_full[2];  // dP(^T) in TMEM (dK/dV kernel: per query half)
   uint64_t ready[2];    // bf16 P^T (dK/dV kernel, per half) or dS (dQ kernel) written back to TMEM
   uint64_t ds_ready[2]; // dK/dV kernel: bf16 dS^T of a half written back to TMEM
-  uint64_t done_a[2];   // unused
   uint64_t done_b[2];   // dV and dK of a half done (its buffer free) / dQ MMA of a buffer done
   uint64_t drain;       // every MMA of the CTA completed
   uint32_t tmem_base;
