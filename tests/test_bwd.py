@@ -101,6 +101,10 @@ CASES = [
     (1, 1, 130, 700, 128, (-1, 0)),    # decode-like, ragged
     (1, 1, 512, 512, 128, (100, 0)),   # sliding window
     (1, 2, 257, 400, 64, (30, 40)),    # two-sided window, ragged
+    # d = 64 with more 128-row tiles than any ring has slots (four each), so
+    # every Q, dO, K and V slot is reused
+    (1, 1, 700, 650, 64, (-1, -1)),
+    (1, 1, 640, 767, 64, (-1, 0)),
 ]
 
 
